@@ -1,0 +1,46 @@
+"""Pixel mask -> latent mask, in float64 (test infrastructure; see ``oracle/__init__``).
+
+[SAMPLING] "inpaint 与 mask": the mask is reshaped, interpolated and broadcast to
+the latent batch and channels.  Reading: bilinear interpolation with half-pixel
+centres (the align_corners=False convention): destination pixel j samples the
+source at (j + 1/2) * (in / out) - 1/2, clamped below at 0; the two
+neighbouring source pixels on each axis are weighted by the fractional part,
+the upper neighbour clamped to the last pixel.  Channel broadcast happens in
+the step itself.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def _axis(n_in: int, n_out: int):
+    """Per destination index: (lower source index, upper source index, upper weight)."""
+    scale = n_in / n_out
+    lo = np.empty(n_out, dtype=np.int64)
+    hi = np.empty(n_out, dtype=np.int64)
+    lam = np.empty(n_out, dtype=np.float64)
+    for j in range(n_out):
+        src = max((j + 0.5) * scale - 0.5, 0.0)
+        i0 = min(int(math.floor(src)), n_in - 1)
+        lo[j] = i0
+        hi[j] = min(i0 + 1, n_in - 1)
+        lam[j] = src - i0
+    return lo, hi, lam
+
+
+def bilinear_resize(mask, H: int, W: int) -> np.ndarray:
+    """[B, 1, Hp, Wp] -> [B, 1, H, W] float64."""
+    m = np.asarray(mask, dtype=np.float64)
+    B, one, Hp, Wp = m.shape
+    if one != 1:
+        raise ValueError("mask must have one channel")
+    ylo, yhi, ly = _axis(Hp, H)
+    xlo, xhi, lx = _axis(Wp, W)
+    ly = ly[:, None]
+    lx = lx[None, :]
+    top = (1.0 - lx) * m[:, :, ylo][:, :, :, xlo] + lx * m[:, :, ylo][:, :, :, xhi]
+    bot = (1.0 - lx) * m[:, :, yhi][:, :, :, xlo] + lx * m[:, :, yhi][:, :, :, xhi]
+    return (1.0 - ly) * top + ly * bot
