@@ -1,0 +1,547 @@
+#!/usr/bin/env python
+"""Benchmark of the fused guided denoise step; rank 0 prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--pdl]
+
+A step is one call of gs_guided_step: the whole per-step path (per-sample
+parameters, regional accumulation, guidance combine, inpaint blend, Euler
+update) over one batch.  Inputs are seeded synthetic tensors resident in HBM
+before timing starts; R input sets whose total exceeds 4x the L2 cache rotate
+from step to step, so every step reads from DRAM.  The K timed steps are
+replayed from CUDA graphs and timed with CUDA events on the launching stream,
+bracketed by a barrier and device synchronisation, max over ranks.
+
+Other keys of the JSON line:
+* e2e: the same metric when every step copies its inputs from pinned host
+  memory and reads x_out back (copies inside the timed region).
+* roofline: algorithmic bytes per launch (``accounting.step_bytes``) over the
+  measured launch time, against the measured HBM copy peak.
+* cpu_baseline: the float64 oracle on a bounded sample of the workload, timed
+  on the host (rank 0 at N = 1 only).
+* clocks: nvidia-smi samples taken while the GPU runs the step.
+
+--impl reference times the oracle (the CPU restatement the kernel is checked
+against) on the same workload, metric and unit.
+
+With N > 1 every rank runs its own batch of the workload on its own GPU (the
+step is independent per sample and needs no exchange), so the job's throughput
+is the sum over ranks: weak scaling.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "guided-step latent Gelem/s and HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "Gelem/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# Per-launch DRAM traffic (read + write bytes) of the step kernel from one ncu
+# capture, with the SHA-256 prefix of the kernel source it was taken on.  A
+# different source hash means the counters are stale: traffic is reported null.
+TRAFFIC = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bcg_bf16_b16")
+    ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-seconds", type=float, default=1.5)
+    return ap.parse_args()
+
+
+def kernel_source_hash() -> str:
+    p = os.path.join(ROOT, "bucketized_guidance_step_gb300", "csrc", "guided_step.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file.read().splitlines() if ln.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def build_sets(wl, R, dev, seed=0):
+    """R rotating input sets on the device, plus the shared per-run state."""
+    import torch
+
+    from bucketized_guidance_step_gb300 import gs
+    from bucketized_guidance_step_gb300.workloads import DTYPES, step_inputs
+
+    dt = DTYPES[wl.dtype]
+    s = wl.schedule
+    sig_np, _ = gs.sigmas(s.kind, s.steps, sigma_min=s.sigma_min, sigma_max=s.sigma_max,
+                          rho=s.rho, denoise=s.denoise, start_step=s.start_step,
+                          last_step=s.last_step, force_full_denoise=s.force_full_denoise)
+    steps = len(sig_np) - 1
+    sig = torch.from_numpy(sig_np).to(dev)
+    lut = None
+    if wl.guidance.cfg is None:
+        g = wl.guidance
+        _, lut_np = gs.bucket_plan(steps, g.num_buckets, curve=g.curve, v0=g.v0, v1=g.v1,
+                                   edge=g.edge)
+        lut = torch.from_numpy(lut_np).to(dev)
+    # geometry (rectangles, strengths, pixel masks) from the seeded generator, once
+    proto = step_inputs(wl, 0, B=1)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    shape = (wl.B, wl.C, wl.H, wl.W)
+
+    def randn(shp):
+        return torch.randn(shp, generator=gen, device=dev, dtype=torch.float32).to(dt)
+
+    sets = []
+    for k in range(R):
+        st = {}
+        st["x"] = randn(shape)
+        if wl.full_frame_cond:
+            st["stacked"] = randn((2 * wl.B,) + shape[1:])
+        else:
+            st["uncond"] = randn(shape)
+        st["regions"] = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather,
+                                   randn((wl.B, wl.C, r.h, r.pitch)))
+                         for r in proto.regions]
+        if wl.inpaint:
+            nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
+            Hp, Wp = wl.pixel_mask_hw
+            from bucketized_guidance_step_gb300.workloads import pixel_mask
+            pm = pixel_mask(wl.B, Hp, Wp, wl.mask_rects, 1000 + k).to(dev)
+            st["mask"] = gs.mask_prepare(pm, wl.H, wl.W)
+            del pm
+            st["orig"] = randn(shape)
+            if nm < wl.B:
+                pres = torch.zeros(wl.B, dtype=torch.uint8, device=dev)
+                pres[:nm] = 1
+                st["present"] = pres
+        if wl.staggered:
+            st["idx"] = torch.randint(0, steps, (wl.B,), generator=gen, device=dev,
+                                      dtype=torch.int32)
+        sets.append(st)
+    torch.cuda.synchronize(dev)
+    return sets, sig, lut, steps
+
+
+def step_kwargs(wl, st, sig, lut, pdl):
+    kw = dict(sigmas=sig, regions=st["regions"], pdl=pdl)
+    if "stacked" in st:
+        kw["stacked"] = st["stacked"]
+    else:
+        kw["uncond"] = st["uncond"]
+    if "idx" in st:
+        kw["step_idx"] = st["idx"]
+    else:
+        kw["step"] = 0
+    if lut is not None:
+        kw["scale_lut"] = lut
+    else:
+        kw["cfg"] = wl.guidance.cfg
+    if "mask" in st:
+        kw.update(inpaint_mask=st["mask"], original=st["orig"], mask_present=st.get("present"))
+    return kw
+
+
+def set_bytes(wl, st) -> int:
+    return sum(t.numel() * t.element_size() for k, t in st.items()
+               if k not in ("regions",)) + sum(r.out.numel() * r.out.element_size()
+                                               for r in st["regions"])
+
+
+def algorithmic_bytes(wl, proto_regions) -> int:
+    from bucketized_guidance_step_gb300.accounting import step_bytes
+    nm = 0
+    if wl.inpaint:
+        nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
+    return step_bytes(wl.B, wl.C, wl.H, wl.W, wl.dtype, uncond=True, cond=wl.full_frame_cond,
+                      regions=[(r.h, r.w) for r in proto_regions], inpaint_samples=nm)
+
+
+def capture(launches, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for fn in launches:
+            fn()
+    return g
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from bucketized_guidance_step_gb300 import gs
+    from bucketized_guidance_step_gb300.workloads import workload
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    gs.load()
+    wl = workload(args.workload)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+
+    one, sig, lut, steps = build_sets(wl, 1, dev, seed=1234 + rank)
+    per_set = set_bytes(wl, one[0])
+    R = max(2, math.ceil(4 * l2 / per_set))
+    del one
+    sets, sig, lut, steps = build_sets(wl, R, dev, seed=1234 + rank)
+    prepared = []
+    for st in sets:
+        a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, args.pdl))
+        prepared.append((a, keep))
+
+    def launcher(a):
+        return lambda: gs.launch_step(a)
+
+    stream = torch.cuda.Stream(dev)
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for k in range(W):                                  # untimed warm-up steps
+            gs.launch_step(prepared[k % R][0])
+        torch.cuda.synchronize(dev)
+        g_full = capture([launcher(a) for a, _ in prepared], stream)
+        rem = K % R
+        g_rem = capture([launcher(prepared[k][0]) for k in range(rem)], stream) if rem else None
+        g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        torch.cuda.synchronize(dev)
+
+        clocks = ClockSampler(local)
+        clocks.start()
+        t_end = time.time() + args.soak_seconds             # load the GPU while clocks settle
+        while time.time() < t_end:
+            g_full.replay()
+            torch.cuda.synchronize(dev)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(K // R):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+        clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    ms_max = ms
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # --- end to end: pinned host buffers in, result out, every step ---------
+    e2e = run_e2e(args, wl, sets[0], sig, lut, stream, dev, pg)
+
+    from bucketized_guidance_step_gb300.workloads import step_inputs
+    proto = step_inputs(wl, 0, B=1)
+    abytes = algorithmic_bytes(wl, proto.regions)
+    elems = wl.elements
+    sec_step = ms_max / 1e3 / K
+    value = world * elems / sec_step / 1e9
+    achieved = abytes / (ms / 1e3 / K) / 1e9
+    peak, peak_src = hbm_peak()
+    tr = TRAFFIC.get(wl.name)
+    traffic = tr[0] if tr and tr[1] == kernel_source_hash() else None
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": describe(wl), "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W,
+                   "l2": f"{R} rotating input sets of {per_set} B (>= 4x L2 of {l2} B)",
+                   "launch": "CUDA graph replay" + (", PDL" if args.pdl else ""),
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "hbm_gbs": round(world * achieved, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": abytes, "peak_source": peak_src},
+        "e2e": e2e,
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, wl, st, sig, lut, stream, dev, pg):
+    """Pinned host inputs -> device -> step -> host result, every step, in a graph."""
+    import torch
+
+    from bucketized_guidance_step_gb300 import gs
+
+    host = {}
+    for k in ("x", "stacked", "uncond", "orig", "idx"):
+        if k in st:
+            host[k] = torch.empty_like(st[k], device="cpu").pin_memory()
+            host[k].copy_(st[k])
+    regions_h = [r.out.to("cpu").pin_memory() for r in st["regions"]]
+    out_h = torch.empty_like(st["x"], device="cpu").pin_memory()
+    a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, False))
+
+    def one_step():
+        for k, h in host.items():
+            st[k].copy_(h, non_blocking=True)
+        for r, h in zip(st["regions"], regions_h):
+            r.out.copy_(h, non_blocking=True)
+        gs.launch_step(a)
+        out_h.copy_(st["x"], non_blocking=True)
+
+    h2d = sum(h.numel() * h.element_size() for h in host.values()) + \
+        sum(h.numel() * h.element_size() for h in regions_h)
+    d2h = out_h.numel() * out_h.element_size()
+    E = max(1, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one_step()
+        torch.cuda.synchronize(dev)
+        g = capture([one_step] * E, stream)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(end)
+    world = 1
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+        world = pg.get_world_size()
+    value = world * wl.elements / (ms / 1e3 / E) / 1e9
+    return {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": E,
+            "path": "pinned host -> cudaMemcpyAsync -> gs_guided_step -> host, CUDA graph"}
+
+
+def describe(wl) -> str:
+    s, g = wl.schedule, wl.guidance
+    parts = [f"{wl.name}: B={wl.B} {wl.C}x{wl.H}x{wl.W} {wl.dtype}",
+             f"{s.kind} {s.steps} steps" + (f" denoise {s.denoise}" if s.denoise < 1 else "")
+             + (" force_full_denoise" if s.force_full_denoise else "")]
+    parts.append(f"cfg {g.cfg}" if g.cfg is not None else
+                 f"{g.num_buckets} buckets {g.curve} {g.v0}->{g.v1}")
+    if wl.full_frame_cond:
+        parts.append("stacked [uncond_0..B-1, cond_0..B-1]")
+    if wl.n_regions:
+        parts.append(f"{wl.n_regions} regions feather {wl.feather}")
+    if wl.inpaint:
+        parts.append("inpaint mask+original" +
+                     (f" on {wl.inpaint_samples} samples" if wl.inpaint_samples else ""))
+    parts.append("per-sample step index" if wl.staggered else "shared step")
+    return ", ".join(parts)
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(wl, n_samples: int, seed: int = 0):
+    """Inputs for the oracle on the first n_samples of the workload (host numpy)."""
+    import numpy as np
+    import torch
+
+    from bucketized_guidance_step_gb300.workloads import step_inputs
+    from oracle import buckets as OB
+    from oracle import mask as OM
+    from oracle import schedules as OS
+    from oracle import step as O
+
+    s, g = wl.schedule, wl.guidance
+    sig, _ = OS.sigmas(OS.KARRAS if s.kind == "karras" else OS.NORMAL, s.steps,
+                       sigma_min=s.sigma_min, sigma_max=s.sigma_max, rho=s.rho,
+                       denoise=s.denoise, start_step=s.start_step, last_step=s.last_step,
+                       force_full_denoise=s.force_full_denoise)
+    sig = sig.astype(np.float32)
+    lut = None
+    if g.cfg is None:
+        c = OB.linear_curve(g.v0, g.v1) if g.curve == "linear" else OB.step_curve(g.v0, g.v1,
+                                                                                  g.edge)
+        _, lut = OB.plan(len(sig) - 1, g.num_buckets, OB.bucket_table(c, g.num_buckets))
+    inp = step_inputs(wl, seed, B=n_samples)
+
+    def f64(t):
+        return None if t is None else t.to(torch.float64).numpy()
+
+    idx = (inp.step_idx.numpy() if inp.step_idx is not None
+           else np.zeros(n_samples, dtype=np.int64))
+    x = sig[idx].astype(np.float64).reshape(-1, 1, 1, 1) * f64(inp.noise)
+    regs = [O.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, f64(r.out)) for r in inp.regions]
+    lat = None if inp.pixel_mask is None else OM.bilinear_resize(inp.pixel_mask.numpy(),
+                                                                 wl.H, wl.W)
+    kw = dict(uncond=f64(inp.uncond), cond=f64(inp.cond), scale_lut=lut,
+              cfg=g.cfg if g.cfg is not None else 1.0, regions=regs, inpaint_mask=lat,
+              mask_present=None if inp.mask_present is None else inp.mask_present.numpy(),
+              original=f64(inp.original))
+    return x, sig, idx, kw
+
+
+def cpu_baseline(wl, seconds: float):
+    from oracle import step as O
+    n_s = 1
+    x, sig, idx, kw = oracle_sample(wl, n_s)
+    elems = x.size
+    O.guided_step(x, sig, idx, **kw)                        # warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        O.guided_step(x, sig, idx, **kw)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"value": round(reps * elems / dt / 1e9, 6), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n_s} of {wl.B} samples ({elems} elements) of {wl.name}, "
+                      f"{reps} oracle steps in {dt:.1f} s, float64 NumPy, one thread"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from bucketized_guidance_step_gb300.workloads import workload
+    from oracle import step as O
+    wl = workload(args.workload)
+    n_s = 1
+    x, sig, idx, kw = oracle_sample(wl, n_s)
+    elems = x.size
+    for _ in range(max(3, args.warmup if args.warmup < 20 else 20)):
+        O.guided_step(x, sig, idx, **kw)
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        O.guided_step(x, sig, idx, **kw)
+    dt = time.perf_counter() - t0
+    value = K * elems / dt / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": describe(wl), "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W,
+                   "sample": f"each step runs {n_s} of the {wl.B} samples"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n_s} of {wl.B} samples ({elems} elements) per step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,72 @@
+// Latent inpaint mask from a pixel mask: gs_mask_prepare (sm_103a).
+//
+// [SAMPLING] "12 · 采样器、调度器与 CFG", section "inpaint 与 mask": the mask is
+// reshaped and interpolated to the latent's size and broadcast over the batch and
+// channels.  The interpolation is bilinear with half-pixel centres
+// (align_corners = False).  It runs once per sampling run, so the index and
+// weight arithmetic is done in binary64 per output pixel (exact for the
+// power-of-two ratios of latent encoders) and only the result is rounded to fp32.
+//
+// One thread per output pixel; consecutive threads take consecutive columns.
+// For an 8x downsample each output reads two neighbouring pixels of two source
+// rows, so a warp's loads cover two contiguous 1 KiB row spans.
+#include <cuda_runtime.h>
+
+#include "gs.h"
+
+namespace {
+
+struct AxisTap {
+    int lo, hi;
+    double frac;
+};
+
+__device__ __forceinline__ AxisTap axis_tap(int j, int n_in, int n_out) {
+    const double scale = static_cast<double>(n_in) / static_cast<double>(n_out);
+    double src = (static_cast<double>(j) + 0.5) * scale - 0.5;
+    if (src < 0.0) src = 0.0;
+    int lo = static_cast<int>(floor(src));
+    if (lo > n_in - 1) lo = n_in - 1;
+    AxisTap t;
+    t.lo = lo;
+    t.hi = lo + 1 < n_in ? lo + 1 : n_in - 1;
+    t.frac = src - static_cast<double>(lo);
+    return t;
+}
+
+__global__ void __launch_bounds__(256) mask_prepare_kernel(const float* __restrict__ src, int Hp,
+                                                           int Wp, float* __restrict__ dst, int H,
+                                                           int W, long long total) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int x = static_cast<int>(i % W);
+    const long long t = i / W;
+    const int y = static_cast<int>(t % H);
+    const long long b = t / H;
+    const AxisTap ty = axis_tap(y, Hp, H);
+    const AxisTap tx = axis_tap(x, Wp, W);
+    const float* s = src + b * Hp * static_cast<long long>(Wp);
+    const double a00 = __ldg(s + static_cast<long long>(ty.lo) * Wp + tx.lo);
+    const double a01 = __ldg(s + static_cast<long long>(ty.lo) * Wp + tx.hi);
+    const double a10 = __ldg(s + static_cast<long long>(ty.hi) * Wp + tx.lo);
+    const double a11 = __ldg(s + static_cast<long long>(ty.hi) * Wp + tx.hi);
+    const double top = (1.0 - tx.frac) * a00 + tx.frac * a01;
+    const double bottom = (1.0 - tx.frac) * a10 + tx.frac * a11;
+    dst[i] = static_cast<float>((1.0 - ty.frac) * top + ty.frac * bottom);
+}
+
+}  // namespace
+
+extern "C" gs_status gs_mask_prepare(const float* pix_mask, int32_t B, int32_t Hp, int32_t Wp,
+                                     float* lat_mask, int32_t H, int32_t W, gs_stream stream) {
+    if (pix_mask == nullptr || lat_mask == nullptr) return GS_ERR_INVALID_ARG;
+    if (B < 1 || Hp < 1 || Wp < 1 || H < 1 || W < 1) return GS_ERR_INVALID_ARG;
+    const long long total = static_cast<long long>(B) * H * W;
+    const long long blocks = (total + 255) / 256;
+    if (blocks > 0x7fffffffll) return GS_ERR_UNSUPPORTED;
+    mask_prepare_kernel<<<static_cast<unsigned int>(blocks), 256, 0,
+                          reinterpret_cast<cudaStream_t>(stream)>>>(pix_mask, Hp, Wp, lat_mask, H,
+                                                                    W, total);
+    if (cudaGetLastError() != cudaSuccess) return GS_ERR_CUDA;
+    return GS_OK;
+}

@@ -1,0 +1,298 @@
+/*
+ * gs.h -- C ABI of the fused guided denoise step for GB300 (sm_103a).
+ *
+ * One sampler step of a diffusion model, after the model has produced its
+ * outputs for the step: regional conditioning accumulation, classifier-free
+ * guidance with a scalar or bucketized per-sample scale, inpaint blend with the
+ * original latent and the Euler update to the next sigma -- all in one kernel
+ * launch.  Host helpers build the sigma schedule and the bucket plan once per
+ * run, and a small kernel prepares the latent inpaint mask once per run.
+ *
+ * Sources (page title, section):
+ *   [SAMPLING] "12 · 采样器、调度器与 CFG" -- ComfyUI's sampler / scheduler / CFG notes.
+ *   [BCG]      the write-up on Bucketized Continuous Guidance in SGLang
+ *              (zwxr.cn news 258547), sections 2-4.
+ *
+ * Conventions for every entry point:
+ *   - The caller owns every buffer.  The library allocates nothing, keeps no
+ *     pointer after a call returns and never synchronises the stream.
+ *   - Device work is enqueued on the caller's stream (a cudaStream_t passed as
+ *     gs_stream; NULL is the legacy default stream).
+ *   - Errors are returned as gs_status; nothing is launched when an argument
+ *     check fails.  No call aborts, throws or traps.  Errors found on the device
+ *     (they depend on device-resident step indices) are OR-ed into an optional
+ *     caller-owned status word; gs_status_from_word() decodes it.
+ *   - Layouts are dense row-major (NCHW) unless a stride is given.
+ */
+#ifndef GS_H
+#define GS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL = the legacy default stream. */
+typedef struct CUstream_st* gs_stream;
+
+typedef enum gs_status {
+    GS_OK = 0,
+    GS_ERR_INVALID_ARG = 1,   /* a pointer, size, rectangle or option is invalid      */
+    GS_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve                */
+    GS_ERR_CUDA = 3,          /* the CUDA runtime reported an error (launch, device)  */
+    GS_ERR_STEP_RANGE = 4,    /* device: a step index did not address sigma[i], sigma[i+1]
+                                 (or the scale table); that sample was skipped        */
+    GS_ERR_NEED_UNCOND = 5,   /* device: a sample's scale was not 1 but no uncond
+                                 branch was given; that sample was skipped            */
+    GS_ERR_SIGMA = 6,         /* device: sigma[i] <= 0 or not finite; sample skipped */
+    GS_ERR_CAPACITY = 7       /* output buffer too small                              */
+} gs_status;
+
+/* Bits of the device status word (uint32, caller-owned, zeroed by the caller). */
+#define GS_DEV_STEP_RANGE  1u
+#define GS_DEV_NEED_UNCOND 2u
+#define GS_DEV_SIGMA       4u
+
+/* Storage types of latents and model outputs; arithmetic is always fp32. */
+enum { GS_DTYPE_F32 = 0, GS_DTYPE_BF16 = 1, GS_DTYPE_F16 = 2 };
+
+/* Largest number of regional conditioning entries one step accepts. */
+#define GS_MAX_REGIONS 16
+
+/* ------------------------------------------------------------------------ */
+/* Sigma schedule (host).                                                    */
+/* ------------------------------------------------------------------------ */
+
+enum { GS_SCHED_KARRAS = 0, GS_SCHED_NORMAL = 1 };
+
+typedef struct gs_schedule_desc {
+    int32_t kind;               /* GS_SCHED_KARRAS or GS_SCHED_NORMAL                   */
+    int32_t steps;              /* steps to take, >= 1                                   */
+    double  sigma_min;          /* Karras only: lowest nonzero sigma, > 0                */
+    double  sigma_max;          /* Karras only: highest sigma, > sigma_min               */
+    double  rho;                /* Karras only: exponent, > 0 (7 is usual)               */
+    double  denoise;            /* (0, 1): tail of a longer schedule; >= 1: full         */
+    int32_t start_step;         /* -1 = none; else drop sigmas before this index         */
+    int32_t last_step;          /* -1 = none; else keep sigmas up to this index          */
+    int32_t force_full_denoise; /* nonzero: the final sigma is set to 0                  */
+    int32_t n_train;            /* normal only: discrete table length (1000)             */
+    double  beta_start;         /* normal only: first beta (0.00085)                     */
+    double  beta_end;           /* normal only: last beta (0.012)                        */
+} gs_schedule_desc;
+
+/*
+ * gs_sigmas -- the 1-D sigma sequence a sampler walks, high to low.
+ *
+ * [SAMPLING] "sigma 序列": built from the model's sampling parameters and the
+ * scheduler's name; "denoise 小于 1": a longer base schedule is built and only
+ * its tail kept, then start_step / last_step crop it; "force_full_denoise": the
+ * final sigma is forced to 0.
+ *   Karras: Karras et al. 2022 eq. (5), steps levels evenly spaced in
+ *           sigma^(1/rho) from sigma_max to sigma_min, then 0.
+ *   normal: the Stable Diffusion scaled-linear discrete table (n_train betas,
+ *           sqrt-linear from beta_start to beta_end, sigma_k =
+ *           sqrt((1 - abar_k)/abar_k)), sampled from its last entry to its first
+ *           at evenly spaced fractional indices with log-linear interpolation,
+ *           then 0.
+ *   Order: base (int(steps/denoise) steps when denoise < 1, keeping the last
+ *   steps+1 values), last_step crop, start_step crop (a start at or past the
+ *   last step leaves an empty schedule), force_full_denoise.
+ * All arithmetic is binary64; values are rounded to fp32 on output.
+ *
+ * out:             host float[cap]; receives *n_out values.
+ * n_out:           host; number of sigmas written (0 = nothing left to do).
+ * base_offset_out: host, may be NULL; index of out[0] in the base schedule.
+ * Errors: GS_ERR_INVALID_ARG (NULL desc/out/n_out, steps < 1, denoise <= 0,
+ *         bad Karras parameters, kind unknown), GS_ERR_CAPACITY (cap too small;
+ *         *n_out still receives the needed length).
+ */
+gs_status gs_sigmas(const gs_schedule_desc* desc, float* out, int32_t cap,
+                    int32_t* n_out, int32_t* base_offset_out);
+
+/* ------------------------------------------------------------------------ */
+/* Bucket plan (host).                                                       */
+/* ------------------------------------------------------------------------ */
+
+enum { GS_CURVE_LINEAR = 0, GS_CURVE_STEP = 1, GS_CURVE_TABLE = 2 };
+
+typedef struct gs_curve_desc {
+    int32_t kind;   /* GS_CURVE_LINEAR: v0 at progress 0 -> v1 at progress 1
+                       GS_CURVE_STEP:   v0 while progress < edge, v1 afterwards
+                       GS_CURVE_TABLE:  the table argument gives one scale per bucket */
+    double  v0;
+    double  v1;
+    double  edge;
+} gs_curve_desc;
+
+/*
+ * gs_bucket_plan -- per-step bucket ids and guidance scales.
+ *
+ * [BCG] section 2: progress = step / steps, bucket = min(int(progress *
+ * num_buckets), num_buckets - 1), evaluated in binary64 as written; the curve
+ * is cut into num_buckets constant segments.  Section 4 stage 1: each step
+ * reads its scale from the per-bucket table.  A bucket's scale is the curve at
+ * the bucket's midpoint progress (b + 1/2)/num_buckets, unless an explicit
+ * table is given.
+ *
+ * steps:           the schedule's step count (n_sigmas - 1), >= 1.
+ * num_buckets:     >= 1.
+ * curve:           host; see gs_curve_desc.
+ * table:           host double[num_buckets] for GS_CURVE_TABLE, else ignored.
+ * bucket_of_step:  host int32[steps], may be NULL.
+ * scale_of_step:   host float[steps] (the scale LUT the step kernel reads),
+ *                  may be NULL.
+ * Errors: GS_ERR_INVALID_ARG.
+ */
+gs_status gs_bucket_plan(int32_t steps, int32_t num_buckets, const gs_curve_desc* curve,
+                         const double* table, int32_t* bucket_of_step, float* scale_of_step);
+
+/* ------------------------------------------------------------------------ */
+/* Inpaint mask preparation (device, once per run).                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * gs_mask_prepare -- pixel mask -> latent mask.
+ *
+ * [SAMPLING] "inpaint 与 mask": the mask is reshaped and interpolated to the
+ * latent size (the channel broadcast happens inside gs_guided_step).  Bilinear
+ * with half-pixel centres (align_corners = False): destination j samples the
+ * source at (j + 1/2) * in/out - 1/2, clamped at 0, upper neighbour clamped to
+ * the last pixel.  Index and weight arithmetic is binary64 per pixel; the
+ * result is rounded to fp32.
+ *
+ * pix_mask: device float[B][1][Hp][Wp].   lat_mask: device float[B][1][H][W].
+ * Errors: GS_ERR_INVALID_ARG (NULL pointers, sizes < 1), GS_ERR_CUDA.
+ */
+gs_status gs_mask_prepare(const float* pix_mask, int32_t B, int32_t Hp, int32_t Wp,
+                          float* lat_mask, int32_t H, int32_t W, gs_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* The guided step (device, one kernel launch per call).                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * A regional conditioning output ([SAMPLING] "calc_cond_batch()"): the model's
+ * output for the latent crop rows y0..y0+h-1, columns x0..x0+w-1, added back
+ * into the frame with weight strength * feather * mask.
+ *   feather: ramp width F in latent pixels (0 = none).  Every rectangle edge
+ *            that is not on the latent border ramps linearly: a pixel at
+ *            distance t (0-based) from it gets min(1, (t+1)/F); the factors of
+ *            the edges multiply.
+ *   mask:    device float[.][h][w] (row pitch w) or NULL (= 1); sample b reads
+ *            mask + b * mask_bstride (mask_bstride 0 = one mask for all samples).
+ *   out:     device, storage dtype, [B][C][h][pitch], pitch >= w; columns
+ *            w..pitch-1 are never read.
+ */
+typedef struct gs_region {
+    int32_t     y0, x0, h, w;
+    float       strength;
+    int32_t     feather;
+    const float* mask;
+    int64_t     mask_bstride;
+    const void* out;
+    int64_t     pitch;
+} gs_region;
+
+/* launch_flags */
+#define GS_LAUNCH_PDL 1u   /* launch with programmatic dependent launch: the kernel
+                              may be scheduled before the previous kernel in the
+                              stream ends; it waits for it before any memory access */
+
+typedef struct gs_step_args {
+    int32_t B, C, H, W;         /* latent batch, channels, rows, columns (all >= 1)      */
+    int32_t dtype;              /* GS_DTYPE_*: storage type of every latent-shaped buffer */
+
+    const void* x;              /* device [B][C][H][W]: the current latent x_i           */
+    void*       x_out;          /* device [B][C][H][W]: x_{i+1}; may alias x             */
+    void*       denoised_out;   /* device [B][C][H][W] or NULL: the blended prediction   */
+
+    /* Model outputs of this step.  A stacked [2B][C][H][W] output laid out as
+       [uncond_0 .. uncond_{B-1}, cond_0 .. cond_{B-1}] ([BCG] section 3) is passed
+       as uncond = base, cond = base + B*C*H*W elements. */
+    const void* uncond;         /* device [B][C][H][W], or NULL when the uncond forward
+                                   was skipped because every scale is 1 ([SAMPLING]
+                                   "cfg = 1 的优化")                                   */
+    const void* cond;           /* device [B][C][H][W], or NULL when regions give the
+                                   positive branch.  With regions it joins them as a
+                                   full-frame entry of weight 1.                        */
+    int32_t n_regions;          /* 0 .. GS_MAX_REGIONS                                   */
+    const gs_region* regions;   /* host array[n_regions]                                 */
+
+    /* Schedule and guidance. */
+    const float*   sigmas;      /* device float[n_sigmas], high to low                   */
+    int32_t        n_sigmas;    /* >= 2                                                  */
+    const int32_t* step_idx;    /* device int32[B]: sample b steps from sigmas[i] to
+                                   sigmas[i+1], i = step_idx[b]; NULL = every sample
+                                   takes `step`                                          */
+    int32_t        step;        /* used when step_idx is NULL: 0 <= step <= n_sigmas-2   */
+    const float*   scale_lut;   /* device float[n_lut]: scale of sample b is
+                                   scale_lut[i]; NULL = `cfg` for every sample           */
+    int32_t        n_lut;
+    float          cfg;
+
+    /* Inpaint ([SAMPLING] "inpaint 与 mask"): den = m*pred + (1-m)*original with the
+       latent mask m broadcast over channels (1 = regenerate, 0 = keep original). */
+    const float*   inpaint_mask;   /* device float[.][1][H][W] or NULL (no inpaint)      */
+    int64_t        mask_bstride;   /* elements between samples' masks; 0 = shared        */
+    const uint8_t* mask_present;   /* device uint8[B] or NULL (= every sample); samples
+                                      with 0 are not blended and their mask and
+                                      original are not read                             */
+    const void*    original;       /* device [B][C][H][W]; required with inpaint_mask    */
+
+    uint32_t* dev_status;       /* device uint32 or NULL: GS_DEV_* bits OR-ed in         */
+    uint32_t  launch_flags;     /* GS_LAUNCH_*                                           */
+} gs_step_args;
+
+/*
+ * gs_guided_step -- one guided denoise step for every sample of the batch.
+ *
+ * For sample b with i = step_idx[b], sigma = sigmas[i], sigma_next =
+ * sigmas[i+1], s = scale_lut[i] (or cfg), all arithmetic in fp32:
+ *   pos  = cond                                  (no regions), or
+ *          sum_r w_r*out_r / sum_r w_r           ([SAMPLING] calc_cond_batch:
+ *                                                 accumulate by strength and mask,
+ *                                                 normalise overlaps by summed
+ *                                                 weight; 0 where no entry covers)
+ *   pred = fma(s, pos, (1-s)*uncond)             ([SAMPLING] "CFG 的核心", [BCG]
+ *                                                 sections 3-4: uncond +
+ *                                                 s*(cond-uncond) in fp32, exact
+ *                                                 at s = 0 and s = 1); pred = pos
+ *                                                 when uncond is NULL
+ *   den  = fma(m, pred, (1-m)*original)          (inpaint samples), else pred
+ *   x'   = fma(sigma_next/sigma, x - den, den)   (Euler: x + (sigma_next-sigma)*
+ *                                                 (x-den)/sigma; exact den at
+ *                                                 sigma_next = 0)
+ * rounded to the storage dtype (round to nearest even).
+ *
+ * Samples whose step index is out of range, whose sigma is not positive, or
+ * that need the missing uncond branch are skipped (x_out and denoised_out are
+ * not written for them) and flagged in dev_status.
+ *
+ * Alignment: when every latent-shaped pointer is 16-byte aligned and W is a
+ * multiple of 8 the kernel moves 16-byte vectors; otherwise it runs a scalar
+ * variant with the same results.  x_out may alias x (or another latent-shaped
+ * input); it must not overlap region outputs or masks.
+ *
+ * Errors: GS_ERR_INVALID_ARG (NULL required pointer, size < 1, region outside
+ * the frame or pitch < w, n_regions out of range, step out of range with
+ * step_idx NULL, neither cond nor regions, inpaint without original, unknown
+ * dtype), GS_ERR_CUDA (launch failure).  Device-found errors: see dev_status.
+ */
+gs_status gs_guided_step(const gs_step_args* args, gs_stream stream);
+
+/* Decode a device status word into the first gs_status it carries (GS_OK if 0). */
+gs_status gs_status_from_word(uint32_t word);
+
+/* A static, human-readable name for a status code. */
+const char* gs_status_string(gs_status status);
+
+/* ABI version of this header (bumped on any layout change). */
+#define GS_ABI_VERSION 1
+int32_t gs_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_H */

@@ -1,0 +1,121 @@
+"""The C-ABI library loads and exports every entry point include/gs.h declares (CPU only).
+
+Argument checks that return before any CUDA call are exercised here too: they
+must answer GS_ERR_INVALID_ARG without a GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from bucketized_guidance_step_gb300 import build, gs
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "gs.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gs.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:gs_status|const char\*|int32_t)\s+(gs_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(gs.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.gs_abi_version() == gs.GS_ABI_VERSION
+    for code in range(8):
+        assert gs.status_string(code) not in ("", "unknown status")
+    assert gs.status_string(99) == "unknown status"
+    assert gs.status_from_word(0) == gs.GS_OK
+    assert gs.status_from_word(gs.GS_DEV_STEP_RANGE) == gs.GS_ERR_STEP_RANGE
+    assert gs.status_from_word(gs.GS_DEV_NEED_UNCOND) == gs.GS_ERR_NEED_UNCOND
+    assert gs.status_from_word(gs.GS_DEV_SIGMA) == gs.GS_ERR_SIGMA
+
+
+def _valid_args():
+    a = gs.StepArgs()
+    a.B, a.C, a.H, a.W, a.dtype = 2, 4, 8, 8, gs.GS_DTYPE_BF16
+    a.x = a.x_out = a.uncond = a.cond = 0x1000
+    a.sigmas, a.n_sigmas, a.step = 0x2000, 5, 0
+    return a
+
+
+@pytest.mark.parametrize("field,value", [
+    ("B", 0), ("C", 0), ("H", -1), ("dtype", 7), ("x", 0), ("x_out", 0), ("sigmas", 0),
+    ("n_sigmas", 1), ("step", 4), ("step", -1), ("n_regions", 17), ("n_regions", -1),
+])
+def test_step_rejects_invalid_arguments(lib, field, value):
+    a = _valid_args()
+    setattr(a, field, value)
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+
+
+def test_step_rejects_bad_regions_and_missing_branches(lib):
+    a = _valid_args()
+    a.cond = 0
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG  # no positive branch
+    a = _valid_args()
+    a.inpaint_mask = 0x3000                                              # mask without original
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+    bad = [gs.RegionDesc(0, 0, 9, 4, 1.0, 0, None, 0, 0x4000, 4),     # taller than the frame
+           gs.RegionDesc(2, 6, 2, 3, 1.0, 0, None, 0, 0x4000, 4),     # past the right edge
+           gs.RegionDesc(0, 0, 2, 4, 1.0, 0, None, 0, 0x4000, 3),     # pitch < w
+           gs.RegionDesc(0, 0, 2, 4, 1.0, 0, None, 0, None, 4),       # no output
+           gs.RegionDesc(0, 0, 2, 4, -1.0, 0, None, 0, 0x4000, 4),    # negative strength
+           gs.RegionDesc(0, 0, 2, 4, 1.0, -2, None, 0, 0x4000, 4)]    # negative feather
+    for r in bad:
+        a = _valid_args()
+        arr = (gs.RegionDesc * 1)(r)
+        a.n_regions = 1
+        a.regions = ctypes.cast(arr, ctypes.POINTER(gs.RegionDesc))
+        assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+    a = _valid_args()
+    a.n_regions = 1                                                      # regions pointer NULL
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_guided_step(None, None) == gs.GS_ERR_INVALID_ARG
+
+
+def test_mask_prepare_rejects_invalid_arguments(lib):
+    assert lib.gs_mask_prepare(None, 1, 8, 8, 0x1000, 4, 4, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_mask_prepare(0x1000, 0, 8, 8, 0x2000, 4, 4, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_mask_prepare(0x1000, 1, 8, 8, 0x2000, 0, 4, None) == gs.GS_ERR_INVALID_ARG
+
+
+def test_host_entry_points_reject_invalid_arguments(lib):
+    for kw in ({"steps": 0}, {"denoise": 0.0}, {"sigma_min": 0.0}, {"rho": 0.0},
+               {"sigma_max": 0.01}):
+        args = {"steps": 10}
+        args.update(kw)
+        steps = args.pop("steps")
+        with pytest.raises(gs.GSError):
+            gs.sigmas("karras", steps, **args)
+    with pytest.raises(gs.GSError):
+        gs.sigmas("cosine", 10)
+    with pytest.raises(gs.GSError):
+        gs.bucket_plan(0, 4)
+    with pytest.raises(gs.GSError):
+        gs.bucket_plan(10, 0)
+    with pytest.raises(gs.GSError):
+        gs.bucket_plan(10, 4, curve="table")
+    # capacity: a too-small buffer reports the needed length
+    d = gs.ScheduleDesc(gs.GS_SCHED_KARRAS, 10, 0.03, 14.6, 7.0, 1.0, -1, -1, 0, 1000,
+                        0.00085, 0.012)
+    n = ctypes.c_int32(0)
+    buf = (ctypes.c_float * 4)()
+    assert lib.gs_sigmas(ctypes.byref(d), buf, 4, ctypes.byref(n), None) == gs.GS_ERR_CAPACITY
+    assert n.value == 11

@@ -1,0 +1,198 @@
+"""Exact invariants of the CUDA guided step, checked bit for bit on the GPU.
+
+These are the pages' own statements (BCG write-up section 4 stage 2: scale 0
+gives uncond and scale 1 gives cond; sampling page "cfg = 1 的优化": with scale
+1 the uncond branch is not needed; a single full-frame region of strength 1 is
+the plain cond; an all-ones inpaint mask changes nothing; sigma_next = 0 lands
+on the denoised prediction), plus determinism, aliasing, the device status
+word, buffer guard bands and the shared-mask stride.  They hold exactly by the
+kernel's fp32 formulation and need no oracle.
+"""
+
+from __future__ import annotations
+
+import pytest
+import torch
+
+from bucketized_guidance_step_gb300 import gs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+DTYPES = [torch.float32, torch.bfloat16, torch.float16]
+SHAPES = [(3, 4, 16, 32), (2, 3, 5, 7)]          # vector path, scalar path
+
+
+def rnd(shape, seed, dtype):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g).to(dtype).to(DEV)
+
+
+def sig(*v):
+    return torch.tensor(v, dtype=torch.float32, device=DEV)
+
+
+def same_bits(a, b):
+    return torch.equal(a.view(torch.uint8) if a.dtype != torch.float32 else a.view(torch.int32),
+                       b.view(torch.uint8) if b.dtype != torch.float32 else b.view(torch.int32))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_scale0_gives_uncond_scale1_gives_cond(dtype, shape):
+    x, u, c = (rnd(shape, s, dtype) for s in (1, 2, 3))
+    out = torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(3.0, 0.0), uncond=u, cond=c, cfg=0.0, x_out=out)
+    torch.cuda.synchronize()
+    assert same_bits(out, u)
+    gs.guided_step(x, sigmas=sig(3.0, 0.0), uncond=u, cond=c, cfg=1.0, x_out=out)
+    torch.cuda.synchronize()
+    assert same_bits(out, c)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_cfg1_skips_uncond_identically(dtype, shape):
+    x, u, c = (rnd(shape, s, dtype) for s in (4, 5, 6))
+    a, b = torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(5.0, 2.0), uncond=u, cond=c, cfg=1.0, x_out=a)
+    gs.guided_step(x, sigmas=sig(5.0, 2.0), uncond=None, cond=c, cfg=1.0, x_out=b)
+    torch.cuda.synchronize()
+    assert same_bits(a, b)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_full_frame_region_equals_plain_cond(dtype, shape):
+    B, C, H, W = shape
+    x, u, c = (rnd(shape, s, dtype) for s in (7, 8, 9))
+    a, b = torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(5.0, 2.0), uncond=u, cond=c, cfg=6.0, x_out=a)
+    reg = gs.Region(0, 0, H, W, 1.0, 8, c)
+    gs.guided_step(x, sigmas=sig(5.0, 2.0), uncond=u, regions=[reg], cfg=6.0, x_out=b)
+    torch.cuda.synchronize()
+    assert same_bits(a, b)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_inpaint_all_ones_and_all_zeros(dtype, shape):
+    B, C, H, W = shape
+    x, u, c, o = (rnd(shape, s, dtype) for s in (10, 11, 12, 13))
+    plain, ones = torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(5.0, 2.0), uncond=u, cond=c, cfg=3.0, x_out=plain)
+    m1 = torch.ones((B, 1, H, W), device=DEV)
+    gs.guided_step(x, sigmas=sig(5.0, 2.0), uncond=u, cond=c, cfg=3.0, x_out=ones,
+                   inpaint_mask=m1, original=o)
+    torch.cuda.synchronize()
+    assert same_bits(plain, ones)
+    zeros = torch.empty_like(x)
+    m0 = torch.zeros((1, 1, H, W), device=DEV)                 # one mask shared by all
+    gs.guided_step(x, sigmas=sig(5.0, 0.0), uncond=u, cond=c, cfg=3.0, x_out=zeros,
+                   inpaint_mask=m0, original=o)
+    torch.cuda.synchronize()
+    assert same_bits(zeros, o)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_sigma_next_zero_lands_on_denoised(dtype, shape):
+    x, u, c = (rnd(shape, s, dtype) for s in (14, 15, 16))
+    out, den = torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(2.0, 0.0), uncond=u, cond=c, cfg=4.5, x_out=out,
+                   denoised_out=den)
+    torch.cuda.synchronize()
+    assert same_bits(out, den)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_deterministic_and_in_place(dtype):
+    shape = (4, 4, 16, 16)
+    x, u, c = (rnd(shape, s, dtype) for s in (17, 18, 19))
+    a, b = torch.empty_like(x), torch.empty_like(x)
+    lut = torch.tensor([2.0, 1.5, 1.2], device=DEV)
+    idx = torch.tensor([0, 1, 2, 1], dtype=torch.int32, device=DEV)
+    sg = sig(9.0, 4.0, 1.0, 0.0)
+    gs.guided_step(x, sigmas=sg, uncond=u, cond=c, scale_lut=lut, step_idx=idx, x_out=a)
+    gs.guided_step(x, sigmas=sg, uncond=u, cond=c, scale_lut=lut, step_idx=idx, x_out=b)
+    xi = x.clone()
+    gs.guided_step(xi, sigmas=sg, uncond=u, cond=c, scale_lut=lut, step_idx=idx)
+    torch.cuda.synchronize()
+    assert same_bits(a, b) and same_bits(a, xi)
+
+
+def test_device_status_word_and_skipped_samples():
+    shape = (4, 2, 8, 8)
+    x, u, c = (rnd(shape, s, torch.bfloat16) for s in (20, 21, 22))
+    sentinel = torch.full_like(x, 123.0)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idx = torch.tensor([0, 2, -1, 1], dtype=torch.int32, device=DEV)   # 2 and -1 out of range
+    out = sentinel.clone()
+    gs.guided_step(x, sigmas=sig(4.0, 1.0, 0.0), uncond=u, cond=c, step_idx=idx, cfg=2.0,
+                   x_out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gs.GS_DEV_STEP_RANGE
+    assert gs.status_from_word(int(st.item())) == gs.GS_ERR_STEP_RANGE
+    assert torch.equal(out[1], sentinel[1]) and torch.equal(out[2], sentinel[2])
+    assert not torch.equal(out[0], sentinel[0]) and not torch.equal(out[3], sentinel[3])
+
+    # a scale other than 1 without the uncond branch
+    st.zero_()
+    out = sentinel.clone()
+    lut = torch.tensor([1.0, 2.0], device=DEV)
+    idx = torch.tensor([0, 1, 0, 1], dtype=torch.int32, device=DEV)
+    gs.guided_step(x, sigmas=sig(4.0, 1.0, 0.0), uncond=None, cond=c, step_idx=idx,
+                   scale_lut=lut, x_out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == gs.GS_DEV_NEED_UNCOND
+    assert torch.equal(out[1], sentinel[1]) and not torch.equal(out[0], sentinel[0])
+
+    # a step from sigma = 0
+    st.zero_()
+    idx = torch.tensor([1, 0, 0, 0], dtype=torch.int32, device=DEV)
+    gs.guided_step(x, sigmas=sig(4.0, 0.0, 0.0), uncond=u, cond=c, step_idx=idx, cfg=2.0,
+                   x_out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == gs.GS_DEV_SIGMA
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_guard_bands_untouched(dtype):
+    shape = (3, 4, 16, 24)
+    n = 3 * 4 * 16 * 24
+    pad = 4096
+    x, u, c, o = (rnd(shape, s, dtype) for s in (23, 24, 25, 26))
+    buf = torch.full((n + 2 * pad,), 7.0, dtype=dtype, device=DEV)
+    out = buf[pad:pad + n].view(shape)
+    den_buf = torch.full((n + 2 * pad,), -5.0, dtype=dtype, device=DEV)
+    den = den_buf[pad:pad + n].view(shape)
+    m = (torch.rand((3, 1, 16, 24), generator=torch.Generator().manual_seed(3)) > 0.5).float()
+    reg = gs.Region(3, 5, 9, 13, 0.8, 4, rnd((3, 4, 9, 16), 27, dtype))
+    gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, regions=[reg], cfg=5.0, x_out=out,
+                   denoised_out=den, inpaint_mask=m.to(DEV), original=o)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 7.0) and torch.all(buf[pad + n:] == 7.0)
+    assert torch.all(den_buf[:pad] == -5.0) and torch.all(den_buf[pad + n:] == -5.0)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_shared_mask_equals_replicated_mask():
+    shape = (4, 4, 16, 16)
+    x, u, c, o = (rnd(shape, s, torch.bfloat16) for s in (28, 29, 30, 31))
+    m = torch.rand((1, 1, 16, 16), generator=torch.Generator().manual_seed(5)).to(DEV)
+    a, b = torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=a, inpaint_mask=m,
+                   original=o)
+    gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=b,
+                   inpaint_mask=m.expand(4, 1, 16, 16).contiguous(), original=o)
+    torch.cuda.synchronize()
+    assert same_bits(a, b)
+
+
+def test_host_rejects_before_launch_on_gpu():
+    x = rnd((2, 4, 8, 8), 32, torch.bfloat16)
+    with pytest.raises(gs.GSError) as e:
+        gs.guided_step(x, sigmas=sig(1.0, 0.0), uncond=x, cond=x, step=1)
+    assert e.value.status == gs.GS_ERR_INVALID_ARG
+    regs = [gs.Region(0, 0, 2, 2, 1.0, 0, x[:, :, :2, :2].contiguous())] * 17
+    with pytest.raises(gs.GSError):
+        gs.guided_step(x, sigmas=sig(1.0, 0.0), uncond=x, regions=regs)

@@ -1,0 +1,182 @@
+"""The CUDA guided step against the float64 oracle, element by element (GPU).
+
+Both sides take the same seeded inputs (``workloads``); schedules, scale tables
+and latent masks given to both come from the oracle.  Every workload runs at its
+full size in the launch configuration ``bench.py`` times, plus ragged and
+degenerate shapes that exercise the scalar path, channel chunking, unaligned
+pointers and partial masks.  The acceptance gate is described in
+``tests/parity.py``.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from bucketized_guidance_step_gb300 import gs
+from bucketized_guidance_step_gb300.workloads import DTYPES, WORKLOADS, Workload, step_inputs
+from oracle import step as O
+from tests.parity import (error_scale, gate, oracle_latent_mask, oracle_lut, oracle_sigmas,
+                          to64)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _cuda(t):
+    return None if t is None else t.to(DEV).contiguous()
+
+
+def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None,
+             step: int = None, region_masks: bool = False, offset: int = 0,
+             uncond_none: bool = False, want_den: bool = False, pitch_align: int = 8):
+    """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok)."""
+    inp = step_inputs(wl, step_seed, B=B, C=C, H=H, W=W, region_masks=region_masks,
+                      pitch_align=pitch_align)
+    dt = DTYPES[wl.dtype]
+    Bn, Cn, Hn, Wn = inp.noise.shape
+    sig = oracle_sigmas(wl)
+    lut = oracle_lut(wl, len(sig) - 1)
+    if inp.step_idx is not None:
+        idx = inp.step_idx.numpy().astype(np.int64)
+    else:
+        idx = np.full(Bn, 0 if step is None else step, dtype=np.int64)
+    x = torch.from_numpy(sig[idx].astype(np.float64).reshape(-1, 1, 1, 1) *
+                         to64(inp.noise)).to(dt)
+    lat = None
+    if inp.pixel_mask is not None:
+        lat = torch.from_numpy(oracle_latent_mask(inp.pixel_mask, Hn, Wn))
+    cfg = wl.guidance.cfg if wl.guidance.cfg is not None else 1.0
+    u = None if uncond_none else inp.uncond
+
+    # --- GPU ---
+    def dev_latent(t):
+        """Device copy, shifted by `offset` elements to break 16-byte alignment."""
+        if t is None:
+            return None
+        if offset == 0:
+            return _cuda(t)
+        flat = torch.empty(t.numel() + offset, dtype=t.dtype, device=DEV)
+        view = flat[offset:].view(t.shape)
+        view.copy_(t.to(DEV))
+        return view
+
+    xd = dev_latent(x)
+    outd = dev_latent(torch.full_like(x, float("nan")))
+    dend = dev_latent(torch.full_like(x, float("nan"))) if want_den else None
+    regs = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, _cuda(r.out),
+                      _cuda(r.mask)) for r in inp.regions]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kw = dict(uncond=dev_latent(u), cond=dev_latent(inp.cond), regions=regs,
+              sigmas=torch.from_numpy(sig).to(DEV), x_out=outd, denoised_out=dend,
+              status=status)
+    if inp.step_idx is not None:
+        kw["step_idx"] = _cuda(inp.step_idx)
+    else:
+        kw["step"] = int(idx[0])
+    if lut is not None:
+        kw["scale_lut"] = torch.from_numpy(lut).to(DEV)
+    else:
+        kw["cfg"] = cfg
+    if lat is not None:
+        kw.update(inpaint_mask=_cuda(lat), original=dev_latent(inp.original),
+                  mask_present=_cuda(inp.mask_present))
+    gs.guided_step(xd, **kw)
+    torch.cuda.synchronize()
+    got = to64(outd)
+
+    # --- oracle ---
+    oregs = [O.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, to64(r.out),
+                      None if r.mask is None else r.mask.numpy().astype(np.float64))
+             for r in inp.regions]
+    present = (np.ones(Bn, bool) if inp.mask_present is None
+               else inp.mask_present.numpy().astype(bool))
+    ref, den, ok = O.guided_step(to64(x), sig, idx, uncond=to64(u), cond=to64(inp.cond), cfg=cfg,
+                                 scale_lut=lut, regions=oregs,
+                                 inpaint_mask=None if lat is None else lat.numpy(),
+                                 mask_present=present if lat is not None else None,
+                                 original=to64(inp.original))
+    s = lut[idx] if lut is not None else np.full(Bn, np.float32(cfg))
+    sg = sig[idx].astype(np.float64)
+    sn = sig[np.minimum(idx + 1, len(sig) - 1)].astype(np.float64)
+    M = error_scale(to64(x), to64(u), to64(inp.cond), oregs, s, sn / sg,
+                    None if lat is None else lat.numpy().astype(np.float64), present,
+                    to64(inp.original), Hn, Wn)
+    okb = ok.reshape(-1)
+    rep = gate(got[okb], ref[okb], M[okb], wl.dtype, len(oregs), what=wl.name)
+    if wl.dtype == "fp32":
+        assert rep.normwise <= 1e-5
+    assert int(status.item()) == 0
+    if want_den:
+        gd = to64(dend)
+        Md = M  # den's own scale is bounded by M as well
+        gate(gd[okb], den[okb], Md[okb], wl.dtype, len(oregs), what=wl.name + " denoised")
+    return rep, got, ref, ok
+
+
+@pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_workload_full_size(wl):
+    rep, *_ = run_case(wl)
+    assert rep.n == wl.elements
+    print(f"{wl.name}: n={rep.n} primary={rep.primary} floor_only={rep.floor_only} "
+          f"worst={rep.worst_ratio:.3f} normwise={rep.normwise:.2e}")
+
+
+def test_cfg_loop_20_steps_stepwise():
+    """The 20-step plain-CFG loop, gated step by step from the GPU's own x_t."""
+    wl = WORKLOADS[0]
+    sig = oracle_sigmas(wl)
+    dt = DTYPES[wl.dtype]
+    inp0 = step_inputs(wl, 0)
+    x = torch.from_numpy(sig[0].astype(np.float64) * to64(inp0.noise)).to(dt).to(DEV)
+    sig_d = torch.from_numpy(sig).to(DEV)
+    for j in range(len(sig) - 1):
+        inp = step_inputs(wl, j)
+        u, c = _cuda(inp.uncond), _cuda(inp.cond)
+        x_in = to64(x)
+        gs.guided_step(x, sigmas=sig_d, uncond=u, cond=c, step=j, cfg=wl.guidance.cfg)
+        torch.cuda.synchronize()
+        ref, _, ok = O.guided_step(x_in, sig, [j], uncond=to64(inp.uncond), cond=to64(inp.cond),
+                                   cfg=wl.guidance.cfg)
+        M = error_scale(x_in, to64(inp.uncond), to64(inp.cond), [], [wl.guidance.cfg],
+                        [sig[j + 1] / sig[j]], None, None, None, wl.H, wl.W)
+        rep = gate(to64(x), ref, M, "fp32", 0, what=f"step {j}")
+        assert rep.normwise <= 1e-5
+    # the last step goes to sigma = 0: x is the denoised prediction
+    assert sig[-1] == 0.0
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1), (3, 3, 13, 11), (2, 6, 7, 24), (1, 4, 5, 8),
+                                   (5, 2, 16, 16)])
+def test_ragged_shapes_regions_inpaint(dtype, shape):
+    B, C, H, W = shape
+    base = WORKLOADS[4]
+    wl = Workload("ragged", B, C, H, W, dtype, base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=3, region_side=(1, max(1, min(H, W))),
+                  feather=3, inpaint=True, inpaint_samples=max(1, B // 2), seed=11)
+    run_case(wl, region_masks=True, want_den=True)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+def test_unaligned_pointers_take_scalar_path(dtype):
+    base = WORKLOADS[3]
+    wl = Workload("unaligned", 3, 4, 16, 24, dtype, base.schedule, base.guidance,
+                  n_regions=2, inpaint=True, seed=12)
+    run_case(wl, offset=1)
+
+
+@pytest.mark.parametrize("pitch_align", [1, 8])
+def test_region_pitch_and_masks(pitch_align):
+    base = WORKLOADS[2]
+    wl = Workload("regions", 4, 4, 40, 48, "fp16", base.schedule, base.guidance,
+                  full_frame_cond=False, n_regions=16, region_side=(3, 40), seed=13)
+    run_case(wl, region_masks=True, pitch_align=pitch_align, step=5)
+
+
+def test_every_scale_one_without_uncond():
+    base = WORKLOADS[1]
+    wl = Workload("cfg1", 4, 4, 32, 32, "bf16", base.schedule, base.guidance.__class__(cfg=1.0),
+                  seed=14)
+    run_case(wl, uncond_none=True)
