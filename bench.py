@@ -63,6 +63,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bcg_bf16_b16")
     ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch")
+    ap.add_argument("--no-tma", action="store_true",
+                    help="force the register-streaming kernel instead of the TMA pipeline")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -180,39 +182,55 @@ def build_sets(wl, R, dev, seed=0):
     def randn(shp):
         return torch.randn(shp, generator=gen, device=dev, dtype=torch.float32).to(dt)
 
+    # Each input role is one contiguous arena [R, ...] sliced per set, so that a
+    # step touches a handful of dense allocations (as a sampler reusing its
+    # buffers would), not hundreds of small scattered ones.
+    def arena(shp):
+        return randn((R,) + tuple(shp))
+
+    xs = arena(shape)
+    branch = arena((2 * wl.B,) + shape[1:]) if wl.full_frame_cond else arena(shape)
+    slabs = [arena((wl.B, wl.C, r.h, r.pitch)) for r in proto.regions]
+    masks = origs = None
+    nm = 0
+    if wl.inpaint:
+        nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
+        masks = torch.empty((R, wl.B, 1, wl.H, wl.W), dtype=torch.float32, device=dev)
+        origs = arena(shape)
+        from bucketized_guidance_step_gb300.workloads import pixel_mask
+        Hp, Wp = wl.pixel_mask_hw
+        for k in range(R):
+            pm = pixel_mask(wl.B, Hp, Wp, wl.mask_rects, 1000 + k % 4).to(dev)
+            gs.mask_prepare(pm, wl.H, wl.W, out=masks[k])
+            del pm
+    idxs = None
+    if wl.staggered:
+        idxs = torch.randint(0, steps, (R, wl.B), generator=gen, device=dev, dtype=torch.int32)
     sets = []
     for k in range(R):
-        st = {}
-        st["x"] = randn(shape)
+        st = {"x": xs[k]}
         if wl.full_frame_cond:
-            st["stacked"] = randn((2 * wl.B,) + shape[1:])
+            st["stacked"] = branch[k]
         else:
-            st["uncond"] = randn(shape)
-        st["regions"] = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather,
-                                   randn((wl.B, wl.C, r.h, r.pitch)))
-                         for r in proto.regions]
+            st["uncond"] = branch[k]
+        st["regions"] = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, slab[k])
+                         for r, slab in zip(proto.regions, slabs)]
         if wl.inpaint:
-            nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
-            Hp, Wp = wl.pixel_mask_hw
-            from bucketized_guidance_step_gb300.workloads import pixel_mask
-            pm = pixel_mask(wl.B, Hp, Wp, wl.mask_rects, 1000 + k).to(dev)
-            st["mask"] = gs.mask_prepare(pm, wl.H, wl.W)
-            del pm
-            st["orig"] = randn(shape)
+            st["mask"] = masks[k]
+            st["orig"] = origs[k]
             if nm < wl.B:
                 pres = torch.zeros(wl.B, dtype=torch.uint8, device=dev)
                 pres[:nm] = 1
                 st["present"] = pres
-        if wl.staggered:
-            st["idx"] = torch.randint(0, steps, (wl.B,), generator=gen, device=dev,
-                                      dtype=torch.int32)
+        if idxs is not None:
+            st["idx"] = idxs[k]
         sets.append(st)
     torch.cuda.synchronize(dev)
     return sets, sig, lut, steps
 
 
-def step_kwargs(wl, st, sig, lut, pdl):
-    kw = dict(sigmas=sig, regions=st["regions"], pdl=pdl)
+def step_kwargs(wl, st, sig, lut, pdl, tma=True):
+    kw = dict(sigmas=sig, regions=st["regions"], pdl=pdl, tma=tma)
     if "stacked" in st:
         kw["stacked"] = st["stacked"]
     else:
@@ -279,8 +297,10 @@ def run_ours(args, world, rank, local):
     sets, sig, lut, steps = build_sets(wl, R, dev, seed=1234 + rank)
     prepared = []
     for st in sets:
-        a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, args.pdl))
+        a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, args.pdl,
+                                                            not args.no_tma))
         prepared.append((a, keep))
+    kernel = gs.kernel_kind(prepared[0][0])
 
     def launcher(a):
         return lambda: gs.launch_step(a)
@@ -347,6 +367,9 @@ def run_ours(args, world, rank, local):
         "config": {"workload": describe(wl), "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W,
                    "l2": f"{R} rotating input sets of {per_set} B (>= 4x L2 of {l2} B)",
                    "launch": "CUDA graph replay" + (", PDL" if args.pdl else ""),
+                   "kernel": kernel,
+                   "tuning": {k: os.environ[k] for k in ("GS_TMA_ROWS", "GS_TMA_CHANNELS", "GS_STEP_CHANNELS")
+                              if k in os.environ},
                    "parallelism": f"replicas x{world} (independent batches)"},
         "hbm_gbs": round(world * achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
@@ -378,7 +401,7 @@ def run_e2e(args, wl, st, sig, lut, stream, dev, pg):
             host[k].copy_(st[k])
     regions_h = [r.out.to("cpu").pin_memory() for r in st["regions"]]
     out_h = torch.empty_like(st["x"], device="cpu").pin_memory()
-    a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, False))
+    a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, False, not args.no_tma))
 
     def one_step():
         for k, h in host.items():

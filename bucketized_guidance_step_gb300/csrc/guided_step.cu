@@ -30,236 +30,151 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <type_traits>
 
 #include "gs.h"
+#include "step_common.cuh"
 
 namespace {
+
+using namespace gs_detail;
 
 constexpr int kThreads = 128;
 
 // ---------------------------------------------------------------------------
-// Launch parameters (kernel parameter space: read through the constant cache,
-// uniform across the grid).
+// Regional accumulation for one item: pos += w_r * out_r, wsum += w_r over the
+// regions that touch the item's pixels ([SAMPLING] calc_cond_batch).
 // ---------------------------------------------------------------------------
-enum : int { kEdgeTop = 1, kEdgeBottom = 2, kEdgeLeft = 4, kEdgeRight = 8 };
-
-struct DevRegion {
-    int y0, x0, h, w;
-    float strength;
-    float feather;           // ramp width F (0 = none)
-    int edges;               // kEdge* bits: edges that ramp (not on the latent border)
-    int pad_;
-    const void* out;         // [B][C][h][pitch]
-    long long pitch;
-    const float* mask;       // [.][h][w] or nullptr
-    long long mask_bstride;
-};
-
-struct StepParams {
-    int B, C, H, W;
-    long long P;             // H * W
-    long long groups;        // pixel groups per plane, P / VEC
-    int chunks;              // C / CH
-    int n_regions;
-    long long n_items;       // B * chunks * groups
-    const void* x;
-    void* x_out;
-    void* den_out;
-    const void* u;
-    const void* c;
-    const float* sig;
-    const int* step_idx;
-    const float* lut;
-    const float* imask;
-    long long imask_bstride;
-    const unsigned char* present;
-    const void* orig;
-    unsigned int* status;
-    int n_sig;
-    int step;
-    int n_lut;
-    float cfg;
-    DevRegion reg[GS_MAX_REGIONS];
-};
-
-// ---------------------------------------------------------------------------
-// Storage types: a "Raw" vector holds VEC elements exactly as loaded.
-// ---------------------------------------------------------------------------
-struct F32 { using scalar = float; };
-struct BF16 { using scalar = unsigned short; };
-struct F16 { using scalar = unsigned short; };
-
-template <typename T, int VEC>
-struct Raw {
-    static constexpr int kBytes = VEC * static_cast<int>(sizeof(typename T::scalar));
-    static constexpr int kWords = kBytes >= 4 ? kBytes / 4 : 1;
-    unsigned int w[kWords];
-};
-
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ void st_v4(void* p, uint4 v) {
-    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-// Streaming load of VEC elements at element offset `off`.
-template <typename T, int VEC>
-__device__ __forceinline__ Raw<T, VEC> load_raw(const void* base, long long off) {
-    using S = typename T::scalar;
-    Raw<T, VEC> r;
-    const S* p = static_cast<const S*>(base) + off;
-    if constexpr (Raw<T, VEC>::kBytes % 16 == 0) {
+template <typename T, int VEC, int CH>
+__device__ __forceinline__ void accumulate_regions(const StepParams& p, const DevRegion* regs,
+                                                   int b, int cc, long long p0,
+                                                   float (&pos)[CH][VEC], float (&wsum)[VEC]) {
+    const int y = static_cast<int>(p0 / p.W);
+    const int x0 = static_cast<int>(p0 - static_cast<long long>(y) * p.W);
+    for (int r = 0; r < p.n_regions; ++r) {
+        const DevRegion& R = regs[r];
+        if (y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w) continue;
+        const int ty = y - R.y0;
+        float wrow = R.strength;
+        if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
+        if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
+        const int xs = x0 - R.x0;                    // slab column of the item's first pixel
+        float wj[VEC];
+        bool in[VEC];
 #pragma unroll
-        for (int q = 0; q < Raw<T, VEC>::kBytes / 16; ++q) {
-            const uint4 v = ld_stream_v4(reinterpret_cast<const char*>(p) + 16 * q);
-            r.w[4 * q + 0] = v.x;
-            r.w[4 * q + 1] = v.y;
-            r.w[4 * q + 2] = v.z;
-            r.w[4 * q + 3] = v.w;
+        for (int j = 0; j < VEC; ++j) {
+            const int tx = xs + j;
+            in[j] = tx >= 0 && tx < R.w;
+            float f = wrow;
+            if (R.edges & kEdgeLeft) f = f * ramp(tx, R.feather, R.inv_feather);
+            if (R.edges & kEdgeRight) f = f * ramp(R.w - 1 - tx, R.feather, R.inv_feather);
+            wj[j] = f;
         }
-    } else {
-        static_assert(VEC == 1, "vector widths are 16-byte multiples");
-        if constexpr (sizeof(S) == 4)
-            r.w[0] = __float_as_uint(__ldg(reinterpret_cast<const float*>(p)));
-        else
-            r.w[0] = __ldg(reinterpret_cast<const unsigned short*>(p));
-    }
-    return r;
-}
-
-template <typename T>
-__device__ __forceinline__ float widen_one(const void* base, long long off) {
-    using S = typename T::scalar;
-    const S v = __ldg(static_cast<const S*>(base) + off);
-    if constexpr (sizeof(S) == 4) {
-        return v;
-    } else if constexpr (std::is_same<T, BF16>::value) {
-        return __uint_as_float(static_cast<unsigned int>(v) << 16);
-    } else {
-        return __half2float(__ushort_as_half(v));
-    }
-}
-
-// Element j of a raw vector, widened exactly to fp32.
-template <typename T, int VEC>
-__device__ __forceinline__ float widen(const Raw<T, VEC>& r, int j) {
-    if constexpr (std::is_same<T, F32>::value) {
-        return __uint_as_float(r.w[j]);
-    } else {
-        const unsigned int word = r.w[j >> 1];
-        const unsigned short h = (j & 1) ? static_cast<unsigned short>(word >> 16)
-                                         : static_cast<unsigned short>(word & 0xffffu);
-        if constexpr (std::is_same<T, BF16>::value)
-            return __uint_as_float(static_cast<unsigned int>(h) << 16);
-        else
-            return __half2float(__ushort_as_half(h));
-    }
-}
-
-// Round VEC fp32 values to the storage type (nearest even) and store them.
-template <typename T, int VEC>
-__device__ __forceinline__ void store_vec(void* base, long long off, const float (&v)[VEC]) {
-    using S = typename T::scalar;
-    S* p = static_cast<S*>(base) + off;
-    unsigned int w[Raw<T, VEC>::kWords];
-    if constexpr (std::is_same<T, F32>::value) {
+        if (R.mask != nullptr) {
+            const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) w[j] = __float_as_uint(v[j]);
-    } else if constexpr (VEC == 1) {
-        if constexpr (std::is_same<T, BF16>::value)
-            w[0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[0]));
-        else
-            w[0] = __half_as_ushort(__float2half_rn(v[0]));
-    } else {
+            for (int j = 0; j < VEC; ++j)
+                if (in[j]) wj[j] = wj[j] * __ldg(mrow + xs + j);
+        }
 #pragma unroll
-        for (int j = 0; j < VEC; j += 2) {
-            unsigned int lo, hi;
-            if constexpr (std::is_same<T, BF16>::value) {
-                lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
-                hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[j + 1]));
-            } else {
-                lo = __half_as_ushort(__float2half_rn(v[j]));
-                hi = __half_as_ushort(__float2half_rn(v[j + 1]));
+        for (int j = 0; j < VEC; ++j) {
+            wj[j] = in[j] ? wj[j] : 0.0f;
+            wsum[j] = wsum[j] + wj[j];
+        }
+        const long long plane = static_cast<long long>(R.h) * R.pitch;
+        const long long row0 =
+            (static_cast<long long>(b) * p.C + static_cast<long long>(cc) * CH) * plane +
+            static_cast<long long>(ty) * R.pitch;
+        if (VEC > 1 && R.vec_ok) {
+            // Two aligned vectors cover the item's window of the slab row.
+            const int q0 = floor_div(xs, VEC);
+            const int sh = xs - q0 * VEC;
+            const bool lo_ok = q0 >= 0 && q0 * VEC < R.w;
+            const bool hi_ok = sh != 0 && q0 + 1 >= 0 && (q0 + 1) * VEC < R.w;
+            Raw<T, VEC> lo[CH], hi[CH];
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const long long row = row0 + k * plane;
+                if (lo_ok) lo[k] = load_raw<T, VEC>(R.out, row + static_cast<long long>(q0) * VEC);
+                else
+#pragma unroll
+                    for (int i = 0; i < Raw<T, VEC>::kWords; ++i) lo[k].w[i] = 0u;
+                if (hi_ok) hi[k] = load_raw<T, VEC>(R.out, row + static_cast<long long>(q0 + 1) * VEC);
+                else
+#pragma unroll
+                    for (int i = 0; i < Raw<T, VEC>::kWords; ++i) hi[k].w[i] = 0u;
             }
-            w[j >> 1] = lo | (hi << 16);
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const Raw<T, VEC> v = window<T, VEC>(lo[k], hi[k], sh);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    pos[k][j] = in[j] ? fmaf(wj[j], widen<T, VEC>(v, j), pos[k][j]) : pos[k][j];
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < CH; ++k)
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    if (in[j])
+                        pos[k][j] = fmaf(wj[j], widen_one<T>(R.out, row0 + k * plane + xs + j),
+                                         pos[k][j]);
         }
     }
-    if constexpr (Raw<T, VEC>::kBytes % 16 == 0) {
-#pragma unroll
-        for (int q = 0; q < Raw<T, VEC>::kBytes / 16; ++q)
-            st_v4(reinterpret_cast<char*>(p) + 16 * q,
-                  make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
-    } else if constexpr (sizeof(S) == 4) {
-        *reinterpret_cast<unsigned int*>(p) = w[0];
-    } else {
-        *reinterpret_cast<unsigned short*>(p) = static_cast<unsigned short>(w[0]);
-    }
-}
-
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependents_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Ramp factor at 0-based distance t from a feathered edge: min(1, (t + 1) / F).
-__device__ __forceinline__ float ramp(int t, float F) {
-    return fminf(1.0f, __fdiv_rn(static_cast<float>(t + 1), F));
 }
 
 // ---------------------------------------------------------------------------
 // One work item: sample b, channels c0 .. c0+CH-1, pixels p0 .. p0+VEC-1 (one row).
+// REG: regional conditioning present.  INP: an inpaint mask is given.
 // ---------------------------------------------------------------------------
-template <typename T, int VEC, int CH>
-__device__ __forceinline__ void step_item(const StepParams& p, long long item) {
+template <typename T, int VEC, int CH, bool REG, bool INP>
+__device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* regs,
+                                          long long item) {
     const long long g = item % p.groups;
     const long long rest = item / p.groups;
     const int cc = static_cast<int>(rest % p.chunks);
     const int b = static_cast<int>(rest / p.chunks);
     const long long p0 = g * VEC;
-    const long long off0 = (static_cast<long long>(b) * p.C + static_cast<long long>(cc) * CH) * p.P + p0;
+    const long long off0 =
+        (static_cast<long long>(b) * p.C + static_cast<long long>(cc) * CH) * p.P + p0;
+    const bool has_u = p.u != nullptr;
+    const bool has_c = p.c != nullptr;
 
-    // 1. Issue every load of the item before any arithmetic needs one.
+    // 1. Issue the item's full-frame loads before any arithmetic needs them.
     Raw<T, VEC> xr[CH], ur[CH], cr[CH], orr[CH];
 #pragma unroll
     for (int k = 0; k < CH; ++k) xr[k] = load_raw<T, VEC>(p.x, off0 + k * p.P);
-    if (p.u != nullptr) {
+    if (has_u) {
 #pragma unroll
         for (int k = 0; k < CH; ++k) ur[k] = load_raw<T, VEC>(p.u, off0 + k * p.P);
     }
-    if (p.c != nullptr) {
+    if (!REG || has_c) {
 #pragma unroll
         for (int k = 0; k < CH; ++k) cr[k] = load_raw<T, VEC>(p.c, off0 + k * p.P);
     }
-    const bool inpaint = p.imask != nullptr && (p.present == nullptr || __ldg(p.present + b) != 0);
+    bool inpaint = false;
     float m[VEC];
-    if (inpaint) {
+    if constexpr (INP) {
+        inpaint = p.present == nullptr || __ldg(p.present + b) != 0;
+        if (inpaint) {
 #pragma unroll
-        for (int k = 0; k < CH; ++k) orr[k] = load_raw<T, VEC>(p.orig, off0 + k * p.P);
-        const float* mrow = p.imask + b * p.imask_bstride + p0;
-        if constexpr (VEC % 4 == 0) {
+            for (int k = 0; k < CH; ++k) orr[k] = load_raw<T, VEC>(p.orig, off0 + k * p.P);
+            const float* mrow = p.imask + b * p.imask_bstride + p0;
+            if constexpr (VEC % 4 == 0) {
 #pragma unroll
-            for (int q = 0; q < VEC / 4; ++q) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(mrow) + q);
-                m[4 * q + 0] = v.x;
-                m[4 * q + 1] = v.y;
-                m[4 * q + 2] = v.z;
-                m[4 * q + 3] = v.w;
+                for (int q = 0; q < VEC / 4; ++q) {
+                    const float4 v = __ldg(reinterpret_cast<const float4*>(mrow) + q);
+                    m[4 * q + 0] = v.x;
+                    m[4 * q + 1] = v.y;
+                    m[4 * q + 2] = v.z;
+                    m[4 * q + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) m[j] = __ldg(mrow + j);
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) m[j] = __ldg(mrow + j);
         }
     }
 
@@ -271,7 +186,7 @@ __device__ __forceinline__ void step_item(const StepParams& p, long long item) {
     const float sigma = __ldg(p.sig + si);
     const float sigma_next = __ldg(p.sig + si + 1);
     const bool sigma_ok = sigma > 0.0f && sigma <= 3.402823466e38f;
-    const bool uncond_ok = p.u != nullptr || s == 1.0f;
+    const bool uncond_ok = has_u || s == 1.0f;
     if (!(in_range && sigma_ok && uncond_ok)) {
         if (p.status != nullptr && g == 0 && cc == 0) {
             unsigned int bits = 0;
@@ -287,65 +202,26 @@ __device__ __forceinline__ void step_item(const StepParams& p, long long item) {
 
     // 3. Positive branch: full-frame cond, or the weight-normalised regional sum.
     float pos[CH][VEC];
-    if (p.n_regions == 0) {
-#pragma unroll
-        for (int k = 0; k < CH; ++k)
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) pos[k][j] = widen<T, VEC>(cr[k], j);
-    } else {
+    if constexpr (REG) {
         float wsum[VEC];
-        const bool has_c = p.c != nullptr;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) wsum[j] = has_c ? 1.0f : 0.0f;
 #pragma unroll
         for (int k = 0; k < CH; ++k)
 #pragma unroll
             for (int j = 0; j < VEC; ++j) pos[k][j] = has_c ? widen<T, VEC>(cr[k], j) : 0.0f;
-
-        const int y = static_cast<int>(p0 / p.W);
-        const int x0 = static_cast<int>(p0 - static_cast<long long>(y) * p.W);
-        for (int r = 0; r < p.n_regions; ++r) {
-            const DevRegion& R = p.reg[r];
-            if (y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w) continue;
-            const int ty = y - R.y0;
-            float fy = 1.0f;
-            if (R.edges & kEdgeTop) fy = fy * ramp(ty, R.feather);
-            if (R.edges & kEdgeBottom) fy = fy * ramp(R.h - 1 - ty, R.feather);
-            const float* mrow = R.mask != nullptr ? R.mask + b * R.mask_bstride +
-                                                        static_cast<long long>(ty) * R.w
-                                                  : nullptr;
-            float wj[VEC];
-            int tx[VEC];
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                tx[j] = x0 + j - R.x0;
-                const bool inside = tx[j] >= 0 && tx[j] < R.w;
-                float fx = 1.0f;
-                if (R.edges & kEdgeLeft) fx = fx * ramp(tx[j], R.feather);
-                if (R.edges & kEdgeRight) fx = fx * ramp(R.w - 1 - tx[j], R.feather);
-                float w = R.strength * (fy * fx);
-                if (mrow != nullptr && inside) w = w * __ldg(mrow + tx[j]);
-                wj[j] = inside ? w : 0.0f;
-                wsum[j] = wsum[j] + wj[j];
-            }
-            const long long row0 =
-                ((static_cast<long long>(b) * p.C + static_cast<long long>(cc) * CH) * R.h + ty) *
-                R.pitch;
-            const long long plane = static_cast<long long>(R.h) * R.pitch;
-#pragma unroll
-            for (int k = 0; k < CH; ++k)
-#pragma unroll
-                for (int j = 0; j < VEC; ++j)
-                    if (tx[j] >= 0 && tx[j] < R.w)
-                        pos[k][j] = fmaf(wj[j], widen_one<T>(R.out, row0 + k * plane + tx[j]),
-                                         pos[k][j]);
-        }
+        accumulate_regions<T, VEC, CH>(p, regs, b, cc, p0, pos, wsum);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             const float inv = wsum[j] > 0.0f ? __frcp_rn(wsum[j]) : 0.0f;
 #pragma unroll
             for (int k = 0; k < CH; ++k) pos[k][j] = pos[k][j] * inv;
         }
+    } else {
+#pragma unroll
+        for (int k = 0; k < CH; ++k)
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) pos[k][j] = widen<T, VEC>(cr[k], j);
     }
 
     // 4. Combine, inpaint blend, Euler update, round and store.
@@ -355,9 +231,9 @@ __device__ __forceinline__ void step_item(const StepParams& p, long long item) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             float pred = pos[k][j];
-            if (p.u != nullptr) pred = fmaf(s, pred, one_minus_s * widen<T, VEC>(ur[k], j));
+            if (has_u) pred = fmaf(s, pred, one_minus_s * widen<T, VEC>(ur[k], j));
             float den = pred;
-            if (inpaint) den = fmaf(m[j], pred, (1.0f - m[j]) * widen<T, VEC>(orr[k], j));
+            if (INP && inpaint) den = fmaf(m[j], pred, (1.0f - m[j]) * widen<T, VEC>(orr[k], j));
             const float xv = widen<T, VEC>(xr[k], j);
             xo[j] = fmaf(ratio, xv - den, den);
             dn[j] = den;
@@ -367,73 +243,275 @@ __device__ __forceinline__ void step_item(const StepParams& p, long long item) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Vector items (VEC >= 2) on packed fp32 pairs.  Same operations and order as
+// step_item; region loads are issued in batches before any of them is used.
+// ---------------------------------------------------------------------------
 template <typename T, int VEC, int CH>
+__device__ __forceinline__ void accumulate_regions_vec(const StepParams& p, const DevRegion* regs,
+                                                       int b, int cc,
+                                                       long long p0, f2 (&pos)[CH][VEC / 2],
+                                                       float (&wsum)[VEC]) {
+    constexpr int NP = VEC / 2;
+    constexpr int kBatch = CH >= 4 ? 1 : (CH == 2 ? 2 : 4);
+    constexpr int kW = Raw<T, VEC>::kWords;
+    const int y = static_cast<int>(p0 / p.W);
+    const int x0 = static_cast<int>(p0 - static_cast<long long>(y) * p.W);
+    for (int r0 = 0; r0 < p.n_regions; r0 += kBatch) {
+        Raw<T, VEC> lo[kBatch][CH], hi[kBatch][CH];
+        bool hit[kBatch];
+        // phase 1: which regions touch the item, and their loads
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int r = r0 + i;
+            hit[i] = false;
+#pragma unroll
+            for (int k = 0; k < CH; ++k)
+#pragma unroll
+                for (int t = 0; t < kW; ++t) lo[i][k].w[t] = hi[i][k].w[t] = 0u;
+            if (r >= p.n_regions) continue;
+            const DevRegion& R = regs[r];
+            hit[i] = !(y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w);
+            if (!hit[i] || !R.vec_ok) continue;
+            const int xs = x0 - R.x0;
+            const int q0 = floor_div(xs, VEC);
+            const int sh = xs - q0 * VEC;
+            const long long plane = static_cast<long long>(R.h) * R.pitch;
+            const long long row0 =
+                (static_cast<long long>(b) * p.C + static_cast<long long>(cc) * CH) * plane +
+                static_cast<long long>(y - R.y0) * R.pitch;
+            const bool lo_ok = q0 >= 0 && q0 * VEC < R.w;
+            const bool hi_ok = sh != 0 && q0 + 1 >= 0 && (q0 + 1) * VEC < R.w;
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                if (lo_ok)
+                    lo[i][k] = load_raw<T, VEC>(R.out, row0 + k * plane +
+                                                           static_cast<long long>(q0) * VEC);
+                if (hi_ok)
+                    hi[i][k] = load_raw<T, VEC>(R.out, row0 + k * plane +
+                                                           static_cast<long long>(q0 + 1) * VEC);
+            }
+        }
+        // phase 2: weights and accumulation
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            if (!hit[i]) continue;
+            const DevRegion& R = regs[r0 + i];
+            const int ty = y - R.y0;
+            float wrow = R.strength;
+            if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
+            if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
+            const int xs = x0 - R.x0;
+            float wj[VEC];
+            bool in[VEC];
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const int tx = xs + j;
+                in[j] = tx >= 0 && tx < R.w;
+                float f = wrow;
+                if (R.edges & kEdgeLeft) f = f * ramp(tx, R.feather, R.inv_feather);
+                if (R.edges & kEdgeRight) f = f * ramp(R.w - 1 - tx, R.feather, R.inv_feather);
+                wj[j] = f;
+            }
+            if (R.mask != nullptr) {
+                const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    if (in[j]) wj[j] = wj[j] * __ldg(mrow + xs + j);
+            }
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                wj[j] = in[j] ? wj[j] : 0.0f;
+                wsum[j] = wsum[j] + wj[j];
+            }
+            f2 w2[NP];
+#pragma unroll
+            for (int q = 0; q < NP; ++q) w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
+            const long long plane = static_cast<long long>(R.h) * R.pitch;
+            const long long row0 =
+                (static_cast<long long>(b) * p.C + static_cast<long long>(cc) * CH) * plane +
+                static_cast<long long>(ty) * R.pitch;
+            const int q0 = floor_div(xs, VEC);
+            const int sh = xs - q0 * VEC;
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                float v[VEC];
+                if (R.vec_ok) {
+                    const Raw<T, VEC> win = window<T, VEC>(lo[i][k], hi[i][k], sh);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) v[j] = in[j] ? widen<T, VEC>(win, j) : 0.0f;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        v[j] = in[j] ? widen_one<T>(R.out, row0 + k * plane + xs + j) : 0.0f;
+                }
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    pos[k][q] = fma2(w2[q], mk2(v[2 * q], v[2 * q + 1]), pos[k][q]);
+            }
+        }
+    }
+}
+
+template <typename T, int VEC, int CH, bool REG, bool INP>
+__device__ __forceinline__ void step_item_vec(const StepParams& p, const DevRegion* regs,
+                                              long long item) {
+    constexpr int NP = VEC / 2;
+    const long long g = item % p.groups;
+    const long long rest = item / p.groups;
+    const int cc = static_cast<int>(rest % p.chunks);
+    const int b = static_cast<int>(rest / p.chunks);
+    const long long p0 = g * VEC;
+    const long long off0 =
+        (static_cast<long long>(b) * p.C + static_cast<long long>(cc) * CH) * p.P + p0;
+    const bool has_u = p.u != nullptr;
+    const bool has_c = p.c != nullptr;
+
+    // 1. Issue the item's full-frame loads.
+    Raw<T, VEC> xr[CH], ur[CH], cr[CH], orr[CH];
+#pragma unroll
+    for (int k = 0; k < CH; ++k) xr[k] = load_raw<T, VEC>(p.x, off0 + k * p.P);
+    if (has_u) {
+#pragma unroll
+        for (int k = 0; k < CH; ++k) ur[k] = load_raw<T, VEC>(p.u, off0 + k * p.P);
+    }
+    if (!REG || has_c) {
+#pragma unroll
+        for (int k = 0; k < CH; ++k) cr[k] = load_raw<T, VEC>(p.c, off0 + k * p.P);
+    }
+    bool inpaint = false;
+    float m[VEC];
+    if constexpr (INP) {
+        inpaint = p.present == nullptr || __ldg(p.present + b) != 0;
+        if (inpaint) {
+#pragma unroll
+            for (int k = 0; k < CH; ++k) orr[k] = load_raw<T, VEC>(p.orig, off0 + k * p.P);
+            const float* mrow = p.imask + b * p.imask_bstride + p0;
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(mrow) + q);
+                m[4 * q + 0] = v.x;
+                m[4 * q + 1] = v.y;
+                m[4 * q + 2] = v.z;
+                m[4 * q + 3] = v.w;
+            }
+        }
+    }
+
+    // 2. Per-sample step parameters.
+    const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
+    const bool in_range = idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
+    const int si = in_range ? idx : 0;
+    const float s = p.lut != nullptr ? __ldg(p.lut + si) : p.cfg;
+    const float sigma = __ldg(p.sig + si);
+    const float sigma_next = __ldg(p.sig + si + 1);
+    const bool sigma_ok = sigma > 0.0f && sigma <= 3.402823466e38f;
+    const bool uncond_ok = has_u || s == 1.0f;
+
+    // 3. Positive branch (regional loads are issued here, before the check below
+    //    needs the per-sample parameters).
+    f2 pos[CH][NP];
+    if constexpr (REG) {
+        float wsum[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) wsum[j] = has_c ? 1.0f : 0.0f;
+#pragma unroll
+        for (int k = 0; k < CH; ++k)
+#pragma unroll
+            for (int q = 0; q < NP; ++q) pos[k][q] = has_c ? widen2<T, VEC>(cr[k], q) : splat2(0.0f);
+        accumulate_regions_vec<T, VEC, CH>(p, regs, b, cc, p0, pos, wsum);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            const float i0 = wsum[2 * q] > 0.0f ? __frcp_rn(wsum[2 * q]) : 0.0f;
+            const float i1 = wsum[2 * q + 1] > 0.0f ? __frcp_rn(wsum[2 * q + 1]) : 0.0f;
+            const f2 inv = mk2(i0, i1);
+#pragma unroll
+            for (int k = 0; k < CH; ++k) pos[k][q] = mul2(pos[k][q], inv);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < CH; ++k)
+#pragma unroll
+            for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(cr[k], q);
+    }
+
+    if (!(in_range && sigma_ok && uncond_ok)) {
+        if (p.status != nullptr && g == 0 && cc == 0) {
+            unsigned int bits = 0;
+            if (!in_range) bits |= GS_DEV_STEP_RANGE;
+            else if (!sigma_ok) bits |= GS_DEV_SIGMA;
+            if (in_range && !uncond_ok) bits |= GS_DEV_NEED_UNCOND;
+            atomicOr(p.status, bits);
+        }
+        return;
+    }
+    const f2 s2 = splat2(s);
+    const f2 oms2 = splat2(1.0f - s);
+    const f2 r2 = splat2(__fdiv_rn(sigma_next, sigma));
+    f2 m2[NP], omm2[NP];
+    if (INP && inpaint) {
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            m2[q] = mk2(m[2 * q], m[2 * q + 1]);
+            omm2[q] = sub2(splat2(1.0f), m2[q]);
+        }
+    }
+
+    // 4. Combine, inpaint blend, Euler update, round and store.
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        Raw<T, VEC> xo, dn;
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            f2 pred = pos[k][q];
+            if (has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(ur[k], q)));
+            f2 den = pred;
+            if (INP && inpaint) den = fma2(m2[q], pred, mul2(omm2[q], widen2<T, VEC>(orr[k], q)));
+            const f2 xn = fma2(r2, sub2(widen2<T, VEC>(xr[k], q), den), den);
+            narrow2<T, VEC>(xo, q, xn);
+            if (p.den_out != nullptr) narrow2<T, VEC>(dn, q, den);
+        }
+        store_raw<T, VEC>(p.x_out, off0 + k * p.P, xo);
+        if (p.den_out != nullptr) store_raw<T, VEC>(p.den_out, off0 + k * p.P, dn);
+    }
+}
+
+template <typename T, int VEC, int CH, bool REG, bool INP>
 __global__ void __launch_bounds__(kThreads) guided_step_kernel(const __grid_constant__ StepParams p) {
+    // The region table lives in kernel parameters; a loop over it with a
+    // runtime index would take one constant-cache miss per region, serially.
+    // Copy it to shared memory with one parallel load instead.
+    __shared__ DevRegion regs[REG ? GS_MAX_REGIONS : 1];
+    if constexpr (REG) {
+        const int words = p.n_regions * static_cast<int>(sizeof(DevRegion) / 4);
+        const int* src = reinterpret_cast<const int*>(p.reg);
+        int* dst = reinterpret_cast<int*>(regs);
+        for (int i = threadIdx.x; i < words; i += kThreads) dst[i] = src[i];
+        __syncthreads();
+    }
     grid_dependency_wait();
     grid_dependents_launch();
-    const long long n = p.n_items;
-    const long long begin = n * blockIdx.x / gridDim.x;
-    const long long end = n * (blockIdx.x + 1) / gridDim.x;
-    for (long long it = begin + threadIdx.x; it < end; it += kThreads) step_item<T, VEC, CH>(p, it);
+    const long long it = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+    if (it >= p.n_items) return;
+    if constexpr (VEC >= 2)
+        step_item_vec<T, VEC, CH, REG, INP>(p, regs, it);
+    else
+        step_item<T, VEC, CH, REG, INP>(p, regs, it);
 }
 
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-using KernelFn = void (*)(StepParams);
-
-struct DeviceInfo {
-    int sms = 0;
-};
-
-constexpr int kMaxDevices = 64;
-
-int sm_count(int dev) {
-    static DeviceInfo info[kMaxDevices];
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= kMaxDevices) return 0;
-    if (info[dev].sms == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        info[dev].sms = v;
-    }
-    return info[dev].sms;
-}
-
-template <typename T, int VEC, int CH>
-int blocks_per_sm(int dev) {
-    static int cached[kMaxDevices] = {0};
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= kMaxDevices) return 0;
-    if (cached[dev] == 0) {
-        int v = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, guided_step_kernel<T, VEC, CH>,
-                                                          kThreads, 0) != cudaSuccess)
-            return 0;
-        cached[dev] = v;
-    }
-    return cached[dev];
-}
-
-template <typename T, int VEC, int CH>
+template <typename T, int VEC, int CH, bool REG, bool INP>
 gs_status launch(StepParams& p, gs_stream stream, unsigned int flags) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GS_ERR_CUDA;
-    const int sms = sm_count(dev);
-    const int occ = blocks_per_sm<T, VEC, CH>(dev);
-    if (sms <= 0 || occ <= 0) return GS_ERR_CUDA;
-
     p.groups = p.P / VEC;
     p.chunks = p.C / CH;
     p.n_items = static_cast<long long>(p.B) * p.chunks * p.groups;
-    // Whole waves of SM-count CTAs, no more than fit at once.
-    const long long needed = (p.n_items + kThreads - 1) / kThreads;
-    long long waves = (needed + sms - 1) / sms;
-    if (waves > occ) waves = occ;
-    if (waves < 1) waves = 1;
-    const unsigned int grid = static_cast<unsigned int>(waves * sms);
+    // One item per thread; the CTA scheduler hands CTAs to SMs as they drain,
+    // which balances SMs whose memory traffic finishes at different rates.
+    const long long blocks = (p.n_items + kThreads - 1) / kThreads;
+    if (blocks > 0x7fffffffll) return GS_ERR_UNSUPPORTED;
+    const unsigned int grid = static_cast<unsigned int>(blocks);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -447,7 +525,7 @@ gs_status launch(StepParams& p, gs_stream stream, unsigned int flags) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, guided_step_kernel<T, VEC, CH>, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, guided_step_kernel<T, VEC, CH, REG, INP>, p);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return GS_ERR_CUDA;
@@ -455,25 +533,59 @@ gs_status launch(StepParams& p, gs_stream stream, unsigned int flags) {
     return GS_OK;
 }
 
-template <typename T, int VEC>
+// Channels per item.  Default: 2 when C is even, else 1 (the scalar path takes
+// one).  GS_STEP_CHANNELS=1|2|4 in the environment overrides the choice where it
+// divides C (a tuning knob; results do not depend on it).
+int channel_override() {
+    static const int v = [] {
+        const char* e = getenv("GS_STEP_CHANNELS");
+        if (e == nullptr) return 0;
+        const int c = atoi(e);
+        return (c == 1 || c == 2 || c == 4) ? c : 0;
+    }();
+    return v;
+}
+
+template <typename T, int VEC, bool REG, bool INP>
 gs_status launch_ch(StepParams& p, gs_stream stream, unsigned int flags) {
-    if (p.C % 4 == 0) return launch<T, VEC, 4>(p, stream, flags);
-    if (p.C % 2 == 0) return launch<T, VEC, 2>(p, stream, flags);
-    return launch<T, VEC, 1>(p, stream, flags);
+    if constexpr (VEC == 1) {
+        return launch<T, 1, 1, REG, INP>(p, stream, flags);
+    } else {
+        int ch = p.C % 2 == 0 ? 2 : 1;
+        const int o = channel_override();
+        if (o != 0 && p.C % o == 0) ch = o;
+        if (ch == 4) return launch<T, VEC, 4, REG, INP>(p, stream, flags);
+        if (ch == 2) return launch<T, VEC, 2, REG, INP>(p, stream, flags);
+        return launch<T, VEC, 1, REG, INP>(p, stream, flags);
+    }
+}
+
+template <typename T, int VEC>
+gs_status launch_features(StepParams& p, gs_stream stream, unsigned int flags) {
+    const bool reg = p.n_regions > 0;
+    const bool inp = p.imask != nullptr;
+    if (reg && inp) return launch_ch<T, VEC, true, true>(p, stream, flags);
+    if (reg) return launch_ch<T, VEC, true, false>(p, stream, flags);
+    if (inp) return launch_ch<T, VEC, false, true>(p, stream, flags);
+    return launch_ch<T, VEC, false, false>(p, stream, flags);
 }
 
 template <typename T>
 gs_status launch_dtype(StepParams& p, bool vector_ok, gs_stream stream, unsigned int flags) {
     constexpr int kVec = 16 / static_cast<int>(sizeof(typename T::scalar));
-    if (vector_ok && p.W % kVec == 0) return launch_ch<T, kVec>(p, stream, flags);
-    return launch_ch<T, 1>(p, stream, flags);
+    if (vector_ok && p.W % kVec == 0) return launch_features<T, kVec>(p, stream, flags);
+    return launch_features<T, 1>(p, stream, flags);
 }
 
 bool aligned16(const void* q) { return (reinterpret_cast<unsigned long long>(q) & 15ull) == 0; }
 
 }  // namespace
 
-extern "C" gs_status gs_guided_step(const gs_step_args* a, gs_stream stream) {
+namespace {
+
+// Validate, build the launch parameters and launch (or, with kind != nullptr, only
+// report which kernel would run).
+gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kind) {
     if (a == nullptr) return GS_ERR_INVALID_ARG;
     if (a->B < 1 || a->C < 1 || a->H < 1 || a->W < 1) return GS_ERR_INVALID_ARG;
     if (a->dtype != GS_DTYPE_F32 && a->dtype != GS_DTYPE_BF16 && a->dtype != GS_DTYPE_F16)
@@ -514,6 +626,7 @@ extern "C" gs_status gs_guided_step(const gs_step_args* a, gs_stream stream) {
     p.orig = a->inpaint_mask != nullptr ? a->original : nullptr;
     p.status = a->dev_status;
     p.n_regions = a->n_regions;
+    const long long esize = a->dtype == GS_DTYPE_F32 ? 4 : 2;
     for (int r = 0; r < a->n_regions; ++r) {
         const gs_region& s = a->regions[r];
         if (s.h < 1 || s.w < 1 || s.y0 < 0 || s.x0 < 0 || s.y0 + s.h > a->H || s.x0 + s.w > a->W)
@@ -527,7 +640,9 @@ extern "C" gs_status gs_guided_step(const gs_step_args* a, gs_stream stream) {
         d.h = s.h;
         d.w = s.w;
         d.strength = s.strength;
-        d.feather = static_cast<float>(s.feather);
+        d.inv_feather = s.feather > 0 ? 1.0f / static_cast<float>(s.feather) : 0.0f;
+        d.feather = s.feather;
+        d.vec_ok = aligned16(s.out) && (s.pitch * esize) % 16 == 0;
         d.edges = 0;
         if (s.feather > 0) {
             if (s.y0 > 0) d.edges |= kEdgeTop;
@@ -549,9 +664,31 @@ extern "C" gs_status gs_guided_step(const gs_step_args* a, gs_stream stream) {
     if (a->inpaint_mask != nullptr)
         vec = vec && aligned16(a->original) && aligned16(a->inpaint_mask) && a->mask_bstride % 4 == 0;
 
+    bool used_tma = false;
+    const gs_status st =
+        launch_step_tma(p, a->dtype, a->launch_flags, stream, &used_tma, kind != nullptr);
+    if (st != GS_OK) return st;
+    if (kind != nullptr) {
+        const int vec16 = a->dtype == GS_DTYPE_F32 ? 4 : 8;
+        *kind = used_tma ? GS_KERNEL_TMA
+                         : (vec && a->W % vec16 == 0 ? GS_KERNEL_VECTOR : GS_KERNEL_SCALAR);
+        return GS_OK;
+    }
+    if (used_tma) return GS_OK;
     switch (a->dtype) {
         case GS_DTYPE_F32: return launch_dtype<F32>(p, vec, stream, a->launch_flags);
         case GS_DTYPE_BF16: return launch_dtype<BF16>(p, vec, stream, a->launch_flags);
         default: return launch_dtype<F16>(p, vec, stream, a->launch_flags);
     }
+}
+
+}  // namespace
+
+extern "C" gs_status gs_guided_step(const gs_step_args* a, gs_stream stream) {
+    return guided_step_impl(a, stream, nullptr);
+}
+
+extern "C" gs_status gs_step_kernel_kind(const gs_step_args* a, int32_t* kind) {
+    if (kind == nullptr) return GS_ERR_INVALID_ARG;
+    return guided_step_impl(a, nullptr, kind);
 }

@@ -5,6 +5,7 @@ extern "C" gs_status gs_status_from_word(uint32_t word) {
     if (word & GS_DEV_STEP_RANGE) return GS_ERR_STEP_RANGE;
     if (word & GS_DEV_NEED_UNCOND) return GS_ERR_NEED_UNCOND;
     if (word & GS_DEV_SIGMA) return GS_ERR_SIGMA;
+    if (word & GS_DEV_TIMEOUT) return GS_ERR_TIMEOUT;
     return GS_OK;
 }
 
@@ -18,6 +19,7 @@ extern "C" const char* gs_status_string(gs_status s) {
         case GS_ERR_NEED_UNCOND: return "scale != 1 without an uncond branch (sample skipped)";
         case GS_ERR_SIGMA: return "sigma not positive (sample skipped)";
         case GS_ERR_CAPACITY: return "output buffer too small";
+        case GS_ERR_TIMEOUT: return "device pipeline wait timed out (output incomplete)";
     }
     return "unknown status";
 }

@@ -1,0 +1,703 @@
+// TMA-fed variant of the fused guided step (sm_103a).
+//
+// Same arithmetic as the register-streaming kernel in guided_step.cu (see the
+// formulas in include/gs.h); a different way to move the bytes.  Each CTA owns
+// one tile = (sample b, a group of CG channels, a band of RB full rows), and
+// every input of the tile arrives as one 3-D TMA box into shared memory:
+//
+//   * x, uncond, cond and original as [CG][RB][W] boxes of their [B*C][H][W]
+//     tensors, and the inpaint mask as a [RB][W] box of [B or 1][H][W];
+//   * every regional output that overlaps the band as a [CG][RB][wbox] box of
+//     its [B*C][h][pitch] slab, started at slab row band*RB - y0 so that box row
+//     i is frame row band*RB + i.  TMA zero-fills rows outside the slab, so a
+//     region arrives row-aligned with the frame whatever its origin, and only
+//     regions that touch the band are fetched at all.
+//
+// Thread 0 arms the CTA's mbarrier with the tile's byte count and issues the
+// boxes; no register holds a load in flight.  Every thread then computes VEC
+// pixels x CG channels of one row from shared memory (region weights and the
+// mask once per pixel, reused over the channels; packed fp32-pair math) and
+// writes x_out with 16-byte stores.  Several tile-CTAs are resident per SM, so
+// the loads of some overlap the arithmetic of others, and the CTA scheduler
+// hands out tiles as SMs drain.
+//
+// The mbarrier wait is bounded (200 ms of %globaltimer); on expiry the thread
+// sets GS_DEV_TIMEOUT in the status word and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "step_common.cuh"
+
+namespace gs_detail {
+namespace {
+
+constexpr int kMaxThreads = 256;
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
+constexpr unsigned kMaxTileBytes = 200u * 1024u;
+
+struct TmaRegion {
+    int y0, x0, h, w;
+    float strength;
+    float inv_feather;
+    int edges;
+    int feather;              // F (ramp width in pixels; 0 = none)
+    int wbox;                 // box width in elements (w rounded up to whole 16-byte vectors)
+    int pad_;
+    const float* mask;
+    long long mask_bstride;
+    unsigned smem_off;        // byte offset of the region's box inside a stage
+    unsigned tile_bytes;      // CG * RB * wbox * element size
+};
+
+static_assert(sizeof(TmaRegion) % 4 == 0, "region descriptors are copied as 32-bit words");
+
+struct TmaParams {
+    CUtensorMap tm_x, tm_u, tm_c, tm_o, tm_m;
+    CUtensorMap tm_r[GS_MAX_REGIONS];
+    TmaRegion reg[GS_MAX_REGIONS];
+    void* x_out;
+    void* den_out;
+    const float* sig;
+    const int* step_idx;
+    const float* lut;
+    const unsigned char* present;
+    unsigned int* status;
+    long long n_tiles;
+    int B, C, H, W;
+    int RB, nbands, ncg;
+    int n_regions, n_sig, step, n_lut;
+    float cfg;
+    int has_u, has_c, mask_shared;
+    unsigned tile_bytes, plane_bytes, mask_bytes;
+    unsigned off_x, off_u, off_c, off_o, off_m;
+};
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about kSuspendNs pass, instead of spinning on issue slots
+// that co-resident CTAs could use.
+constexpr unsigned kSuspendNs = 1000000u;
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete; false after the time limit.
+__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_3d(unsigned dst, const CUtensorMap* map, int x, int y,
+                                            int z, unsigned bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<unsigned long long>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<unsigned long long>(map))
+                 : "memory");
+}
+
+__device__ __forceinline__ void flag(unsigned int* status, unsigned bits) {
+    if (status != nullptr) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ bool band_hits(const TmaRegion& R, int y_band, int RB) {
+    return y_band < R.y0 + R.h && y_band + RB > R.y0;
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ Raw<T, VEC> ld_smem(const unsigned char* base, unsigned byte_off) {
+    Raw<T, VEC> r;
+    const uint4 v = *reinterpret_cast<const uint4*>(base + byte_off);
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+    r.w[2] = v.z;
+    r.w[3] = v.w;
+    return r;
+}
+
+// ---- the kernel ---------------------------------------------------------------
+// One CTA per tile.  Thread 0 arms the CTA's mbarrier with the tile's byte count
+// and issues its TMA boxes; every thread then waits on the barrier and computes
+// VEC pixels x CG channels of one row of the band from shared memory.
+template <typename T, int CG, bool REG, bool INP>
+__global__ void __launch_bounds__(kMaxThreads)
+    guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
+    using S = typename T::scalar;
+    constexpr int VEC = 16 / static_cast<int>(sizeof(S));
+    constexpr int NP = VEC / 2;
+    constexpr unsigned ES = sizeof(S);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<unsigned long long>(smem_raw) + 127ull) & ~127ull);
+    unsigned long long* full = reinterpret_cast<unsigned long long*>(smem);
+    const unsigned char* st = smem + 128;
+
+    const long long t = blockIdx.x;
+    const int per_b = p.ncg * p.nbands;
+    const int b = static_cast<int>(t / per_b);
+    const int rem = static_cast<int>(t - static_cast<long long>(b) * per_b);
+    const int cgi = rem / p.nbands;
+    const int band = rem - cgi * p.nbands;
+    const int y_band = band * p.RB;
+    const int z = b * p.C + cgi * CG;
+    const bool has_u = p.has_u != 0, has_c = p.has_c != 0;
+    const bool inpaint = INP && (p.present == nullptr || __ldg(p.present + b) != 0);
+
+    // Region descriptors: one parallel copy from kernel parameters to shared
+    // memory (a runtime-indexed loop over the parameter copy would serialise one
+    // constant-cache miss per region).
+    __shared__ TmaRegion regs[REG ? GS_MAX_REGIONS : 1];
+    if constexpr (REG) {
+        const int words = p.n_regions * static_cast<int>(sizeof(TmaRegion) / 4);
+        const int* src = reinterpret_cast<const int*>(p.reg);
+        int* dst = reinterpret_cast<int*>(regs);
+        for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+    }
+    if (threadIdx.x == 0) {
+        // Start fetching the tensor-map descriptors while the CTA sets up.
+        prefetch_map(&p.tm_x);
+        if (has_u) prefetch_map(&p.tm_u);
+        if (has_c) prefetch_map(&p.tm_c);
+        if (inpaint) {
+            prefetch_map(&p.tm_o);
+            prefetch_map(&p.tm_m);
+        }
+        mbar_init(smem_u32(full), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    grid_dependency_wait();
+    grid_dependents_launch();
+
+    if (threadIdx.x == 0) {
+        unsigned bytes = p.plane_bytes;
+        if (has_u) bytes += p.plane_bytes;
+        if (has_c) bytes += p.plane_bytes;
+        if (inpaint) bytes += p.plane_bytes + p.mask_bytes;
+        if constexpr (REG) {
+            for (int r = 0; r < p.n_regions; ++r)
+                if (band_hits(regs[r], y_band, p.RB)) bytes += regs[r].tile_bytes;
+        }
+        const unsigned bar = smem_u32(full);
+        const unsigned s0 = smem_u32(st);
+        mbar_expect_tx(bar, bytes);
+        tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
+        if (has_u) tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
+        if (has_c) tma_load_3d(s0 + p.off_c, &p.tm_c, 0, y_band, z, bar);
+        if (inpaint) {
+            tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, bar);
+            tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, bar);
+        }
+        if constexpr (REG) {
+            for (int r = 0; r < p.n_regions; ++r) {
+                const TmaRegion& R = regs[r];
+                if (band_hits(R, y_band, p.RB))
+                    tma_load_3d(s0 + R.smem_off, &p.tm_r[r], 0, y_band - R.y0, z, bar);
+            }
+        }
+    }
+
+    // Per-sample parameters, read while the tile is in flight.
+    const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
+    const bool in_range = idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
+    const int si = in_range ? idx : 0;
+    const float s = p.lut != nullptr ? __ldg(p.lut + si) : p.cfg;
+    const float sigma = __ldg(p.sig + si);
+    const float sigma_next = __ldg(p.sig + si + 1);
+    const bool sigma_ok = sigma > 0.0f && sigma <= 3.402823466e38f;
+    const bool uncond_ok = has_u || s == 1.0f;
+
+    const int gpr = p.W / VEC;
+    const int row = threadIdx.x / gpr;
+    const int x0 = (threadIdx.x - row * gpr) * VEC;
+    const int y = y_band + row;
+
+    if (!mbar_wait(smem_u32(full), 0)) {
+        flag(p.status, GS_DEV_TIMEOUT);
+        return;
+    }
+    if (!(in_range && sigma_ok && uncond_ok)) {
+        if (threadIdx.x == 0 && band == 0 && cgi == 0) {
+            unsigned bits = 0;
+            if (!in_range) bits |= GS_DEV_STEP_RANGE;
+            else if (!sigma_ok) bits |= GS_DEV_SIGMA;
+            if (in_range && !uncond_ok) bits |= GS_DEV_NEED_UNCOND;
+            flag(p.status, bits);
+        }
+        return;
+    }
+    if (y >= p.H) return;
+
+    const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
+    const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
+
+    // positive branch
+    f2 pos[CG][NP];
+    if constexpr (REG) {
+        float wsum[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) wsum[j] = has_c ? 1.0f : 0.0f;
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+            if (has_c) {
+                const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_c, k * kstride + pix);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(v, q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) pos[k][q] = splat2(0.0f);
+            }
+        }
+        for (int r = 0; r < p.n_regions; ++r) {
+            const TmaRegion& R = regs[r];
+            if (y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w) continue;
+            const int ty = y - R.y0;
+            float wrow = R.strength;
+            if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
+            if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
+            const int xs = x0 - R.x0;
+            float wj[VEC];
+            // Fast path: all VEC pixels inside the region and clear of the side
+            // ramps (1/F > 0 only when some edge ramps; the ramp is 1 from t = F-1 on).
+            const int lpad = (R.edges & kEdgeLeft) ? R.feather - 1 : 0;
+            const int rpad = (R.edges & kEdgeRight) ? R.feather - 1 : 0;
+            if (xs >= lpad && xs + VEC - 1 <= R.w - 1 - rpad && R.mask == nullptr) {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) wj[j] = wrow;
+            } else {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const int tx = xs + j;
+                    float f = wrow;
+                    if (R.edges & kEdgeLeft) f = f * ramp(tx, R.feather, R.inv_feather);
+                    if (R.edges & kEdgeRight) f = f * ramp(R.w - 1 - tx, R.feather, R.inv_feather);
+                    wj[j] = f;
+                }
+                if (R.mask != nullptr) {
+                    const float* mrow =
+                        R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        if (xs + j >= 0 && xs + j < R.w) wj[j] = wj[j] * __ldg(mrow + xs + j);
+                }
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) wj[j] = (xs + j >= 0 && xs + j < R.w) ? wj[j] : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) wsum[j] = wsum[j] + wj[j];
+            f2 w2[NP];
+#pragma unroll
+            for (int q = 0; q < NP; ++q) w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
+            // box row `row` of this region's tile is frame row y
+            const int q0 = floor_div(xs, VEC);
+            const int sh = xs - q0 * VEC;
+            const int nq = R.wbox / VEC;
+            const bool lo_ok = q0 >= 0 && q0 < nq;
+            const bool hi_ok = sh != 0 && q0 + 1 >= 0 && q0 + 1 < nq;
+            const unsigned rbase = R.smem_off + static_cast<unsigned>(row) * R.wbox * ES;
+            const unsigned rk = static_cast<unsigned>(p.RB) * R.wbox * ES;
+#pragma unroll
+            for (int k = 0; k < CG; ++k) {
+                Raw<T, VEC> lo, hi;
+#pragma unroll
+                for (int i = 0; i < Raw<T, VEC>::kWords; ++i) lo.w[i] = hi.w[i] = 0u;
+                if (lo_ok) lo = ld_smem<T, VEC>(st, rbase + k * rk + q0 * 16);
+                if (hi_ok) hi = ld_smem<T, VEC>(st, rbase + k * rk + (q0 + 1) * 16);
+                // Columns outside [0, w) are zeros (TMA fills the box past the
+                // slab's width, and vectors outside the box are not read), so no
+                // pixel outside the region can bring a non-finite value.
+                const Raw<T, VEC> win = window<T, VEC>(lo, hi, sh);
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    pos[k][q] = fma2(w2[q], widen2<T, VEC>(win, q), pos[k][q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            const float i0 = wsum[2 * q] > 0.0f ? __frcp_rn(wsum[2 * q]) : 0.0f;
+            const float i1 = wsum[2 * q + 1] > 0.0f ? __frcp_rn(wsum[2 * q + 1]) : 0.0f;
+            const f2 inv = mk2(i0, i1);
+#pragma unroll
+            for (int k = 0; k < CG; ++k) pos[k][q] = mul2(pos[k][q], inv);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+            const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_c, k * kstride + pix);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(v, q);
+        }
+    }
+
+    // combine, inpaint blend, Euler, round and store
+    const f2 s2 = splat2(s);
+    const f2 oms2 = splat2(1.0f - s);
+    const f2 r2 = splat2(__fdiv_rn(sigma_next, sigma));
+    f2 m2[NP], omm2[NP];
+    if (INP && inpaint) {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(
+                st + p.off_m + (static_cast<unsigned>(row) * p.W + x0 + 4 * q) * 4u);
+            m2[2 * q] = mk2(v.x, v.y);
+            m2[2 * q + 1] = mk2(v.z, v.w);
+        }
+#pragma unroll
+        for (int q = 0; q < NP; ++q) omm2[q] = sub2(splat2(1.0f), m2[q]);
+    }
+    const long long plane = static_cast<long long>(p.H) * p.W;
+    const long long gbase = static_cast<long long>(z) * plane + static_cast<long long>(y) * p.W + x0;
+#pragma unroll
+    for (int k = 0; k < CG; ++k) {
+        const Raw<T, VEC> xv = ld_smem<T, VEC>(st + p.off_x, k * kstride + pix);
+        Raw<T, VEC> uv, ov, xo, dn;
+        if (has_u) uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+        if (INP && inpaint) ov = ld_smem<T, VEC>(st + p.off_o, k * kstride + pix);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            f2 pred = pos[k][q];
+            if (has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(uv, q)));
+            f2 den = pred;
+            if (INP && inpaint) den = fma2(m2[q], pred, mul2(omm2[q], widen2<T, VEC>(ov, q)));
+            const f2 xn = fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den);
+            narrow2<T, VEC>(xo, q, xn);
+            if (p.den_out != nullptr) narrow2<T, VEC>(dn, q, den);
+        }
+        store_raw<T, VEC>(p.x_out, gbase + k * plane, xo);
+        if (p.den_out != nullptr) store_raw<T, VEC>(p.den_out, gbase + k * plane, dn);
+    }
+}
+
+// ---- host side ------------------------------------------------------------------
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiled>(nullptr);
+        return reinterpret_cast<EncodeTiled>(f);
+    }();
+    return fn;
+}
+
+// A 3-D tiled map of a dense [d2][d1][d0] tensor with a [b2][b1][b0] box.
+bool encode3d(CUtensorMap* m, CUtensorMapDataType dt, unsigned esize, const void* base,
+              unsigned long long d0, unsigned long long d1, unsigned long long d2,
+              unsigned long long pitch_elems, unsigned b0, unsigned b1, unsigned b2) {
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {pitch_elems * esize, pitch_elems * d1 * esize};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encoder()(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* q) { return (reinterpret_cast<unsigned long long>(q) & 15ull) == 0; }
+
+unsigned round128(unsigned v) { return (v + 127u) & ~127u; }
+
+int gcd_int(int a, int b) {
+    while (b != 0) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+int sm_count_cached() {
+    static int cached[64] = {0};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+template <typename T, int CG, bool REG, bool INP>
+gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stream, unsigned flags) {
+    auto kern = guided_step_tma_kernel<T, CG, REG, INP>;
+    static std::mutex mu;
+    static unsigned smem_set[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GS_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (smem_set[dev] < smem) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return GS_ERR_CUDA;
+            }
+            smem_set[dev] = smem;
+        }
+    }
+    if (p.n_tiles > 0x7fffffffll) return GS_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.n_tiles));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (flags & GS_LAUNCH_PDL) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GS_ERR_CUDA;
+    }
+    return GS_OK;
+}
+
+template <typename T, bool REG, bool INP>
+gs_status launch_cg(TmaParams& p, int cg, int threads, unsigned smem, gs_stream stream,
+                    unsigned flags) {
+    if (cg == 4) return launch_kernel<T, 4, REG, INP>(p, threads, smem, stream, flags);
+    if (cg == 2) return launch_kernel<T, 2, REG, INP>(p, threads, smem, stream, flags);
+    return launch_kernel<T, 1, REG, INP>(p, threads, smem, stream, flags);
+}
+
+template <typename T>
+gs_status launch_features(TmaParams& p, int cg, int threads, unsigned smem, bool reg, bool inp,
+                          gs_stream stream, unsigned flags) {
+    if (reg && inp) return launch_cg<T, true, true>(p, cg, threads, smem, stream, flags);
+    if (reg) return launch_cg<T, true, false>(p, cg, threads, smem, stream, flags);
+    if (inp) return launch_cg<T, false, true>(p, cg, threads, smem, stream, flags);
+    return launch_cg<T, false, false>(p, cg, threads, smem, stream, flags);
+}
+
+}  // namespace
+
+// Launch the TMA-pipelined step if the request fits it; *used says whether it did.
+gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_stream stream,
+                          bool* used, bool dry_run) {
+    *used = false;
+    if (flags & GS_LAUNCH_NO_TMA) return GS_OK;
+    if (encoder() == nullptr) return GS_OK;
+    const unsigned es = dtype == GS_DTYPE_F32 ? 4u : 2u;
+    const int vec = static_cast<int>(16u / es);
+    const int B = sp.B, C = sp.C, H = sp.H, W = sp.W;
+    if ((static_cast<unsigned>(W) * es) % 16u != 0 || W > 256) return GS_OK;
+    if (!aligned16(sp.x) || !aligned16(sp.x_out)) return GS_OK;
+    if (sp.den_out != nullptr && !aligned16(sp.den_out)) return GS_OK;
+    if (sp.u != nullptr && !aligned16(sp.u)) return GS_OK;
+    if (sp.c != nullptr && !aligned16(sp.c)) return GS_OK;
+    const bool inp = sp.imask != nullptr;
+    if (inp && (!aligned16(sp.orig) || !aligned16(sp.imask) ||
+                (sp.imask_bstride != 0 && sp.imask_bstride != static_cast<long long>(H) * W)))
+        return GS_OK;
+    if (static_cast<long long>(B) * C > (1ll << 31) - 1) return GS_OK;
+    for (int r = 0; r < sp.n_regions; ++r) {
+        const DevRegion& R = sp.reg[r];
+        if (!R.vec_ok) return GS_OK;
+        const int wbox = (R.w + vec - 1) / vec * vec;
+        if (wbox > 256 || wbox > R.pitch) return GS_OK;
+    }
+
+    // Channels per tile: up to 4, fewer when 4 would leave under eight tiles of
+    // 64 threads per SM (small steps are latency-bound: shorter threads, more of
+    // them).  GS_TMA_CHANNELS=1|2|4 overrides (a tuning knob).
+    const int sms_for_cg = sm_count_cached();
+    int cg = C % 4 == 0 ? 4 : (C % 2 == 0 ? 2 : 1);
+    {
+        const long long pix_groups = static_cast<long long>(B) * H * (W / vec);
+        while (cg > 1 && C % (cg / 2) == 0 && pix_groups * (C / cg) < 8ll * 64 * sms_for_cg)
+            cg /= 2;
+        static const int cg_override = [] {
+            const char* e = getenv("GS_TMA_CHANNELS");
+            const int v = e != nullptr ? atoi(e) : 0;
+            return (v == 1 || v == 2 || v == 4) ? v : 0;
+        }();
+        if (cg_override != 0 && C % cg_override == 0) cg = cg_override;
+    }
+    const int gpr = W / vec;
+    const int rb0 = 32 / gcd_int(gpr, 32);             // smallest band with whole warps
+    if (rb0 * gpr > kMaxThreads) return GS_OK;
+    // About 128 threads per tile; smaller bands when that leaves fewer than four
+    // tiles per SM, so that small steps still spread over every SM.
+    int rb = rb0 * std::max(1, 128 / (rb0 * gpr));
+    const int sms = sm_count_cached();
+    auto tiles_for = [&](int band) {
+        return static_cast<long long>(B) * (C / cg) * ((H + band - 1) / band);
+    };
+    while (rb > rb0 && rb * gpr > 64 && tiles_for(rb) < 4ll * sms) rb -= rb0;
+    static const int rows_override = [] {
+        const char* e = getenv("GS_TMA_ROWS");
+        return e != nullptr ? atoi(e) : 0;
+    }();
+    if (rows_override > 0 && rows_override % rb0 == 0 && rows_override * gpr <= kMaxThreads)
+        rb = rows_override;
+    const int threads = rb * gpr;
+
+    TmaParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = B;
+    p.C = C;
+    p.H = H;
+    p.W = W;
+    p.RB = rb;
+    p.nbands = (H + rb - 1) / rb;
+    p.ncg = C / cg;
+    p.n_tiles = static_cast<long long>(B) * p.ncg * p.nbands;
+    p.x_out = sp.x_out;
+    p.den_out = sp.den_out;
+    p.sig = sp.sig;
+    p.step_idx = sp.step_idx;
+    p.lut = sp.lut;
+    p.present = sp.present;
+    p.status = sp.status;
+    p.n_sig = sp.n_sig;
+    p.step = sp.step;
+    p.n_lut = sp.n_lut;
+    p.cfg = sp.cfg;
+    p.has_u = sp.u != nullptr;
+    p.has_c = sp.c != nullptr;
+    p.mask_shared = inp && sp.imask_bstride == 0;
+    p.n_regions = sp.n_regions;
+
+    // stage layout
+    const unsigned plane = static_cast<unsigned>(cg) * rb * W * es;
+    const unsigned maskb = static_cast<unsigned>(rb) * W * 4u;
+    unsigned off = 0;
+    p.plane_bytes = plane;
+    p.mask_bytes = maskb;
+    p.off_x = off;
+    off += round128(plane);
+    if (p.has_u) { p.off_u = off; off += round128(plane); }
+    if (p.has_c) { p.off_c = off; off += round128(plane); }
+    if (inp) {
+        p.off_o = off;
+        off += round128(plane);
+        p.off_m = off;
+        off += round128(maskb);
+    }
+    for (int r = 0; r < sp.n_regions; ++r) {
+        const DevRegion& R = sp.reg[r];
+        TmaRegion& d = p.reg[r];
+        d.y0 = R.y0;
+        d.x0 = R.x0;
+        d.h = R.h;
+        d.w = R.w;
+        d.strength = R.strength;
+        d.inv_feather = R.inv_feather;
+        d.edges = R.edges;
+        d.feather = R.feather;
+        d.wbox = (R.w + vec - 1) / vec * vec;
+        d.mask = R.mask;
+        d.mask_bstride = R.mask_bstride;
+        d.tile_bytes = static_cast<unsigned>(cg) * rb * d.wbox * es;
+        d.smem_off = off;
+        off += round128(d.tile_bytes);
+    }
+    p.tile_bytes = off;
+    if (p.tile_bytes > kMaxTileBytes) return GS_OK;
+    const unsigned smem = 128u + 128u + p.tile_bytes;   // alignment slack + mbarrier line
+
+    // tensor maps
+    const CUtensorMapDataType dt = dtype == GS_DTYPE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == GS_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const unsigned long long bc = static_cast<unsigned long long>(B) * C;
+    bool ok = encode3d(&p.tm_x, dt, es, sp.x, W, H, bc, W, W, rb, cg);
+    if (p.has_u) ok = ok && encode3d(&p.tm_u, dt, es, sp.u, W, H, bc, W, W, rb, cg);
+    if (p.has_c) ok = ok && encode3d(&p.tm_c, dt, es, sp.c, W, H, bc, W, W, rb, cg);
+    if (inp) {
+        ok = ok && encode3d(&p.tm_o, dt, es, sp.orig, W, H, bc, W, W, rb, cg);
+        ok = ok && encode3d(&p.tm_m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sp.imask, W, H,
+                            p.mask_shared ? 1 : B, W, W, rb, 1);
+    }
+    for (int r = 0; r < sp.n_regions && ok; ++r) {
+        const DevRegion& R = sp.reg[r];
+        // Inner extent w (not pitch): TMA zero-fills box columns w .. wbox-1.
+        ok = encode3d(&p.tm_r[r], dt, es, R.out, static_cast<unsigned long long>(R.w),
+                      static_cast<unsigned long long>(R.h), bc,
+                      static_cast<unsigned long long>(R.pitch),
+                      static_cast<unsigned>(p.reg[r].wbox), rb, cg);
+    }
+    if (!ok) return GS_OK;
+    if (dry_run) {
+        *used = true;
+        return GS_OK;
+    }
+
+    gs_status st;
+    const bool reg = sp.n_regions > 0;
+    switch (dtype) {
+        case GS_DTYPE_F32:
+            st = launch_features<F32>(p, cg, threads, smem, reg, inp, stream, flags);
+            break;
+        case GS_DTYPE_BF16:
+            st = launch_features<BF16>(p, cg, threads, smem, reg, inp, stream, flags);
+            break;
+        default:
+            st = launch_features<F16>(p, cg, threads, smem, reg, inp, stream, flags);
+            break;
+    }
+    if (st == GS_OK) *used = true;
+    return st;
+}
+
+}  // namespace gs_detail

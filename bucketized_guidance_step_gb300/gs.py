@@ -27,16 +27,20 @@ _lock = threading.Lock()
 # ---- constants mirrored from include/gs.h ---------------------------------
 GS_OK, GS_ERR_INVALID_ARG, GS_ERR_UNSUPPORTED, GS_ERR_CUDA = 0, 1, 2, 3
 GS_ERR_STEP_RANGE, GS_ERR_NEED_UNCOND, GS_ERR_SIGMA, GS_ERR_CAPACITY = 4, 5, 6, 7
-GS_DEV_STEP_RANGE, GS_DEV_NEED_UNCOND, GS_DEV_SIGMA = 1, 2, 4
+GS_ERR_TIMEOUT = 8
+GS_DEV_STEP_RANGE, GS_DEV_NEED_UNCOND, GS_DEV_SIGMA, GS_DEV_TIMEOUT = 1, 2, 4, 8
 GS_DTYPE_F32, GS_DTYPE_BF16, GS_DTYPE_F16 = 0, 1, 2
 GS_SCHED_KARRAS, GS_SCHED_NORMAL = 0, 1
 GS_CURVE_LINEAR, GS_CURVE_STEP, GS_CURVE_TABLE = 0, 1, 2
 GS_MAX_REGIONS = 16
 GS_LAUNCH_PDL = 1
+GS_LAUNCH_NO_TMA = 2
 GS_ABI_VERSION = 1
 
 EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_guided_step",
-           "gs_status_from_word", "gs_status_string", "gs_abi_version")
+           "gs_step_kernel_kind", "gs_status_from_word", "gs_status_string", "gs_abi_version")
+GS_KERNEL_SCALAR, GS_KERNEL_VECTOR, GS_KERNEL_TMA = 0, 1, 2
+KERNEL_NAMES = {0: "scalar", 1: "vector", 2: "tma"}
 
 
 class GSLibraryError(RuntimeError):
@@ -113,12 +117,13 @@ def load() -> ctypes.CDLL:
         lib.gs_bucket_plan.argtypes = [i32, i32, ctypes.POINTER(CurveDesc), p, p, p]
         lib.gs_mask_prepare.argtypes = [p, i32, i32, i32, p, i32, i32, p]
         lib.gs_guided_step.argtypes = [ctypes.POINTER(StepArgs), p]
+        lib.gs_step_kernel_kind.argtypes = [ctypes.POINTER(StepArgs), p]
         lib.gs_status_from_word.argtypes = [ctypes.c_uint32]
         lib.gs_status_string.argtypes = [i32]
         lib.gs_status_string.restype = ctypes.c_char_p
         lib.gs_abi_version.argtypes = []
         for f in ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_guided_step",
-                  "gs_status_from_word", "gs_abi_version"):
+                  "gs_step_kernel_kind", "gs_status_from_word", "gs_abi_version"):
             getattr(lib, f).restype = i32
         if lib.gs_abi_version() != GS_ABI_VERSION:
             raise GSLibraryError("libgs.so ABI version does not match the binding")
@@ -251,7 +256,7 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
                    step: int = 0, scale_lut=None, cfg: float = 1.0,
                    regions: Sequence[Region] = (), inpaint_mask=None, mask_present=None,
                    original=None, x_out=None, denoised_out=None, status=None,
-                   pdl: bool = False):
+                   pdl: bool = False, tma: bool = True):
     """Build a gs_step_args (and the region array it points to) from tensors."""
     torch = _torch()
     B, C, H, W = x.shape
@@ -317,7 +322,7 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
     a.mask_present = _dptr(mask_present, "mask_present", torch.uint8)
     a.original = _dptr(original, "original", dt)
     a.dev_status = _dptr(status, "status", torch.int32)
-    a.launch_flags = GS_LAUNCH_PDL if pdl else 0
+    a.launch_flags = (GS_LAUNCH_PDL if pdl else 0) | (0 if tma else GS_LAUNCH_NO_TMA)
     return a, reg_arr
 
 
@@ -326,13 +331,21 @@ def launch_step(args: StepArgs, stream=None) -> None:
     _check("gs_guided_step", load().gs_guided_step(ctypes.byref(args), _stream_ptr(stream)))
 
 
+def kernel_kind(args: StepArgs) -> str:
+    """gs_step_kernel_kind: "tma", "vector" or "scalar" for prepared arguments."""
+    k = ctypes.c_int32(-1)
+    _check("gs_step_kernel_kind", load().gs_step_kernel_kind(ctypes.byref(args), ctypes.byref(k)))
+    return KERNEL_NAMES[k.value]
+
+
 def guided_step(x, *, sigmas, stream=None, **kw):
     """gs_guided_step: one fused guided denoise step; returns x_out (x itself by default).
 
     Keyword arguments follow gs_step_args: uncond / cond or stacked, regions,
     step_idx (int32 [B]) or step, scale_lut (fp32) or cfg, inpaint_mask
     ([B or 1, 1, H, W] fp32), mask_present (uint8 [B]), original, x_out,
-    denoised_out, status (int32 [1], device flags OR-ed in), pdl.
+    denoised_out, status (int32 [1], device flags OR-ed in), pdl, tma (False forces
+    the register-streaming kernel).
     """
     args, _keep = make_step_args(x, sigmas=sigmas, **kw)
     launch_step(args, stream)

@@ -46,13 +46,16 @@ typedef enum gs_status {
     GS_ERR_NEED_UNCOND = 5,   /* device: a sample's scale was not 1 but no uncond
                                  branch was given; that sample was skipped            */
     GS_ERR_SIGMA = 6,         /* device: sigma[i] <= 0 or not finite; sample skipped */
-    GS_ERR_CAPACITY = 7       /* output buffer too small                              */
+    GS_ERR_CAPACITY = 7,      /* output buffer too small                              */
+    GS_ERR_TIMEOUT = 8        /* device: a pipeline wait gave up (200 ms); the step's
+                                 output is incomplete                                 */
 } gs_status;
 
 /* Bits of the device status word (uint32, caller-owned, zeroed by the caller). */
 #define GS_DEV_STEP_RANGE  1u
 #define GS_DEV_NEED_UNCOND 2u
 #define GS_DEV_SIGMA       4u
+#define GS_DEV_TIMEOUT     8u
 
 /* Storage types of latents and model outputs; arithmetic is always fp32. */
 enum { GS_DTYPE_F32 = 0, GS_DTYPE_BF16 = 1, GS_DTYPE_F16 = 2 };
@@ -195,9 +198,11 @@ typedef struct gs_region {
 } gs_region;
 
 /* launch_flags */
-#define GS_LAUNCH_PDL 1u   /* launch with programmatic dependent launch: the kernel
-                              may be scheduled before the previous kernel in the
-                              stream ends; it waits for it before any memory access */
+#define GS_LAUNCH_PDL    1u  /* launch with programmatic dependent launch: the kernel
+                                may be scheduled before the previous kernel in the
+                                stream ends; it waits for it before any memory access */
+#define GS_LAUNCH_NO_TMA 2u  /* use the register-streaming kernel even where the
+                                TMA-pipelined one applies (same results)            */
 
 typedef struct gs_step_args {
     int32_t B, C, H, W;         /* latent batch, channels, rows, columns (all >= 1)      */
@@ -269,10 +274,22 @@ typedef struct gs_step_args {
  * that need the missing uncond branch are skipped (x_out and denoised_out are
  * not written for them) and flagged in dev_status.
  *
- * Alignment: when every latent-shaped pointer is 16-byte aligned and W is a
- * multiple of 8 the kernel moves 16-byte vectors; otherwise it runs a scalar
- * variant with the same results.  x_out may alias x (or another latent-shaped
- * input); it must not overlap region outputs or masks.
+ * Kernels (all give the same results):
+ *   - TMA-pipelined: used when every latent-shaped pointer is 16-byte aligned,
+ *     W * element size is a multiple of 16 bytes, W <= 256, every region output
+ *     is 16-byte aligned with a 16-byte-multiple row pitch and rounds up to at
+ *     most 256 columns, and the inpaint mask is per-sample dense or shared.
+ *     Tensor maps are encoded per call (host cost of a few microseconds).
+ *     One CTA per tile of (sample, up to 4 channels, a band of rows); the band
+ *     height is chosen for about 128 threads per tile, or set with the
+ *     environment variable GS_TMA_ROWS (a tuning knob; results do not change).
+ *   - register-streaming with 16-byte vectors: pointers 16-byte aligned and W a
+ *     multiple of 16 bytes / element size; one item of 8 (16-bit) or 4 (fp32)
+ *     pixels x 2 channels per thread, or as many channels (1, 2 or 4) as the
+ *     environment variable GS_STEP_CHANNELS asks (a tuning knob);
+ *   - scalar: anything else.
+ * x_out may alias x (or another latent-shaped input); it must not overlap
+ * region outputs or masks.
  *
  * Errors: GS_ERR_INVALID_ARG (NULL required pointer, size < 1, region outside
  * the frame or pitch < w, n_regions out of range, step out of range with
@@ -280,6 +297,16 @@ typedef struct gs_step_args {
  * dtype), GS_ERR_CUDA (launch failure).  Device-found errors: see dev_status.
  */
 gs_status gs_guided_step(const gs_step_args* args, gs_stream stream);
+
+/* Kernels gs_guided_step chooses between (same results, different data movement). */
+enum { GS_KERNEL_SCALAR = 0, GS_KERNEL_VECTOR = 1, GS_KERNEL_TMA = 2 };
+
+/*
+ * gs_step_kernel_kind -- which kernel gs_guided_step would launch for these
+ * arguments, after the same argument checks, without launching anything.
+ * kind: host int32; receives GS_KERNEL_*.  Errors: as gs_guided_step's checks.
+ */
+gs_status gs_step_kernel_kind(const gs_step_args* args, int32_t* kind);
 
 /* Decode a device status word into the first gs_status it carries (GS_OK if 0). */
 gs_status gs_status_from_word(uint32_t word);

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.gs_abi_version() == gs.GS_ABI_VERSION
-    for code in range(8):
+    for code in range(9):
         assert gs.status_string(code) not in ("", "unknown status")
     assert gs.status_string(99) == "unknown status"
     assert gs.status_from_word(0) == gs.GS_OK

@@ -19,7 +19,20 @@ from bucketized_guidance_step_gb300 import gs
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 DTYPES = [torch.float32, torch.bfloat16, torch.float16]
-SHAPES = [(3, 4, 16, 32), (2, 3, 5, 7)]          # vector path, scalar path
+SHAPES = [(3, 4, 16, 32), (2, 3, 5, 7)]          # vector/TMA path, scalar path
+
+
+@pytest.fixture(params=[True, False], ids=["tma", "registers"], autouse=True)
+def kernel_choice(request, monkeypatch):
+    """Run every invariant on the TMA-pipelined kernel and on the register kernel."""
+    orig = gs.make_step_args
+
+    def make(*a, **kw):
+        kw.setdefault("tma", request.param)
+        return orig(*a, **kw)
+
+    monkeypatch.setattr(gs, "make_step_args", make)
+    return request.param
 
 
 def rnd(shape, seed, dtype):

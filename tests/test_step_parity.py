@@ -30,7 +30,8 @@ def _cuda(t):
 
 def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None,
              step: int = None, region_masks: bool = False, offset: int = 0,
-             uncond_none: bool = False, want_den: bool = False, pitch_align: int = 8):
+             uncond_none: bool = False, want_den: bool = False, pitch_align: int = 8,
+             tma: bool = True, expect_kernel: str = None):
     """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok)."""
     inp = step_inputs(wl, step_seed, B=B, C=C, H=H, W=W, region_masks=region_masks,
                       pitch_align=pitch_align)
@@ -70,7 +71,7 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     kw = dict(uncond=dev_latent(u), cond=dev_latent(inp.cond), regions=regs,
               sigmas=torch.from_numpy(sig).to(DEV), x_out=outd, denoised_out=dend,
-              status=status)
+              status=status, tma=tma)
     if inp.step_idx is not None:
         kw["step_idx"] = _cuda(inp.step_idx)
     else:
@@ -82,7 +83,13 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     if lat is not None:
         kw.update(inpaint_mask=_cuda(lat), original=dev_latent(inp.original),
                   mask_present=_cuda(inp.mask_present))
-    gs.guided_step(xd, **kw)
+    args, _keep = gs.make_step_args(xd, **kw)
+    kind = gs.kernel_kind(args)
+    if expect_kernel is not None:
+        assert kind == expect_kernel, (kind, expect_kernel)
+    if not tma:
+        assert kind != "tma"
+    gs.launch_step(args)
     torch.cuda.synchronize()
     got = to64(outd)
 
@@ -115,9 +122,10 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     return rep, got, ref, ok
 
 
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
 @pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
-def test_workload_full_size(wl):
-    rep, *_ = run_case(wl)
+def test_workload_full_size(wl, tma):
+    rep, *_ = run_case(wl, tma=tma, expect_kernel="tma" if tma else "vector")
     assert rep.n == wl.elements
     print(f"{wl.name}: n={rep.n} primary={rep.primary} floor_only={rep.floor_only} "
           f"worst={rep.worst_ratio:.3f} normwise={rep.normwise:.2e}")
@@ -147,16 +155,17 @@ def test_cfg_loop_20_steps_stepwise():
     assert sig[-1] == 0.0
 
 
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1), (3, 3, 13, 11), (2, 6, 7, 24), (1, 4, 5, 8),
-                                   (5, 2, 16, 16)])
-def test_ragged_shapes_regions_inpaint(dtype, shape):
+                                   (5, 2, 16, 16), (2, 4, 37, 64), (1, 2, 3, 256)])
+def test_ragged_shapes_regions_inpaint(dtype, shape, tma):
     B, C, H, W = shape
     base = WORKLOADS[4]
     wl = Workload("ragged", B, C, H, W, dtype, base.schedule, base.guidance,
                   full_frame_cond=True, n_regions=3, region_side=(1, max(1, min(H, W))),
                   feather=3, inpaint=True, inpaint_samples=max(1, B // 2), seed=11)
-    run_case(wl, region_masks=True, want_den=True)
+    run_case(wl, region_masks=True, want_den=True, tma=tma)
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
@@ -164,19 +173,23 @@ def test_unaligned_pointers_take_scalar_path(dtype):
     base = WORKLOADS[3]
     wl = Workload("unaligned", 3, 4, 16, 24, dtype, base.schedule, base.guidance,
                   n_regions=2, inpaint=True, seed=12)
-    run_case(wl, offset=1)
+    run_case(wl, offset=1, expect_kernel="scalar")
 
 
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
 @pytest.mark.parametrize("pitch_align", [1, 8])
-def test_region_pitch_and_masks(pitch_align):
+def test_region_pitch_and_masks(pitch_align, tma):
     base = WORKLOADS[2]
     wl = Workload("regions", 4, 4, 40, 48, "fp16", base.schedule, base.guidance,
                   full_frame_cond=False, n_regions=16, region_side=(3, 40), seed=13)
-    run_case(wl, region_masks=True, pitch_align=pitch_align, step=5)
+    # a pitch that is not a 16-byte multiple keeps regions off the TMA path
+    want = ("tma" if tma and pitch_align == 8 else "vector")
+    run_case(wl, region_masks=True, pitch_align=pitch_align, step=5, tma=tma, expect_kernel=want)
 
 
-def test_every_scale_one_without_uncond():
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
+def test_every_scale_one_without_uncond(tma):
     base = WORKLOADS[1]
     wl = Workload("cfg1", 4, 4, 32, 32, "bf16", base.schedule, base.guidance.__class__(cfg=1.0),
                   seed=14)
-    run_case(wl, uncond_none=True)
+    run_case(wl, uncond_none=True, tma=tma)
