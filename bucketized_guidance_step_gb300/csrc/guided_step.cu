@@ -213,7 +213,7 @@ __device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* 
         accumulate_regions<T, VEC, CH>(p, regs, b, cc, p0, pos, wsum);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-            const float inv = wsum[j] > 0.0f ? __frcp_rn(wsum[j]) : 0.0f;
+            const float inv = recip_or_zero(wsum[j]);
 #pragma unroll
             for (int k = 0; k < CH; ++k) pos[k][j] = pos[k][j] * inv;
         }
@@ -422,8 +422,8 @@ __device__ __forceinline__ void step_item_vec(const StepParams& p, const DevRegi
         accumulate_regions_vec<T, VEC, CH>(p, regs, b, cc, p0, pos, wsum);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
-            const float i0 = wsum[2 * q] > 0.0f ? __frcp_rn(wsum[2 * q]) : 0.0f;
-            const float i1 = wsum[2 * q + 1] > 0.0f ? __frcp_rn(wsum[2 * q + 1]) : 0.0f;
+            const float i0 = recip_or_zero(wsum[2 * q]);
+            const float i1 = recip_or_zero(wsum[2 * q + 1]);
             const f2 inv = mk2(i0, i1);
 #pragma unroll
             for (int k = 0; k < CH; ++k) pos[k][q] = mul2(pos[k][q], inv);

@@ -294,6 +294,18 @@ __device__ __forceinline__ f2 sub2(f2 a, f2 b) {
     return r;
 }
 
+// 1 / w (hardware approximation, relative error below 2^-22, exact at powers of
+// two), or 0 where w <= 0 (a pixel no region covers): the normaliser of the
+// regional sum.
+__device__ __forceinline__ float recip_or_zero(float w) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(w));
+    return w > 0.0f ? r : 0.0f;
+}
+__device__ __forceinline__ f2 recip_or_zero2(f2 w) {
+    return mk2(recip_or_zero(lo_of(w)), recip_or_zero(hi_of(w)));
+}
+
 // Elements 2q and 2q+1 of a raw vector, widened exactly to an fp32 pair.
 template <typename T, int VEC>
 __device__ __forceinline__ f2 widen2(const Raw<T, VEC>& r, int q) {

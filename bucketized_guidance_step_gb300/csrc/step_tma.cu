@@ -149,6 +149,42 @@ __device__ __forceinline__ bool band_hits(const TmaRegion& R, int y_band, int RB
     return y_band < R.y0 + R.h && y_band + RB > R.y0;
 }
 
+// Weights of region R at pixels (y, x0 .. x0+VEC-1) of sample b: strength times
+// the feather ramps times the region mask, 0 outside the region.  Pixel groups
+// wholly inside the region and clear of its side ramps take a short path.
+template <int VEC>
+__device__ __forceinline__ void region_weights(const TmaRegion& R, int b, int y, int x0,
+                                               float (&wj)[VEC]) {
+    const int ty = y - R.y0;
+    float wrow = R.strength;
+    if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
+    if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
+    const int xs = x0 - R.x0;
+    const int lpad = (R.edges & kEdgeLeft) ? R.feather - 1 : 0;
+    const int rpad = (R.edges & kEdgeRight) ? R.feather - 1 : 0;
+    if (xs >= lpad && xs + VEC - 1 <= R.w - 1 - rpad && R.mask == nullptr) {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) wj[j] = wrow;
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        const int tx = xs + j;
+        float f = wrow;
+        if (R.edges & kEdgeLeft) f = f * ramp(tx, R.feather, R.inv_feather);
+        if (R.edges & kEdgeRight) f = f * ramp(R.w - 1 - tx, R.feather, R.inv_feather);
+        wj[j] = f;
+    }
+    if (R.mask != nullptr) {
+        const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            if (xs + j >= 0 && xs + j < R.w) wj[j] = wj[j] * __ldg(mrow + xs + j);
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) wj[j] = (xs + j >= 0 && xs + j < R.w) ? wj[j] : 0.0f;
+}
+
 template <typename T, int VEC>
 __device__ __forceinline__ Raw<T, VEC> ld_smem(const unsigned char* base, unsigned byte_off) {
     Raw<T, VEC> r;
@@ -161,9 +197,12 @@ __device__ __forceinline__ Raw<T, VEC> ld_smem(const unsigned char* base, unsign
 }
 
 // ---- the kernel ---------------------------------------------------------------
-// One CTA per tile.  Thread 0 arms the CTA's mbarrier with the tile's byte count
-// and issues its TMA boxes; every thread then waits on the barrier and computes
-// VEC pixels x CG channels of one row of the band from shared memory.
+// One CTA per tile; grid (band, channel group, sample), block (pixel group, row).
+// Thread 0 arms the CTA's mbarrier with the tile's byte count and issues its TMA
+// boxes.  While they are in flight every thread reads its sample's parameters
+// and, with regions, finds the regions touching its VEC pixels, their summed
+// weight and its reciprocal; then it waits and computes CG channels of its
+// pixels from shared memory.
 template <typename T, int CG, bool REG, bool INP>
 __global__ void __launch_bounds__(kMaxThreads)
     guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
@@ -178,13 +217,14 @@ __global__ void __launch_bounds__(kMaxThreads)
     unsigned long long* full = reinterpret_cast<unsigned long long*>(smem);
     const unsigned char* st = smem + 128;
 
-    const long long t = blockIdx.x;
-    const int per_b = p.ncg * p.nbands;
-    const int b = static_cast<int>(t / per_b);
-    const int rem = static_cast<int>(t - static_cast<long long>(b) * per_b);
-    const int cgi = rem / p.nbands;
-    const int band = rem - cgi * p.nbands;
+    const int band = blockIdx.x;
+    const int cgi = blockIdx.y;
+    const int b = blockIdx.z;
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+    const int row = threadIdx.y;
+    const int x0 = threadIdx.x * VEC;
     const int y_band = band * p.RB;
+    const int y = y_band + row;
     const int z = b * p.C + cgi * CG;
     const bool has_u = p.has_u != 0, has_c = p.has_c != 0;
     const bool inpaint = INP && (p.present == nullptr || __ldg(p.present + b) != 0);
@@ -197,9 +237,10 @@ __global__ void __launch_bounds__(kMaxThreads)
         const int words = p.n_regions * static_cast<int>(sizeof(TmaRegion) / 4);
         const int* src = reinterpret_cast<const int*>(p.reg);
         int* dst = reinterpret_cast<int*>(regs);
-        for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+        const int nthreads = blockDim.x * blockDim.y;
+        for (int i = tid; i < words; i += nthreads) dst[i] = src[i];
     }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         // Start fetching the tensor-map descriptors while the CTA sets up.
         prefetch_map(&p.tm_x);
         if (has_u) prefetch_map(&p.tm_u);
@@ -215,7 +256,7 @@ __global__ void __launch_bounds__(kMaxThreads)
     grid_dependency_wait();
     grid_dependents_launch();
 
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         unsigned bytes = p.plane_bytes;
         if (has_u) bytes += p.plane_bytes;
         if (has_c) bytes += p.plane_bytes;
@@ -243,7 +284,7 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
     }
 
-    // Per-sample parameters, read while the tile is in flight.
+    // ---- while the tile is in flight ----
     const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
     const bool in_range = idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
     const int si = in_range ? idx : 0;
@@ -252,18 +293,36 @@ __global__ void __launch_bounds__(kMaxThreads)
     const float sigma_next = __ldg(p.sig + si + 1);
     const bool sigma_ok = sigma > 0.0f && sigma <= 3.402823466e38f;
     const bool uncond_ok = has_u || s == 1.0f;
+    const bool live = in_range && sigma_ok && uncond_ok && y < p.H;
 
-    const int gpr = p.W / VEC;
-    const int row = threadIdx.x / gpr;
-    const int x0 = (threadIdx.x - row * gpr) * VEC;
-    const int y = y_band + row;
-
-    if (!mbar_wait(smem_u32(full), 0)) {
-        flag(p.status, GS_DEV_TIMEOUT);
-        return;
+    // Regions touching this thread's pixels.
+    unsigned hits = 0;
+    if constexpr (REG) {
+        if (live) {
+            for (int r = 0; r < p.n_regions; ++r) {
+                const TmaRegion& R = regs[r];
+                if (!(y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w))
+                    hits |= 1u << r;
+            }
+        }
     }
+    const f2 s2 = splat2(s);
+    const f2 oms2 = splat2(1.0f - s);
+    const f2 r2 = splat2(__fdiv_rn(sigma_next, sigma));
+
+    // ---- the tile ----
+    // One thread polls the mbarrier; the rest of the CTA sleeps at the CTA
+    // barrier, where waiting warps take no issue slots from co-resident CTAs.
+    __shared__ int tile_ok;
+    if (tid == 0) {
+        const bool ok = mbar_wait(smem_u32(full), 0);
+        if (!ok) flag(p.status, GS_DEV_TIMEOUT);
+        tile_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!tile_ok) return;
     if (!(in_range && sigma_ok && uncond_ok)) {
-        if (threadIdx.x == 0 && band == 0 && cgi == 0) {
+        if (tid == 0 && band == 0 && cgi == 0) {
             unsigned bits = 0;
             if (!in_range) bits |= GS_DEV_STEP_RANGE;
             else if (!sigma_ok) bits |= GS_DEV_SIGMA;
@@ -280,9 +339,9 @@ __global__ void __launch_bounds__(kMaxThreads)
     // positive branch
     f2 pos[CG][NP];
     if constexpr (REG) {
-        float wsum[VEC];
+        f2 wsum2[NP];
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) wsum[j] = has_c ? 1.0f : 0.0f;
+        for (int q = 0; q < NP; ++q) wsum2[q] = splat2(has_c ? 1.0f : 0.0f);
 #pragma unroll
         for (int k = 0; k < CG; ++k) {
             if (has_c) {
@@ -294,47 +353,23 @@ __global__ void __launch_bounds__(kMaxThreads)
                 for (int q = 0; q < NP; ++q) pos[k][q] = splat2(0.0f);
             }
         }
-        for (int r = 0; r < p.n_regions; ++r) {
+        while (hits != 0) {
+            const int r = __ffs(hits) - 1;
+            hits &= hits - 1;
             const TmaRegion& R = regs[r];
-            if (y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w) continue;
-            const int ty = y - R.y0;
-            float wrow = R.strength;
-            if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
-            if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
-            const int xs = x0 - R.x0;
             float wj[VEC];
-            // Fast path: all VEC pixels inside the region and clear of the side
-            // ramps (1/F > 0 only when some edge ramps; the ramp is 1 from t = F-1 on).
-            const int lpad = (R.edges & kEdgeLeft) ? R.feather - 1 : 0;
-            const int rpad = (R.edges & kEdgeRight) ? R.feather - 1 : 0;
-            if (xs >= lpad && xs + VEC - 1 <= R.w - 1 - rpad && R.mask == nullptr) {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) wj[j] = wrow;
-            } else {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const int tx = xs + j;
-                    float f = wrow;
-                    if (R.edges & kEdgeLeft) f = f * ramp(tx, R.feather, R.inv_feather);
-                    if (R.edges & kEdgeRight) f = f * ramp(R.w - 1 - tx, R.feather, R.inv_feather);
-                    wj[j] = f;
-                }
-                if (R.mask != nullptr) {
-                    const float* mrow =
-                        R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        if (xs + j >= 0 && xs + j < R.w) wj[j] = wj[j] * __ldg(mrow + xs + j);
-                }
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) wj[j] = (xs + j >= 0 && xs + j < R.w) ? wj[j] : 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) wsum[j] = wsum[j] + wj[j];
+            region_weights<VEC>(R, b, y, x0, wj);
             f2 w2[NP];
 #pragma unroll
-            for (int q = 0; q < NP; ++q) w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
-            // box row `row` of this region's tile is frame row y
+            for (int q = 0; q < NP; ++q) {
+                w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
+                wsum2[q] = add2(wsum2[q], w2[q]);
+            }
+            // Box row `row` of this region's tile is frame row y.  Columns outside
+            // [0, w) are zeros (TMA fills the box past the slab's width, and
+            // vectors outside the box are not read), so no pixel outside the
+            // region can bring a non-finite value.
+            const int xs = x0 - R.x0;
             const int q0 = floor_div(xs, VEC);
             const int sh = xs - q0 * VEC;
             const int nq = R.wbox / VEC;
@@ -349,9 +384,6 @@ __global__ void __launch_bounds__(kMaxThreads)
                 for (int i = 0; i < Raw<T, VEC>::kWords; ++i) lo.w[i] = hi.w[i] = 0u;
                 if (lo_ok) lo = ld_smem<T, VEC>(st, rbase + k * rk + q0 * 16);
                 if (hi_ok) hi = ld_smem<T, VEC>(st, rbase + k * rk + (q0 + 1) * 16);
-                // Columns outside [0, w) are zeros (TMA fills the box past the
-                // slab's width, and vectors outside the box are not read), so no
-                // pixel outside the region can bring a non-finite value.
                 const Raw<T, VEC> win = window<T, VEC>(lo, hi, sh);
 #pragma unroll
                 for (int q = 0; q < NP; ++q)
@@ -360,9 +392,7 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
-            const float i0 = wsum[2 * q] > 0.0f ? __frcp_rn(wsum[2 * q]) : 0.0f;
-            const float i1 = wsum[2 * q + 1] > 0.0f ? __frcp_rn(wsum[2 * q + 1]) : 0.0f;
-            const f2 inv = mk2(i0, i1);
+            const f2 inv = recip_or_zero2(wsum2[q]);
 #pragma unroll
             for (int k = 0; k < CG; ++k) pos[k][q] = mul2(pos[k][q], inv);
         }
@@ -376,9 +406,6 @@ __global__ void __launch_bounds__(kMaxThreads)
     }
 
     // combine, inpaint blend, Euler, round and store
-    const f2 s2 = splat2(s);
-    const f2 oms2 = splat2(1.0f - s);
-    const f2 r2 = splat2(__fdiv_rn(sigma_next, sigma));
     f2 m2[NP], omm2[NP];
     if (INP && inpaint) {
 #pragma unroll
@@ -492,10 +519,12 @@ gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stre
             smem_set[dev] = smem;
         }
     }
-    if (p.n_tiles > 0x7fffffffll) return GS_ERR_UNSUPPORTED;
+    if (p.B > 65535 || p.ncg > 65535) return GS_ERR_UNSUPPORTED;
+    const int gpr = threads / p.RB;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.n_tiles));
-    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.gridDim = dim3(static_cast<unsigned>(p.nbands), static_cast<unsigned>(p.ncg),
+                       static_cast<unsigned>(p.B));
+    cfg.blockDim = dim3(static_cast<unsigned>(gpr), static_cast<unsigned>(p.RB));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -549,7 +578,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     if (inp && (!aligned16(sp.orig) || !aligned16(sp.imask) ||
                 (sp.imask_bstride != 0 && sp.imask_bstride != static_cast<long long>(H) * W)))
         return GS_OK;
-    if (static_cast<long long>(B) * C > (1ll << 31) - 1) return GS_OK;
+    if (static_cast<long long>(B) * C > (1ll << 31) - 1 || B > 65535) return GS_OK;
     for (int r = 0; r < sp.n_regions; ++r) {
         const DevRegion& R = sp.reg[r];
         if (!R.vec_ok) return GS_OK;

@@ -258,7 +258,11 @@ typedef struct gs_step_args {
  *          sum_r w_r*out_r / sum_r w_r           ([SAMPLING] calc_cond_batch:
  *                                                 accumulate by strength and mask,
  *                                                 normalise overlaps by summed
- *                                                 weight; 0 where no entry covers)
+ *                                                 weight; 0 where no entry covers;
+ *                                                 the division multiplies by the
+ *                                                 hardware reciprocal, relative
+ *                                                 error below 2^-22, exact for a
+ *                                                 summed weight of 1)
  *   pred = fma(s, pos, (1-s)*uncond)             ([SAMPLING] "CFG 的核心", [BCG]
  *                                                 sections 3-4: uncond +
  *                                                 s*(cond-uncond) in fp32, exact
