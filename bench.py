@@ -2,7 +2,7 @@
 """Benchmark of the fused guided denoise step; rank 0 prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--pdl]
+                    [--impl ours|reference] [--no-pdl] [--no-tma]
 
 A step is one call of gs_guided_step: the whole per-step path (per-sample
 parameters, regional accumulation, guidance combine, inpaint blend, Euler
@@ -52,7 +52,10 @@ FALLBACK_HBM_GBS = 6800.0
 # Per-launch DRAM traffic (read + write bytes) of the step kernel from one ncu
 # capture, with the SHA-256 prefix of the kernel source it was taken on.  A
 # different source hash means the counters are stale: traffic is reported null.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/guided_step_tma__bcg_bf16_b16.md (dram read 6,302,208 B + write 0 B)
+    "bcg_bf16_b16": (6302208, "3271c4400a414baf"),
+}
 
 
 def parse_args():
@@ -62,7 +65,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bcg_bf16_b16")
-    ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch (on by default: each "
+                         "step's CTAs are scheduled while the previous kernel drains, and wait "
+                         "for it before touching memory)")
     ap.add_argument("--no-tma", action="store_true",
                     help="force the register-streaming kernel instead of the TMA pipeline")
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -73,9 +79,13 @@ def parse_args():
 
 
 def kernel_source_hash() -> str:
-    p = os.path.join(ROOT, "bucketized_guidance_step_gb300", "csrc", "guided_step.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """SHA-256 prefix over the kernel sources and the C ABI header."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bucketized_guidance_step_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)) + ["../../include/gs.h"]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def hbm_peak():
@@ -153,7 +163,26 @@ def dist_env():
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def build_sets(wl, R, dev, seed=0):
+def plan(wl, world, dev):
+    """Schedule and scale table from the library; with N ranks, rank 0's copy is
+    broadcast once so every rank steps with identical sigmas and scales."""
+    from bucketized_guidance_step_gb300 import dist as D
+    from bucketized_guidance_step_gb300 import gs
+
+    s, g = wl.schedule, wl.guidance
+    sig_np, _ = gs.sigmas(s.kind, s.steps, sigma_min=s.sigma_min, sigma_max=s.sigma_max,
+                          rho=s.rho, denoise=s.denoise, start_step=s.start_step,
+                          last_step=s.last_step, force_full_denoise=s.force_full_denoise)
+    lut_np = None
+    if g.cfg is None:
+        _, lut_np = gs.bucket_plan(len(sig_np) - 1, g.num_buckets, curve=g.curve, v0=g.v0,
+                                   v1=g.v1, edge=g.edge)
+    if world > 1:
+        sig_np, lut_np = D.replicate_plan(sig_np, lut_np, device=dev)
+    return sig_np, lut_np
+
+
+def build_sets(wl, R, dev, sig_np, lut_np, seed=0):
     """R rotating input sets on the device, plus the shared per-run state."""
     import torch
 
@@ -161,18 +190,9 @@ def build_sets(wl, R, dev, seed=0):
     from bucketized_guidance_step_gb300.workloads import DTYPES, step_inputs
 
     dt = DTYPES[wl.dtype]
-    s = wl.schedule
-    sig_np, _ = gs.sigmas(s.kind, s.steps, sigma_min=s.sigma_min, sigma_max=s.sigma_max,
-                          rho=s.rho, denoise=s.denoise, start_step=s.start_step,
-                          last_step=s.last_step, force_full_denoise=s.force_full_denoise)
     steps = len(sig_np) - 1
     sig = torch.from_numpy(sig_np).to(dev)
-    lut = None
-    if wl.guidance.cfg is None:
-        g = wl.guidance
-        _, lut_np = gs.bucket_plan(steps, g.num_buckets, curve=g.curve, v0=g.v0, v1=g.v1,
-                                   edge=g.edge)
-        lut = torch.from_numpy(lut_np).to(dev)
+    lut = None if lut_np is None else torch.from_numpy(lut_np).to(dev)
     # geometry (rectangles, strengths, pixel masks) from the seeded generator, once
     proto = step_inputs(wl, 0, B=1)
     gen = torch.Generator(device=dev)
@@ -290,14 +310,15 @@ def run_ours(args, world, rank, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
 
-    one, sig, lut, steps = build_sets(wl, 1, dev, seed=1234 + rank)
+    sig_np, lut_np = plan(wl, world, dev)
+    one, sig, lut, steps = build_sets(wl, 1, dev, sig_np, lut_np, seed=1234 + rank)
     per_set = set_bytes(wl, one[0])
     R = max(2, math.ceil(4 * l2 / per_set))
     del one
-    sets, sig, lut, steps = build_sets(wl, R, dev, seed=1234 + rank)
+    sets, sig, lut, steps = build_sets(wl, R, dev, sig_np, lut_np, seed=1234 + rank)
     prepared = []
     for st in sets:
-        a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, args.pdl,
+        a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, (not args.no_pdl),
                                                             not args.no_tma))
         prepared.append((a, keep))
     kernel = gs.kernel_kind(prepared[0][0])
@@ -342,12 +363,11 @@ def run_ours(args, world, rank, local):
     ms = start.elapsed_time(end)
     ms_max = ms
     if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_max = float(t.item())
+        from bucketized_guidance_step_gb300 import dist as D
+        ms_max = D.max_over_ranks(ms, device=dev)
 
     # --- end to end: pinned host buffers in, result out, every step ---------
-    e2e = run_e2e(args, wl, sets[0], sig, lut, stream, dev, pg)
+    e2e = run_e2e(args, wl, sets, sig, lut, stream, dev, pg)
 
     from bucketized_guidance_step_gb300.workloads import step_inputs
     proto = step_inputs(wl, 0, B=1)
@@ -366,7 +386,7 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": describe(wl), "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W,
                    "l2": f"{R} rotating input sets of {per_set} B (>= 4x L2 of {l2} B)",
-                   "launch": "CUDA graph replay" + (", PDL" if args.pdl else ""),
+                   "launch": "CUDA graph replay" + (", PDL" if (not args.no_pdl) else ""),
                    "kernel": kernel,
                    "tuning": {k: os.environ[k] for k in ("GS_TMA_ROWS", "GS_TMA_CHANNELS", "GS_STEP_CHANNELS")
                               if k in os.environ},
@@ -388,38 +408,75 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, wl, st, sig, lut, stream, dev, pg):
-    """Pinned host inputs -> device -> step -> host result, every step, in a graph."""
+def run_e2e(args, wl, sets, sig, lut, stream, dev, pg):
+    """Pinned host inputs -> device -> step -> host result, every step.
+
+    Two device buffer sets and three streams form a pipeline: the copy-in of
+    step k+1 and the copy-out of step k-1 overlap the kernel of step k, as a
+    serving loop would run it.  Each step's inputs are copied in full from
+    pinned host memory and its x_out is read back in full; the dependency
+    chain per buffer is copy-in -> step -> copy-out -> next copy-in.  E steps
+    are captured in one CUDA graph and timed with events.
+    """
     import torch
 
     from bucketized_guidance_step_gb300 import gs
 
-    host = {}
-    for k in ("x", "stacked", "uncond", "orig", "idx"):
-        if k in st:
-            host[k] = torch.empty_like(st[k], device="cpu").pin_memory()
-            host[k].copy_(st[k])
-    regions_h = [r.out.to("cpu").pin_memory() for r in st["regions"]]
-    out_h = torch.empty_like(st["x"], device="cpu").pin_memory()
-    a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, False, not args.no_tma))
+    keys = [k for k in ("x", "stacked", "uncond", "orig", "idx") if k in sets[0]]
+    host_in = []
+    for j in range(2):
+        h = {k: torch.empty_like(sets[j][k], device="cpu").pin_memory() for k in keys}
+        for k in keys:
+            h[k].copy_(sets[j][k])
+        hr = [r.out.to("cpu").pin_memory() for r in sets[j]["regions"]]
+        host_in.append((h, hr))
+    out_h = [torch.empty_like(sets[0]["x"], device="cpu").pin_memory() for _ in range(2)]
+    prepared = [gs.make_step_args(sets[j]["x"], **step_kwargs(wl, sets[j], sig, lut, False,
+                                                              not args.no_tma))
+                for j in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0][0].values()) + \
+        sum(t.numel() * t.element_size() for t in host_in[0][1])
+    d2h = out_h[0].numel() * out_h[0].element_size()
 
-    def one_step():
-        for k, h in host.items():
-            st[k].copy_(h, non_blocking=True)
-        for r, h in zip(st["regions"], regions_h):
-            r.out.copy_(h, non_blocking=True)
-        gs.launch_step(a)
-        out_h.copy_(st["x"], non_blocking=True)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_step = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    h2d = sum(h.numel() * h.element_size() for h in host.values()) + \
-        sum(h.numel() * h.element_size() for h in regions_h)
-    d2h = out_h.numel() * out_h.element_size()
-    E = max(1, args.e2e_steps)
+    def pipeline(E):
+        # fork the side streams from the capture stream
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for k in range(E):
+            j = k % 2
+            st = sets[j]
+            h, hr = host_in[j]
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(ev_out[j])
+                for key in keys:
+                    st[key].copy_(h[key], non_blocking=True)
+                for r, hb in zip(st["regions"], hr):
+                    r.out.copy_(hb, non_blocking=True)
+                ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            gs.launch_step(prepared[j][0], stream)
+            ev_step[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_step[j])
+                out_h[j].copy_(st["x"], non_blocking=True)
+                ev_out[j].record(s_out)
+        # join
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    E = max(2, args.e2e_steps)
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            one_step()
+        pipeline(4)
         torch.cuda.synchronize(dev)
-        g = capture([one_step] * E, stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            pipeline(E)
         g.replay()
         torch.cuda.synchronize(dev)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -433,14 +490,14 @@ def run_e2e(args, wl, st, sig, lut, stream, dev, pg):
     ms = start.elapsed_time(end)
     world = 1
     if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+        from bucketized_guidance_step_gb300 import dist as D
+        ms = D.max_over_ranks(ms, device=dev)
         world = pg.get_world_size()
     value = world * wl.elements / (ms / 1e3 / E) / 1e9
     return {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": E,
-            "path": "pinned host -> cudaMemcpyAsync -> gs_guided_step -> host, CUDA graph"}
+            "path": "pinned host -> copy-in stream -> gs_guided_step -> copy-out stream -> "
+                    "pinned host, double-buffered, one CUDA graph"}
 
 
 def describe(wl) -> str:
