@@ -67,10 +67,7 @@ __device__ __forceinline__ void accumulate_regions(const StepParams& p, const De
         for (int j = 0; j < VEC; ++j) {
             const int tx = xs + j;
             in[j] = tx >= 0 && tx < R.w;
-            float f = wrow;
-            if (R.edges & kEdgeLeft) f = f * ramp(tx, R.feather, R.inv_feather);
-            if (R.edges & kEdgeRight) f = f * ramp(R.w - 1 - tx, R.feather, R.inv_feather);
-            wj[j] = f;
+            wj[j] = wrow * column_factor(R.edges, R.feather, R.inv_feather, tx, R.w);
         }
         if (R.mask != nullptr) {
             const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
@@ -308,10 +305,7 @@ __device__ __forceinline__ void accumulate_regions_vec(const StepParams& p, cons
             for (int j = 0; j < VEC; ++j) {
                 const int tx = xs + j;
                 in[j] = tx >= 0 && tx < R.w;
-                float f = wrow;
-                if (R.edges & kEdgeLeft) f = f * ramp(tx, R.feather, R.inv_feather);
-                if (R.edges & kEdgeRight) f = f * ramp(R.w - 1 - tx, R.feather, R.inv_feather);
-                wj[j] = f;
+                wj[j] = wrow * column_factor(R.edges, R.feather, R.inv_feather, tx, R.w);
             }
             if (R.mask != nullptr) {
                 const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;

@@ -198,6 +198,17 @@ __device__ __forceinline__ float ramp(int t, int feather, float inv_feather) {
     return t + 1 >= feather ? 1.0f : static_cast<float>(t + 1) * inv_feather;
 }
 
+// Product of the left and right ramps at region column tx (1 where neither
+// edge ramps).  A pixel's weight is strength * top * bottom (the row factor)
+// times this column factor, in that order, in every kernel.
+__device__ __forceinline__ float column_factor(int edges, int feather, float inv_feather, int tx,
+                                               int w) {
+    float f = 1.0f;
+    if (edges & kEdgeLeft) f = ramp(tx, feather, inv_feather);
+    if (edges & kEdgeRight) f = f * ramp(w - 1 - tx, feather, inv_feather);
+    return f;
+}
+
 __device__ __forceinline__ int floor_div(int a, int b) {
     const int q = a / b;
     return (a % b != 0 && a < 0) ? q - 1 : q;
@@ -254,44 +265,19 @@ __device__ __forceinline__ Raw<T, VEC> window(const Raw<T, VEC>& lo, const Raw<T
 // rounded to nearest, so results equal the scalar fmaf / * / + / - bit for bit.
 // ---------------------------------------------------------------------------
 struct f2 {
-    unsigned long long v;
+    float2 v;
 };
 
-__device__ __forceinline__ f2 mk2(float lo, float hi) {
-    f2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
-    return r;
-}
+__device__ __forceinline__ f2 mk2(float lo, float hi) { return f2{make_float2(lo, hi)}; }
 __device__ __forceinline__ f2 splat2(float a) { return mk2(a, a); }
-__device__ __forceinline__ float lo_of(f2 a) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
-    return lo;
-}
-__device__ __forceinline__ float hi_of(f2 a) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
-    return hi;
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-    f2 r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
-    return r;
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-    f2 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-    return r;
-}
-__device__ __forceinline__ f2 add2(f2 a, f2 b) {
-    f2 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-    return r;
-}
+__device__ __forceinline__ float lo_of(f2 a) { return a.v.x; }
+__device__ __forceinline__ float hi_of(f2 a) { return a.v.y; }
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) { return f2{__ffma2_rn(a.v, b.v, c.v)}; }
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) { return f2{__fmul2_rn(a.v, b.v)}; }
+__device__ __forceinline__ f2 add2(f2 a, f2 b) { return f2{__fadd2_rn(a.v, b.v)}; }
+// a - b is defined as a + (-b) in IEEE arithmetic, bit for bit.
 __device__ __forceinline__ f2 sub2(f2 a, f2 b) {
-    f2 r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-    return r;
+    return f2{__fadd2_rn(a.v, make_float2(-b.v.x, -b.v.y))};
 }
 
 // 1 / w (hardware approximation, relative error below 2^-22, exact at powers of

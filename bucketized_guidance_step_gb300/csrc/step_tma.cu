@@ -50,8 +50,12 @@ struct TmaRegion {
     int pad_;
     const float* mask;
     long long mask_bstride;
-    unsigned smem_off;        // byte offset of the region's box inside a stage
+    unsigned smem_off;        // byte offset of the region's box inside the tile
     unsigned tile_bytes;      // CG * RB * wbox * element size
+    int col0;                 // frame column of column-table entry 0 (x0 rounded down to VEC)
+    int ncol;                 // column-table length (multiple of VEC)
+    unsigned tab_off;         // byte offset of the column table inside the tile
+    int pad2_;
 };
 
 static_assert(sizeof(TmaRegion) % 4 == 0, "region descriptors are copied as 32-bit words");
@@ -88,6 +92,12 @@ __device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
 
 __device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Add bytes the current phase must receive before it can complete (no arrival).
+__device__ __forceinline__ void mbar_add_tx(unsigned bar, unsigned bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
 
@@ -149,42 +159,6 @@ __device__ __forceinline__ bool band_hits(const TmaRegion& R, int y_band, int RB
     return y_band < R.y0 + R.h && y_band + RB > R.y0;
 }
 
-// Weights of region R at pixels (y, x0 .. x0+VEC-1) of sample b: strength times
-// the feather ramps times the region mask, 0 outside the region.  Pixel groups
-// wholly inside the region and clear of its side ramps take a short path.
-template <int VEC>
-__device__ __forceinline__ void region_weights(const TmaRegion& R, int b, int y, int x0,
-                                               float (&wj)[VEC]) {
-    const int ty = y - R.y0;
-    float wrow = R.strength;
-    if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
-    if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
-    const int xs = x0 - R.x0;
-    const int lpad = (R.edges & kEdgeLeft) ? R.feather - 1 : 0;
-    const int rpad = (R.edges & kEdgeRight) ? R.feather - 1 : 0;
-    if (xs >= lpad && xs + VEC - 1 <= R.w - 1 - rpad && R.mask == nullptr) {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) wj[j] = wrow;
-        return;
-    }
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-        const int tx = xs + j;
-        float f = wrow;
-        if (R.edges & kEdgeLeft) f = f * ramp(tx, R.feather, R.inv_feather);
-        if (R.edges & kEdgeRight) f = f * ramp(R.w - 1 - tx, R.feather, R.inv_feather);
-        wj[j] = f;
-    }
-    if (R.mask != nullptr) {
-        const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            if (xs + j >= 0 && xs + j < R.w) wj[j] = wj[j] * __ldg(mrow + xs + j);
-    }
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) wj[j] = (xs + j >= 0 && xs + j < R.w) ? wj[j] : 0.0f;
-}
-
 template <typename T, int VEC>
 __device__ __forceinline__ Raw<T, VEC> ld_smem(const unsigned char* base, unsigned byte_off) {
     Raw<T, VEC> r;
@@ -196,13 +170,58 @@ __device__ __forceinline__ Raw<T, VEC> ld_smem(const unsigned char* base, unsign
     return r;
 }
 
+// Accumulate one region into pos over CG channels: the region's box row for this
+// thread is at byte rbase (channel stride rk); the thread's window starts SH
+// elements into aligned vector q0 (SH is the same for every thread of the tile,
+// so it is a template parameter and the switch that picks it runs once per region).
+template <typename T, int VEC, int CG, int SH>
+__device__ __forceinline__ void region_channels(const unsigned char* st, unsigned rbase,
+                                                unsigned rk, int q0, bool lo_ok, bool hi_ok,
+                                                const f2 (&w2)[VEC / 2], f2 (&pos)[CG][VEC / 2]) {
+    constexpr int kW = Raw<T, VEC>::kWords;
+#pragma unroll
+    for (int k = 0; k < CG; ++k) {
+        Raw<T, VEC> lo, hi;
+#pragma unroll
+        for (int i = 0; i < kW; ++i) lo.w[i] = hi.w[i] = 0u;
+        if (lo_ok) lo = ld_smem<T, VEC>(st, rbase + k * rk + q0 * 16);
+        if (SH != 0 && hi_ok) hi = ld_smem<T, VEC>(st, rbase + k * rk + (q0 + 1) * 16);
+        Raw<T, VEC> win;
+        unsigned cat[2 * kW];
+#pragma unroll
+        for (int i = 0; i < kW; ++i) {
+            cat[i] = lo.w[i];
+            cat[kW + i] = hi.w[i];
+        }
+        if constexpr (sizeof(typename T::scalar) == 4) {
+#pragma unroll
+            for (int i = 0; i < kW; ++i) win.w[i] = cat[i + SH];
+        } else {
+#pragma unroll
+            for (int i = 0; i < kW; ++i)
+                win.w[i] = (SH & 1) ? __funnelshift_r(cat[i + SH / 2], cat[i + SH / 2 + 1], 16)
+                                    : cat[i + SH / 2];
+        }
+#pragma unroll
+        for (int q = 0; q < VEC / 2; ++q) pos[k][q] = fma2(w2[q], widen2<T, VEC>(win, q), pos[k][q]);
+    }
+}
+
 // ---- the kernel ---------------------------------------------------------------
 // One CTA per tile; grid (band, channel group, sample), block (pixel group, row).
-// Thread 0 arms the CTA's mbarrier with the tile's byte count and issues its TMA
-// boxes.  While they are in flight every thread reads its sample's parameters
-// and, with regions, finds the regions touching its VEC pixels, their summed
-// weight and its reciprocal; then it waits and computes CG channels of its
-// pixels from shared memory.
+// Thread 0 arms the CTA's mbarrier with the tile's byte count, issues its TMA
+// boxes, then reads the sample's step parameters and waits for the boxes.
+// Meanwhile the other threads build, for every region touching the band, a
+// frame-aligned table of its column factors (feather ramps, 0 outside the
+// region), so that a thread's VEC weights are two 16-byte loads.  After a CTA
+// barrier every thread computes CG channels of its VEC pixels from shared memory.
+struct TileParams {
+    float s, one_minus_s, ratio;
+    int ok;             // 1 = step this sample, 0 = skip it
+    int inpaint;        // 1 = this sample blends with its original
+    int arrived;        // 0 = the wait for the tile gave up
+};
+
 template <typename T, int CG, bool REG, bool INP>
 __global__ void __launch_bounds__(kMaxThreads)
     guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
@@ -215,11 +234,12 @@ __global__ void __launch_bounds__(kMaxThreads)
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<unsigned long long>(smem_raw) + 127ull) & ~127ull);
     unsigned long long* full = reinterpret_cast<unsigned long long*>(smem);
-    const unsigned char* st = smem + 128;
+    unsigned char* st = smem + 128;
 
     const int band = blockIdx.x;
     const int cgi = blockIdx.y;
     const int b = blockIdx.z;
+    const int nthreads = blockDim.x * blockDim.y;
     const int tid = threadIdx.y * blockDim.x + threadIdx.x;
     const int row = threadIdx.y;
     const int x0 = threadIdx.x * VEC;
@@ -227,111 +247,124 @@ __global__ void __launch_bounds__(kMaxThreads)
     const int y = y_band + row;
     const int z = b * p.C + cgi * CG;
     const bool has_u = p.has_u != 0, has_c = p.has_c != 0;
-    const bool inpaint = INP && (p.present == nullptr || __ldg(p.present + b) != 0);
 
-    // Region descriptors: one parallel copy from kernel parameters to shared
-    // memory (a runtime-indexed loop over the parameter copy would serialise one
-    // constant-cache miss per region).
     __shared__ TmaRegion regs[REG ? GS_MAX_REGIONS : 1];
-    if constexpr (REG) {
-        const int words = p.n_regions * static_cast<int>(sizeof(TmaRegion) / 4);
-        const int* src = reinterpret_cast<const int*>(p.reg);
-        int* dst = reinterpret_cast<int*>(regs);
-        const int nthreads = blockDim.x * blockDim.y;
-        for (int i = tid; i < words; i += nthreads) dst[i] = src[i];
-    }
+    __shared__ TileParams tp;
+    const unsigned bar = smem_u32(full);
+    const unsigned s0 = smem_u32(st);
     if (tid == 0) {
-        // Start fetching the tensor-map descriptors while the CTA sets up.
+        // Every descriptor this tile may use starts on its way now.
         prefetch_map(&p.tm_x);
         if (has_u) prefetch_map(&p.tm_u);
         if (has_c) prefetch_map(&p.tm_c);
-        if (inpaint) {
+        if (INP) {
             prefetch_map(&p.tm_o);
             prefetch_map(&p.tm_m);
         }
-        mbar_init(smem_u32(full), 1);
+        if constexpr (REG) {
+            for (int r = 0; r < p.n_regions; ++r) prefetch_map(&p.tm_r[r]);
+        }
+        mbar_init(bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     grid_dependency_wait();
     grid_dependents_launch();
 
-    if (tid == 0) {
-        unsigned bytes = p.plane_bytes;
-        if (has_u) bytes += p.plane_bytes;
-        if (has_c) bytes += p.plane_bytes;
-        if (inpaint) bytes += p.plane_bytes + p.mask_bytes;
-        if constexpr (REG) {
-            for (int r = 0; r < p.n_regions; ++r)
-                if (band_hits(regs[r], y_band, p.RB)) bytes += regs[r].tile_bytes;
-        }
-        const unsigned bar = smem_u32(full);
-        const unsigned s0 = smem_u32(st);
-        mbar_expect_tx(bar, bytes);
-        tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
-        if (has_u) tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
-        if (has_c) tma_load_3d(s0 + p.off_c, &p.tm_c, 0, y_band, z, bar);
-        if (inpaint) {
-            tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, bar);
-            tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, bar);
-        }
-        if constexpr (REG) {
-            for (int r = 0; r < p.n_regions; ++r) {
-                const TmaRegion& R = regs[r];
-                if (band_hits(R, y_band, p.RB))
-                    tma_load_3d(s0 + R.smem_off, &p.tm_r[r], 0, y_band - R.y0, z, bar);
-            }
-        }
-    }
-
-    // ---- while the tile is in flight ----
-    const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
-    const bool in_range = idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
-    const int si = in_range ? idx : 0;
-    const float s = p.lut != nullptr ? __ldg(p.lut + si) : p.cfg;
-    const float sigma = __ldg(p.sig + si);
-    const float sigma_next = __ldg(p.sig + si + 1);
-    const bool sigma_ok = sigma > 0.0f && sigma <= 3.402823466e38f;
-    const bool uncond_ok = has_u || s == 1.0f;
-    const bool live = in_range && sigma_ok && uncond_ok && y < p.H;
-
-    // Regions touching this thread's pixels.
-    unsigned hits = 0;
-    if constexpr (REG) {
-        if (live) {
-            for (int r = 0; r < p.n_regions; ++r) {
-                const TmaRegion& R = regs[r];
-                if (!(y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w))
-                    hits |= 1u << r;
-            }
-        }
-    }
-    const f2 s2 = splat2(s);
-    const f2 oms2 = splat2(1.0f - s);
-    const f2 r2 = splat2(__fdiv_rn(sigma_next, sigma));
-
-    // ---- the tile ----
-    // One thread polls the mbarrier; the rest of the CTA sleeps at the CTA
-    // barrier, where waiting warps take no issue slots from co-resident CTAs.
-    __shared__ int tile_ok;
-    if (tid == 0) {
-        const bool ok = mbar_wait(smem_u32(full), 0);
-        if (!ok) flag(p.status, GS_DEV_TIMEOUT);
-        tile_ok = ok ? 1 : 0;
-    }
-    __syncthreads();
-    if (!tile_ok) return;
-    if (!(in_range && sigma_ok && uncond_ok)) {
-        if (tid == 0 && band == 0 && cgi == 0) {
+    // The sample's step parameters: two dependent loads (step index, then scale
+    // and sigmas) on a thread other than the one issuing the boxes, so that the
+    // chain overlaps the issue and the transfer.
+    if (tid == (nthreads > 32 ? 32 : 0)) {
+        const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
+        const bool in_range =
+            idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
+        const int si = in_range ? idx : 0;
+        const float sv = p.lut != nullptr ? __ldg(p.lut + si) : p.cfg;
+        const float sigma = __ldg(p.sig + si);
+        const float sigma_next = __ldg(p.sig + si + 1);
+        const bool sigma_ok = sigma > 0.0f && sigma <= 3.402823466e38f;
+        const bool uncond_ok = has_u || sv == 1.0f;
+        tp.s = sv;
+        tp.one_minus_s = 1.0f - sv;
+        tp.ratio = __fdiv_rn(sigma_next, sigma);
+        tp.ok = in_range && sigma_ok && uncond_ok ? 1 : 0;
+        if (!tp.ok && band == 0 && cgi == 0) {
             unsigned bits = 0;
             if (!in_range) bits |= GS_DEV_STEP_RANGE;
             else if (!sigma_ok) bits |= GS_DEV_SIGMA;
             if (in_range && !uncond_ok) bits |= GS_DEV_NEED_UNCOND;
             flag(p.status, bits);
         }
-        return;
     }
-    if (y >= p.H) return;
+
+    // The frame boxes go first: they need nothing but the tile coordinates.  Each
+    // box's bytes are added to the barrier before the box is issued, and the one
+    // arrival comes after the last box, so the phase cannot complete early.
+    if (tid == 0) {
+        mbar_add_tx(bar, p.plane_bytes);
+        tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
+        if (has_u) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
+        }
+        if (has_c) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_c, &p.tm_c, 0, y_band, z, bar);
+        }
+        bool present = false;
+        if (INP) {
+            present = p.present == nullptr || __ldg(p.present + b) != 0;
+            if (present) {
+                mbar_add_tx(bar, p.plane_bytes + p.mask_bytes);
+                tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, bar);
+                tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, bar);
+            }
+        }
+        tp.inpaint = present ? 1 : 0;
+        tp.arrived = 1;
+    }
+    if constexpr (REG) {
+        // Region descriptors: one parallel copy from kernel parameters (a
+        // runtime-indexed loop over the parameter copy would serialise one
+        // constant-cache miss per region), overlapping the frame boxes.
+        const int words = p.n_regions * static_cast<int>(sizeof(TmaRegion) / 4);
+        const int* src = reinterpret_cast<const int*>(p.reg);
+        int* dst = reinterpret_cast<int*>(regs);
+        for (int i = tid; i < words; i += nthreads) dst[i] = src[i];
+        __syncthreads();
+        if (tid == 0) {
+            for (int r = 0; r < p.n_regions; ++r) {
+                const TmaRegion& R = regs[r];
+                if (!band_hits(R, y_band, p.RB)) continue;
+                mbar_add_tx(bar, R.tile_bytes);
+                tma_load_3d(s0 + R.smem_off, &p.tm_r[r], 0, y_band - R.y0, z, bar);
+            }
+        } else {
+            // column-factor tables of the regions touching the band
+            for (int r = 0; r < p.n_regions; ++r) {
+                const TmaRegion& R = regs[r];
+                if (!band_hits(R, y_band, p.RB)) continue;
+                float* tab = reinterpret_cast<float*>(st + R.tab_off);
+                for (int i = tid - 1; i < R.ncol; i += nthreads - 1) {
+                    const int tx = R.col0 + i - R.x0;
+                    tab[i] = (tx >= 0 && tx < R.w)
+                                 ? column_factor(R.edges, R.feather, R.inv_feather, tx, R.w)
+                                 : 0.0f;
+                }
+            }
+        }
+    }
+    if (tid == 0) {
+        mbar_arrive(bar);
+        // ---- wait for the boxes (the rest of the CTA sleeps at the barrier) ----
+        if (!mbar_wait(bar, 0)) {
+            flag(p.status, GS_DEV_TIMEOUT);
+            tp.arrived = 0;
+        }
+    }
+    __syncthreads();
+    if (tp.ok != 1 || tp.arrived != 1 || y >= p.H) return;
+    const bool inpaint = INP && tp.inpaint != 0;
 
     const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
     const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
@@ -353,41 +386,66 @@ __global__ void __launch_bounds__(kMaxThreads)
                 for (int q = 0; q < NP; ++q) pos[k][q] = splat2(0.0f);
             }
         }
-        while (hits != 0) {
-            const int r = __ffs(hits) - 1;
-            hits &= hits - 1;
+        for (int r = 0; r < p.n_regions; ++r) {
             const TmaRegion& R = regs[r];
-            float wj[VEC];
-            region_weights<VEC>(R, b, y, x0, wj);
+            if (y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w) continue;
+            const int ty = y - R.y0;
+            float wrow = R.strength;
+            if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
+            if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
+            // weights: row factor times the tabulated column factors (0 outside)
+            const float* tab = reinterpret_cast<const float*>(st + R.tab_off) + (x0 - R.col0);
+            const f2 wr2 = splat2(wrow);
             f2 w2[NP];
 #pragma unroll
-            for (int q = 0; q < NP; ++q) {
-                w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
-                wsum2[q] = add2(wsum2[q], w2[q]);
+            for (int q = 0; q < VEC / 4; ++q) {
+                const float4 c4 = *reinterpret_cast<const float4*>(tab + 4 * q);
+                w2[2 * q] = mul2(wr2, mk2(c4.x, c4.y));
+                w2[2 * q + 1] = mul2(wr2, mk2(c4.z, c4.w));
             }
+            const int xs = x0 - R.x0;
+            if (R.mask != nullptr) {
+                const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
+                float wj[VEC];
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    wj[2 * q] = lo_of(w2[q]);
+                    wj[2 * q + 1] = hi_of(w2[q]);
+                }
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    if (xs + j >= 0 && xs + j < R.w) wj[j] = wj[j] * __ldg(mrow + xs + j);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
+            }
+#pragma unroll
+            for (int q = 0; q < NP; ++q) wsum2[q] = add2(wsum2[q], w2[q]);
             // Box row `row` of this region's tile is frame row y.  Columns outside
             // [0, w) are zeros (TMA fills the box past the slab's width, and
             // vectors outside the box are not read), so no pixel outside the
             // region can bring a non-finite value.
-            const int xs = x0 - R.x0;
             const int q0 = floor_div(xs, VEC);
             const int sh = xs - q0 * VEC;
             const int nq = R.wbox / VEC;
             const bool lo_ok = q0 >= 0 && q0 < nq;
-            const bool hi_ok = sh != 0 && q0 + 1 >= 0 && q0 + 1 < nq;
+            const bool hi_ok = q0 + 1 >= 0 && q0 + 1 < nq;
             const unsigned rbase = R.smem_off + static_cast<unsigned>(row) * R.wbox * ES;
             const unsigned rk = static_cast<unsigned>(p.RB) * R.wbox * ES;
-#pragma unroll
-            for (int k = 0; k < CG; ++k) {
-                Raw<T, VEC> lo, hi;
-#pragma unroll
-                for (int i = 0; i < Raw<T, VEC>::kWords; ++i) lo.w[i] = hi.w[i] = 0u;
-                if (lo_ok) lo = ld_smem<T, VEC>(st, rbase + k * rk + q0 * 16);
-                if (hi_ok) hi = ld_smem<T, VEC>(st, rbase + k * rk + (q0 + 1) * 16);
-                const Raw<T, VEC> win = window<T, VEC>(lo, hi, sh);
-#pragma unroll
-                for (int q = 0; q < NP; ++q)
-                    pos[k][q] = fma2(w2[q], widen2<T, VEC>(win, q), pos[k][q]);
+            switch (sh) {
+                case 0: region_channels<T, VEC, CG, 0>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                case 1: region_channels<T, VEC, CG, 1>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                case 2: region_channels<T, VEC, CG, 2>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                case 3: region_channels<T, VEC, CG, 3>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                default:
+                    if constexpr (VEC == 8) {
+                        switch (sh) {
+                            case 4: region_channels<T, VEC, CG, 4>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                            case 5: region_channels<T, VEC, CG, 5>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                            case 6: region_channels<T, VEC, CG, 6>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                            default: region_channels<T, VEC, CG, 7>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                        }
+                    }
+                    break;
             }
         }
 #pragma unroll
@@ -406,6 +464,9 @@ __global__ void __launch_bounds__(kMaxThreads)
     }
 
     // combine, inpaint blend, Euler, round and store
+    const f2 s2 = splat2(tp.s);
+    const f2 oms2 = splat2(tp.one_minus_s);
+    const f2 r2 = splat2(tp.ratio);
     f2 m2[NP], omm2[NP];
     if (INP && inpaint) {
 #pragma unroll
@@ -680,6 +741,14 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
         d.tile_bytes = static_cast<unsigned>(cg) * rb * d.wbox * es;
         d.smem_off = off;
         off += round128(d.tile_bytes);
+    }
+    // Column-factor tables (fp32), frame-aligned: entry i is frame column col0 + i.
+    for (int r = 0; r < sp.n_regions; ++r) {
+        TmaRegion& d = p.reg[r];
+        d.col0 = d.x0 - d.x0 % vec;
+        d.ncol = (d.x0 + d.w - d.col0 + vec - 1) / vec * vec;
+        d.tab_off = off;
+        off += round128(static_cast<unsigned>(d.ncol) * 4u);
     }
     p.tile_bytes = off;
     if (p.tile_bytes > kMaxTileBytes) return GS_OK;
