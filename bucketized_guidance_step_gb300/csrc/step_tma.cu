@@ -267,7 +267,32 @@ __global__ void __launch_bounds__(kMaxThreads)
         mbar_init(bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if constexpr (REG) {
+        // Region descriptors: one parallel copy from kernel parameters (a
+        // runtime-indexed loop over the parameter copy would serialise one
+        // constant-cache miss per region).
+        const int words = p.n_regions * static_cast<int>(sizeof(TmaRegion) / 4);
+        const int* src = reinterpret_cast<const int*>(p.reg);
+        int* dst = reinterpret_cast<int*>(regs);
+        for (int i = tid; i < words; i += nthreads) dst[i] = src[i];
+        __syncthreads();
+        // Column-factor tables of the regions touching the band.
+        for (int r = 0; r < p.n_regions; ++r) {
+            const TmaRegion& R = regs[r];
+            if (!band_hits(R, y_band, p.RB)) continue;
+            float* tab = reinterpret_cast<float*>(st + R.tab_off);
+            for (int i = tid; i < R.ncol; i += nthreads) {
+                const int tx = R.col0 + i - R.x0;
+                tab[i] = (tx >= 0 && tx < R.w)
+                             ? column_factor(R.edges, R.feather, R.inv_feather, tx, R.w)
+                             : 0.0f;
+            }
+        }
+    }
     __syncthreads();
+    // Everything above reads only kernel parameters; with programmatic
+    // dependent launch it overlaps the tail of the previous kernel.  Inputs
+    // (which a preceding kernel may produce) are read only after this wait.
     grid_dependency_wait();
     grid_dependents_launch();
 
@@ -324,33 +349,12 @@ __global__ void __launch_bounds__(kMaxThreads)
         tp.arrived = 1;
     }
     if constexpr (REG) {
-        // Region descriptors: one parallel copy from kernel parameters (a
-        // runtime-indexed loop over the parameter copy would serialise one
-        // constant-cache miss per region), overlapping the frame boxes.
-        const int words = p.n_regions * static_cast<int>(sizeof(TmaRegion) / 4);
-        const int* src = reinterpret_cast<const int*>(p.reg);
-        int* dst = reinterpret_cast<int*>(regs);
-        for (int i = tid; i < words; i += nthreads) dst[i] = src[i];
-        __syncthreads();
         if (tid == 0) {
             for (int r = 0; r < p.n_regions; ++r) {
                 const TmaRegion& R = regs[r];
                 if (!band_hits(R, y_band, p.RB)) continue;
                 mbar_add_tx(bar, R.tile_bytes);
                 tma_load_3d(s0 + R.smem_off, &p.tm_r[r], 0, y_band - R.y0, z, bar);
-            }
-        } else {
-            // column-factor tables of the regions touching the band
-            for (int r = 0; r < p.n_regions; ++r) {
-                const TmaRegion& R = regs[r];
-                if (!band_hits(R, y_band, p.RB)) continue;
-                float* tab = reinterpret_cast<float*>(st + R.tab_off);
-                for (int i = tid - 1; i < R.ncol; i += nthreads - 1) {
-                    const int tx = R.col0 + i - R.x0;
-                    tab[i] = (tx >= 0 && tx < R.w)
-                                 ? column_factor(R.edges, R.feather, R.inv_feather, tx, R.w)
-                                 : 0.0f;
-                }
             }
         }
     }
@@ -548,20 +552,6 @@ int gcd_int(int a, int b) {
     return a;
 }
 
-int sm_count_cached() {
-    static int cached[64] = {0};
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    std::lock_guard<std::mutex> lock(mu);
-    if (cached[dev] == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached[dev] = v;
-    }
-    return cached[dev];
-}
-
 template <typename T, int CG, bool REG, bool INP>
 gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stream, unsigned flags) {
     auto kern = guided_step_tma_kernel<T, CG, REG, INP>;
@@ -647,33 +637,35 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
         if (wbox > 256 || wbox > R.pitch) return GS_OK;
     }
 
-    // Channels per tile: up to 4, fewer when 4 would leave under eight tiles of
-    // 64 threads per SM (small steps are latency-bound: shorter threads, more of
-    // them).  GS_TMA_CHANNELS=1|2|4 overrides (a tuning knob).
-    const int sms_for_cg = sm_count_cached();
-    int cg = C % 4 == 0 ? 4 : (C % 2 == 0 ? 2 : 1);
-    {
-        const long long pix_groups = static_cast<long long>(B) * H * (W / vec);
-        while (cg > 1 && C % (cg / 2) == 0 && pix_groups * (C / cg) < 8ll * 64 * sms_for_cg)
-            cg /= 2;
-        static const int cg_override = [] {
-            const char* e = getenv("GS_TMA_CHANNELS");
-            const int v = e != nullptr ? atoi(e) : 0;
-            return (v == 1 || v == 2 || v == 4) ? v : 0;
-        }();
-        if (cg_override != 0 && C % cg_override == 0) cg = cg_override;
-    }
+    // Tile shape.  Measured on GB300 (rotating L2-cold inputs, back-to-back steps):
+    //   small steps (under ~2^18 pixel-group x channel units, a few MB) are
+    //     latency-bound: 1 channel x ~128 threads per tile, the most CTAs;
+    //   large steps without regions: 2 channels x ~64 threads per tile (short
+    //     CTA lifetimes keep the tail of the step short);
+    //   large steps with regions: 4 channels x ~128 threads per tile (the
+    //     per-tile region set-up is amortised over more work).
+    // GS_TMA_CHANNELS=1|2|4 and GS_TMA_ROWS override (tuning knobs; results do
+    // not depend on them).
     const int gpr = W / vec;
     const int rb0 = 32 / gcd_int(gpr, 32);             // smallest band with whole warps
     if (rb0 * gpr > kMaxThreads) return GS_OK;
-    // About 128 threads per tile; smaller bands when that leaves fewer than four
-    // tiles per SM, so that small steps still spread over every SM.
-    int rb = rb0 * std::max(1, 128 / (rb0 * gpr));
-    const int sms = sm_count_cached();
-    auto tiles_for = [&](int band) {
-        return static_cast<long long>(B) * (C / cg) * ((H + band - 1) / band);
-    };
-    while (rb > rb0 && rb * gpr > 64 && tiles_for(rb) < 4ll * sms) rb -= rb0;
+    const long long units = static_cast<long long>(B) * H * gpr * C;
+    const bool large = units >= (1ll << 18);
+    int cg = 1, target_threads = 128;
+    if (large && sp.n_regions > 0) {
+        cg = 4;
+    } else if (large) {
+        cg = 2;
+        target_threads = 64;
+    }
+    while (cg > 1 && C % cg != 0) cg /= 2;
+    static const int cg_override = [] {
+        const char* e = getenv("GS_TMA_CHANNELS");
+        const int v = e != nullptr ? atoi(e) : 0;
+        return (v == 1 || v == 2 || v == 4) ? v : 0;
+    }();
+    if (cg_override != 0 && C % cg_override == 0) cg = cg_override;
+    int rb = rb0 * std::max(1, target_threads / (rb0 * gpr));
     static const int rows_override = [] {
         const char* e = getenv("GS_TMA_ROWS");
         return e != nullptr ? atoi(e) : 0;
