@@ -77,6 +77,7 @@ struct TmaParams {
     int n_regions, n_sig, step, n_lut;
     float cfg;
     int has_u, has_c, mask_shared;
+    int test_wait_timeout;
     unsigned tile_bytes, plane_bytes, mask_bytes;
     unsigned off_x, off_u, off_c, off_o, off_m;
 };
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
     }
     if (tid == 0) {
+        if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
         mbar_arrive(bar);
         // ---- wait for the boxes (the rest of the CTA sleeps at the barrier) ----
         if (!mbar_wait(bar, 0)) {
@@ -698,6 +700,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     p.has_u = sp.u != nullptr;
     p.has_c = sp.c != nullptr;
     p.mask_shared = inp && sp.imask_bstride == 0;
+    p.test_wait_timeout = (flags & GS_LAUNCH_TEST_WAIT_TIMEOUT) ? 1 : 0;
     p.n_regions = sp.n_regions;
 
     // stage layout

@@ -35,6 +35,7 @@ GS_CURVE_LINEAR, GS_CURVE_STEP, GS_CURVE_TABLE = 0, 1, 2
 GS_MAX_REGIONS = 16
 GS_LAUNCH_PDL = 1
 GS_LAUNCH_NO_TMA = 2
+GS_LAUNCH_TEST_WAIT_TIMEOUT = 4
 GS_ABI_VERSION = 1
 
 EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_guided_step",
@@ -256,7 +257,7 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
                    step: int = 0, scale_lut=None, cfg: float = 1.0,
                    regions: Sequence[Region] = (), inpaint_mask=None, mask_present=None,
                    original=None, x_out=None, denoised_out=None, status=None,
-                   pdl: bool = False, tma: bool = True):
+                   pdl: bool = False, tma: bool = True, test_wait_timeout: bool = False):
     """Build a gs_step_args (and the region array it points to) from tensors."""
     torch = _torch()
     B, C, H, W = x.shape
@@ -322,7 +323,8 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
     a.mask_present = _dptr(mask_present, "mask_present", torch.uint8)
     a.original = _dptr(original, "original", dt)
     a.dev_status = _dptr(status, "status", torch.int32)
-    a.launch_flags = (GS_LAUNCH_PDL if pdl else 0) | (0 if tma else GS_LAUNCH_NO_TMA)
+    a.launch_flags = ((GS_LAUNCH_PDL if pdl else 0) | (0 if tma else GS_LAUNCH_NO_TMA) |
+                      (GS_LAUNCH_TEST_WAIT_TIMEOUT if test_wait_timeout else 0))
     return a, reg_arr
 
 

@@ -203,6 +203,12 @@ typedef struct gs_region {
                                 stream ends; it waits for it before any memory access */
 #define GS_LAUNCH_NO_TMA 2u  /* use the register-streaming kernel even where the
                                 TMA-pipelined one applies (same results)            */
+#define GS_LAUNCH_TEST_WAIT_TIMEOUT 4u
+                             /* tests of the error path only: every tile of the TMA
+                                kernel also waits for 16 bytes that never arrive, so
+                                its bounded wait (200 ms) expires; the kernel then
+                                sets GS_DEV_TIMEOUT and writes no output.  All real
+                                transfers still complete before any CTA exits.      */
 
 typedef struct gs_step_args {
     int32_t B, C, H, W;         /* latent batch, channels, rows, columns (all >= 1)      */

@@ -209,3 +209,27 @@ def test_host_rejects_before_launch_on_gpu():
     regs = [gs.Region(0, 0, 2, 2, 1.0, 0, x[:, :, :2, :2].contiguous())] * 17
     with pytest.raises(gs.GSError):
         gs.guided_step(x, sigmas=sig(1.0, 0.0), uncond=x, regions=regs)
+
+
+def test_bounded_wait_expires_with_status(kernel_choice):
+    """The TMA kernel's tile wait is bounded: made to run out, it reports and returns."""
+    if not kernel_choice:
+        pytest.skip("the register kernel has no waits")
+    shape = (1, 4, 8, 16)                       # one tile
+    x, u, c = (rnd(shape, s, torch.bfloat16) for s in (40, 41, 42))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sentinel = torch.full_like(x, 9.0)
+    out = sentinel.clone()
+    a, keep = gs.make_step_args(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=out,
+                                status=st, test_wait_timeout=True)
+    assert gs.kernel_kind(a) == "tma"
+    gs.launch_step(a)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gs.GS_DEV_TIMEOUT
+    assert gs.status_from_word(int(st.item())) == gs.GS_ERR_TIMEOUT
+    assert torch.equal(out, sentinel)           # no output from a tile that never arrived
+    # the context stays usable: the same call without the hook steps normally
+    st.zero_()
+    gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and not torch.equal(out, sentinel)
