@@ -210,12 +210,16 @@ __device__ __forceinline__ void region_channels(const unsigned char* st, unsigne
 
 // ---- the kernel ---------------------------------------------------------------
 // One CTA per tile; grid (band, channel group, sample), block (pixel group, row).
-// Thread 0 arms the CTA's mbarrier with the tile's byte count, issues its TMA
-// boxes, then reads the sample's step parameters and waits for the boxes.
-// Meanwhile the other threads build, for every region touching the band, a
-// frame-aligned table of its column factors (feather ramps, 0 outside the
-// region), so that a thread's VEC weights are two 16-byte loads.  After a CTA
-// barrier every thread computes CG channels of its VEC pixels from shared memory.
+// Before the grid-dependency wait (parameters only) the CTA builds, for every
+// region touching the band, a frame-aligned table of its column factors (feather
+// ramps, 0 outside the region), so that a thread's VEC weights are two 16-byte
+// loads.  After it, two threads feed the CTA's mbarrier, each arriving once:
+// thread 0 issues the boxes that need only the tile coordinates (x, uncond,
+// cond, regions); the parameter thread loads the sample's step index and
+// inpaint flag together, issues the original and mask boxes if the sample
+// carries a mask, and then finishes the step parameters.  No box waits on a
+// global load that another box does not need.  After a CTA barrier every
+// thread computes CG channels of its VEC pixels from shared memory.
 struct TileParams {
     float s, one_minus_s, ratio;
     int ok;             // 1 = step this sample, 0 = skip it
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(kMaxThreads)
         if constexpr (REG) {
             for (int r = 0; r < p.n_regions; ++r) prefetch_map(&p.tm_r[r]);
         }
-        mbar_init(bar, 1);
+        mbar_init(bar, nthreads > 32 ? 2u : 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if constexpr (REG) {
@@ -297,11 +301,49 @@ __global__ void __launch_bounds__(kMaxThreads)
     grid_dependency_wait();
     grid_dependents_launch();
 
-    // The sample's step parameters: two dependent loads (step index, then scale
-    // and sigmas) on a thread other than the one issuing the boxes, so that the
-    // chain overlaps the issue and the transfer.
-    if (tid == (nthreads > 32 ? 32 : 0)) {
+    // Thread 0: the boxes that need nothing but the tile coordinates.  Each box's
+    // bytes are added to the barrier before the box is issued, and each feeding
+    // thread arrives after its last box, so the phase cannot complete early.
+    if (tid == 0) {
+        mbar_add_tx(bar, p.plane_bytes);
+        tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
+        if (has_u) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
+        }
+        if (has_c) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_c, &p.tm_c, 0, y_band, z, bar);
+        }
+        if constexpr (REG) {
+            for (int r = 0; r < p.n_regions; ++r) {
+                const TmaRegion& R = regs[r];
+                if (!band_hits(R, y_band, p.RB)) continue;
+                mbar_add_tx(bar, R.tile_bytes);
+                tma_load_3d(s0 + R.smem_off, &p.tm_r[r], 0, y_band - R.y0, z, bar);
+            }
+        }
+    }
+
+    // The parameter thread: the step index and the inpaint flag are independent
+    // loads issued together; the original and mask boxes go out as soon as the
+    // flag is known, then the scale and sigmas (which depend on the index) are read.
+    // With a single warp, thread 0 plays both parts (frame boxes first) and
+    // arrives once.
+    const int ptid = nthreads > 32 ? 32 : 0;
+    if (tid == ptid) {
         const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
+        bool present = false;
+        if (INP) {
+            present = p.present == nullptr || __ldg(p.present + b) != 0;
+            if (present) {
+                mbar_add_tx(bar, p.plane_bytes + p.mask_bytes);
+                tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, bar);
+                tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, bar);
+            }
+        }
+        tp.inpaint = present ? 1 : 0;
+        if (ptid != 0) mbar_arrive(bar);
         const bool in_range =
             idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
         const int si = in_range ? idx : 0;
@@ -323,43 +365,8 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
     }
 
-    // The frame boxes go first: they need nothing but the tile coordinates.  Each
-    // box's bytes are added to the barrier before the box is issued, and the one
-    // arrival comes after the last box, so the phase cannot complete early.
     if (tid == 0) {
-        mbar_add_tx(bar, p.plane_bytes);
-        tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
-        if (has_u) {
-            mbar_add_tx(bar, p.plane_bytes);
-            tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
-        }
-        if (has_c) {
-            mbar_add_tx(bar, p.plane_bytes);
-            tma_load_3d(s0 + p.off_c, &p.tm_c, 0, y_band, z, bar);
-        }
-        bool present = false;
-        if (INP) {
-            present = p.present == nullptr || __ldg(p.present + b) != 0;
-            if (present) {
-                mbar_add_tx(bar, p.plane_bytes + p.mask_bytes);
-                tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, bar);
-                tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, bar);
-            }
-        }
-        tp.inpaint = present ? 1 : 0;
         tp.arrived = 1;
-    }
-    if constexpr (REG) {
-        if (tid == 0) {
-            for (int r = 0; r < p.n_regions; ++r) {
-                const TmaRegion& R = regs[r];
-                if (!band_hits(R, y_band, p.RB)) continue;
-                mbar_add_tx(bar, R.tile_bytes);
-                tma_load_3d(s0 + R.smem_off, &p.tm_r[r], 0, y_band - R.y0, z, bar);
-            }
-        }
-    }
-    if (tid == 0) {
         if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
         mbar_arrive(bar);
         // ---- wait for the boxes (the rest of the CTA sleeps at the barrier) ----

@@ -193,3 +193,15 @@ def test_every_scale_one_without_uncond(tma):
     wl = Workload("cfg1", 4, 4, 32, 32, "bf16", base.schedule, base.guidance.__class__(cfg=1.0),
                   seed=14)
     run_case(wl, uncond_none=True, tma=tma)
+
+
+@pytest.mark.parametrize("regions", [0, 3], ids=["dense", "regions"])
+def test_large_ragged_height(regions):
+    """A step large enough for the TMA kernel's wide tile shape, with a height that
+    leaves a ragged last band (rows past H read as zero and are never stored)."""
+    base = WORKLOADS[4]
+    wl = Workload("tall", 64, 16, 37, 128, "bf16", base.schedule, base.guidance,
+                  full_frame_cond=regions == 0, n_regions=regions, inpaint=True,
+                  inpaint_samples=40, region_side=(8, 37), seed=15)
+    rep, *_ = run_case(wl, expect_kernel="tma")
+    assert rep.n == wl.elements
