@@ -58,7 +58,7 @@ struct TmaRegion {
     int pad2_;
 };
 
-static_assert(sizeof(TmaRegion) % 4 == 0, "region descriptors are copied as 32-bit words");
+static_assert(sizeof(TmaRegion) % 8 == 0, "region descriptors keep 8-byte alignment in arrays");
 
 struct TmaParams {
     CUtensorMap tm_x, tm_u, tm_c, tm_o, tm_m;
@@ -273,20 +273,19 @@ __global__ void __launch_bounds__(kMaxThreads)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if constexpr (REG) {
-        // Region descriptors: one parallel copy from kernel parameters (a
-        // runtime-indexed loop over the parameter copy would serialise one
-        // constant-cache miss per region).
-        const int words = p.n_regions * static_cast<int>(sizeof(TmaRegion) / 4);
-        const int* src = reinterpret_cast<const int*>(p.reg);
-        int* dst = reinterpret_cast<int*>(regs);
-        for (int i = tid; i < words; i += nthreads) dst[i] = src[i];
-        __syncthreads();
-        // Column-factor tables of the regions touching the band.
-        for (int r = 0; r < p.n_regions; ++r) {
-            const TmaRegion& R = regs[r];
+        // One warp per region: every lane reads the region's descriptor from the
+        // kernel parameters with the same addresses (a broadcast, where lanes
+        // reading different words would serialise one parameter load per lane),
+        // lane 0 keeps a copy in shared memory for the compute loop, and the warp
+        // fills the region's frame-aligned column-factor table if the region
+        // touches the band.  Regions proceed in parallel across the warps.
+        const int warp = tid >> 5, lane = tid & 31, nwarps = (nthreads + 31) >> 5;
+        for (int r = warp; r < p.n_regions; r += nwarps) {
+            const TmaRegion R = p.reg[r];
+            if (lane == 0) regs[r] = R;
             if (!band_hits(R, y_band, p.RB)) continue;
             float* tab = reinterpret_cast<float*>(st + R.tab_off);
-            for (int i = tid; i < R.ncol; i += nthreads) {
+            for (int i = lane; i < R.ncol; i += 32) {
                 const int tx = R.col0 + i - R.x0;
                 tab[i] = (tx >= 0 && tx < R.w)
                              ? column_factor(R.edges, R.feather, R.inv_feather, tx, R.w)
