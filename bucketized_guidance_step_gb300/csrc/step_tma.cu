@@ -210,16 +210,17 @@ __device__ __forceinline__ void region_channels(const unsigned char* st, unsigne
 
 // ---- the kernel ---------------------------------------------------------------
 // One CTA per tile; grid (band, channel group, sample), block (pixel group, row).
-// Before the grid-dependency wait (parameters only) the CTA builds, for every
-// region touching the band, a frame-aligned table of its column factors (feather
-// ramps, 0 outside the region), so that a thread's VEC weights are two 16-byte
-// loads.  After it, two threads feed the CTA's mbarrier, each arriving once:
-// thread 0 issues the boxes that need only the tile coordinates (x, uncond,
-// cond, regions); the parameter thread loads the sample's step index and
-// inpaint flag together, issues the original and mask boxes if the sample
+// Before the grid-dependency wait the CTA only prefetches its tensor maps and
+// initialises its mbarrier.  After it, two threads feed the barrier, each
+// arriving once: thread 0 issues the boxes that need only the tile coordinates
+// (x, uncond, cond, regions); the parameter thread loads the sample's step index
+// and inpaint flag together, issues the original and mask boxes if the sample
 // carries a mask, and then finishes the step parameters.  No box waits on a
-// global load that another box does not need.  After a CTA barrier every
-// thread computes CG channels of its VEC pixels from shared memory.
+// global load that another box does not need.  While the boxes are in flight the
+// remaining warps build, for every region touching the band, a frame-aligned
+// table of its column factors (feather ramps, 0 outside the region), so that a
+// thread's VEC weights are two 16-byte loads.  After a CTA barrier every thread
+// computes CG channels of its VEC pixels from shared memory.
 struct TileParams {
     float s, one_minus_s, ratio;
     int ok;             // 1 = step this sample, 0 = skip it
@@ -272,29 +273,8 @@ __global__ void __launch_bounds__(kMaxThreads)
         mbar_init(bar, nthreads > 32 ? 2u : 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if constexpr (REG) {
-        // One warp per region: every lane reads the region's descriptor from the
-        // kernel parameters with the same addresses (a broadcast, where lanes
-        // reading different words would serialise one parameter load per lane),
-        // lane 0 keeps a copy in shared memory for the compute loop, and the warp
-        // fills the region's frame-aligned column-factor table if the region
-        // touches the band.  Regions proceed in parallel across the warps.
-        const int warp = tid >> 5, lane = tid & 31, nwarps = (nthreads + 31) >> 5;
-        for (int r = warp; r < p.n_regions; r += nwarps) {
-            const TmaRegion R = p.reg[r];
-            if (lane == 0) regs[r] = R;
-            if (!band_hits(R, y_band, p.RB)) continue;
-            float* tab = reinterpret_cast<float*>(st + R.tab_off);
-            for (int i = lane; i < R.ncol; i += 32) {
-                const int tx = R.col0 + i - R.x0;
-                tab[i] = (tx >= 0 && tx < R.w)
-                             ? column_factor(R.edges, R.feather, R.inv_feather, tx, R.w)
-                             : 0.0f;
-            }
-        }
-    }
     __syncthreads();
-    // Everything above reads only kernel parameters; with programmatic
+    // Everything above touches only kernel parameters; with programmatic
     // dependent launch it overlaps the tail of the previous kernel.  Inputs
     // (which a preceding kernel may produce) are read only after this wait.
     grid_dependency_wait();
@@ -315,11 +295,12 @@ __global__ void __launch_bounds__(kMaxThreads)
             tma_load_3d(s0 + p.off_c, &p.tm_c, 0, y_band, z, bar);
         }
         if constexpr (REG) {
+            // only the four fields the issue needs, read straight from the parameters
             for (int r = 0; r < p.n_regions; ++r) {
-                const TmaRegion& R = regs[r];
-                if (!band_hits(R, y_band, p.RB)) continue;
-                mbar_add_tx(bar, R.tile_bytes);
-                tma_load_3d(s0 + R.smem_off, &p.tm_r[r], 0, y_band - R.y0, z, bar);
+                const int ry0 = p.reg[r].y0, rh = p.reg[r].h;
+                if (y_band >= ry0 + rh || y_band + p.RB <= ry0) continue;
+                mbar_add_tx(bar, p.reg[r].tile_bytes);
+                tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], 0, y_band - ry0, z, bar);
             }
         }
     }
@@ -361,6 +342,30 @@ __global__ void __launch_bounds__(kMaxThreads)
             else if (!sigma_ok) bits |= GS_DEV_SIGMA;
             if (in_range && !uncond_ok) bits |= GS_DEV_NEED_UNCOND;
             flag(p.status, bits);
+        }
+    }
+
+    if constexpr (REG) {
+        // While the boxes are in flight: one warp per region reads the region's
+        // descriptor from the kernel parameters with the same addresses in every
+        // lane (a broadcast, where lanes reading different words would serialise
+        // one parameter load per lane), lane 0 keeps a copy in shared memory for
+        // the compute loop, and the warp fills the region's frame-aligned
+        // column-factor table if the region touches the band.  Warps 0 and 1 feed
+        // the barrier, so with three or more warps the others take this work.
+        const int warp = tid >> 5, lane = tid & 31, nwarps = (nthreads + 31) >> 5;
+        const int w0 = nwarps >= 3 ? 2 : 0;
+        for (int r = warp - w0; r >= 0 && r < p.n_regions; r += nwarps - w0) {
+            const TmaRegion R = p.reg[r];
+            if (lane == 0) regs[r] = R;
+            if (!band_hits(R, y_band, p.RB)) continue;
+            float* tab = reinterpret_cast<float*>(st + R.tab_off);
+            for (int i = lane; i < R.ncol; i += 32) {
+                const int tx = R.col0 + i - R.x0;
+                tab[i] = (tx >= 0 && tx < R.w)
+                             ? column_factor(R.edges, R.feather, R.inv_feather, tx, R.w)
+                             : 0.0f;
+            }
         }
     }
 
