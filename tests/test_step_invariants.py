@@ -19,7 +19,9 @@ from bucketized_guidance_step_gb300 import gs
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 DTYPES = [torch.float32, torch.bfloat16, torch.float16]
-SHAPES = [(3, 4, 16, 32), (2, 3, 5, 7)]          # vector/TMA path, scalar path
+# small (vector / TMA path, one channel per tile), scalar path, large (TMA tiles of
+# 2 or 4 channels)
+SHAPES = [(3, 4, 16, 32), (2, 3, 5, 7), (32, 8, 64, 128)]
 
 
 @pytest.fixture(params=[True, False], ids=["tma", "registers"], autouse=True)
@@ -117,9 +119,9 @@ def test_sigma_next_zero_lands_on_denoised(dtype, shape):
     assert same_bits(out, den)
 
 
+@pytest.mark.parametrize("shape", [(4, 4, 16, 16), (4, 32, 128, 128)], ids=["small", "large"])
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_deterministic_and_in_place(dtype):
-    shape = (4, 4, 16, 16)
+def test_deterministic_and_in_place(dtype, shape):
     x, u, c = (rnd(shape, s, dtype) for s in (17, 18, 19))
     a, b = torch.empty_like(x), torch.empty_like(x)
     lut = torch.tensor([2.0, 1.5, 1.2], device=DEV)
@@ -133,8 +135,8 @@ def test_deterministic_and_in_place(dtype):
     assert same_bits(a, b) and same_bits(a, xi)
 
 
-def test_device_status_word_and_skipped_samples():
-    shape = (4, 2, 8, 8)
+@pytest.mark.parametrize("shape", [(4, 2, 8, 8), (4, 32, 128, 128)], ids=["small", "large"])
+def test_device_status_word_and_skipped_samples(shape):
     x, u, c = (rnd(shape, s, torch.bfloat16) for s in (20, 21, 22))
     sentinel = torch.full_like(x, 123.0)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -168,18 +170,19 @@ def test_device_status_word_and_skipped_samples():
     assert int(st.item()) == gs.GS_DEV_SIGMA
 
 
+@pytest.mark.parametrize("shape", [(3, 4, 16, 24), (48, 8, 64, 96)], ids=["small", "large"])
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_guard_bands_untouched(dtype):
-    shape = (3, 4, 16, 24)
-    n = 3 * 4 * 16 * 24
+def test_guard_bands_untouched(dtype, shape):
+    B, C, H, W = shape
+    n = B * C * H * W
     pad = 4096
     x, u, c, o = (rnd(shape, s, dtype) for s in (23, 24, 25, 26))
     buf = torch.full((n + 2 * pad,), 7.0, dtype=dtype, device=DEV)
     out = buf[pad:pad + n].view(shape)
     den_buf = torch.full((n + 2 * pad,), -5.0, dtype=dtype, device=DEV)
     den = den_buf[pad:pad + n].view(shape)
-    m = (torch.rand((3, 1, 16, 24), generator=torch.Generator().manual_seed(3)) > 0.5).float()
-    reg = gs.Region(3, 5, 9, 13, 0.8, 4, rnd((3, 4, 9, 16), 27, dtype))
+    m = (torch.rand((B, 1, H, W), generator=torch.Generator().manual_seed(3)) > 0.5).float()
+    reg = gs.Region(3, 5, 9, 13, 0.8, 4, rnd((B, C, 9, 16), 27, dtype))
     gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, regions=[reg], cfg=5.0, x_out=out,
                    denoised_out=den, inpaint_mask=m.to(DEV), original=o)
     torch.cuda.synchronize()
@@ -188,15 +191,16 @@ def test_guard_bands_untouched(dtype):
     assert torch.isfinite(out.float()).all()
 
 
-def test_shared_mask_equals_replicated_mask():
-    shape = (4, 4, 16, 16)
+@pytest.mark.parametrize("shape", [(4, 4, 16, 16), (32, 8, 64, 128)], ids=["small", "large"])
+def test_shared_mask_equals_replicated_mask(shape):
+    B, C, H, W = shape
     x, u, c, o = (rnd(shape, s, torch.bfloat16) for s in (28, 29, 30, 31))
-    m = torch.rand((1, 1, 16, 16), generator=torch.Generator().manual_seed(5)).to(DEV)
+    m = torch.rand((1, 1, H, W), generator=torch.Generator().manual_seed(5)).to(DEV)
     a, b = torch.empty_like(x), torch.empty_like(x)
     gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=a, inpaint_mask=m,
                    original=o)
     gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=b,
-                   inpaint_mask=m.expand(4, 1, 16, 16).contiguous(), original=o)
+                   inpaint_mask=m.expand(B, 1, H, W).contiguous(), original=o)
     torch.cuda.synchronize()
     assert same_bits(a, b)
 

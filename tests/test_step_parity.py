@@ -205,3 +205,18 @@ def test_large_ragged_height(regions):
                   inpaint_samples=40, region_side=(8, 37), seed=15)
     rep, *_ = run_case(wl, expect_kernel="tma")
     assert rep.n == wl.elements
+
+
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
+@pytest.mark.parametrize("dtype", ["fp32", "fp16"])
+@pytest.mark.parametrize("regions", [0, 5])
+def test_large_fp32_fp16(dtype, regions, tma):
+    """Large steps in fp32 and fp16 (the TMA kernel's 2- and 4-channel tiles), with
+    region masks, a denoised output and rows of 24 or 12 pixel groups."""
+    base = WORKLOADS[4]
+    wl = Workload("large", 64, 8, 200, 96, dtype, base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=regions, region_side=(5, 90), inpaint=True,
+                  inpaint_samples=20, seed=16)
+    rep, *_ = run_case(wl, region_masks=regions > 0, want_den=True, tma=tma,
+                       expect_kernel="tma" if tma else "vector")
+    assert rep.n == wl.elements
