@@ -80,6 +80,7 @@ struct TmaParams {
     int test_wait_timeout;
     unsigned tile_bytes, plane_bytes, mask_bytes;
     unsigned off_x, off_u, off_c, off_o, off_m;
+    unsigned rowtab_off;
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -228,6 +229,21 @@ struct TileParams {
     int arrived;        // 0 = the wait for the tile gave up
 };
 
+// One region as this tile's threads use it, built once per CTA by the region's
+// warp, so that a thread reads three 16-byte words per region instead of the
+// descriptor's fields one by one.  Tile rows [row_lo, row_hi) and frame columns
+// [x_lo, x_hi) are the region's; a thread whose VEC pixels start at frame column
+// x0 finds its first box vector at q0 = (x0 + qoff) / VEC (an exact division)
+// and its window sh elements into it; box row i starts at byte rbase0 + i*rrow of
+// the tile, channel k at k*rk further; column-factor entry of frame column x is
+// at byte tabx + 4x of the tile.
+struct __align__(16) TileRegion {
+    int row_lo, row_hi, x_lo, x_hi;
+    int qoff, sh, nq, has_mask;
+    unsigned rbase0, rrow, rk;
+    int tabx;
+};
+
 template <typename T, int CG, bool REG, bool INP>
 __global__ void __launch_bounds__(kMaxThreads)
     guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
@@ -255,6 +271,7 @@ __global__ void __launch_bounds__(kMaxThreads)
     const bool has_u = p.has_u != 0, has_c = p.has_c != 0;
 
     __shared__ TmaRegion regs[REG ? GS_MAX_REGIONS : 1];
+    __shared__ TileRegion tregs[REG ? GS_MAX_REGIONS : 1];
     __shared__ TileParams tp;
     const unsigned bar = smem_u32(full);
     const unsigned s0 = smem_u32(st);
@@ -357,8 +374,34 @@ __global__ void __launch_bounds__(kMaxThreads)
         const int w0 = nwarps >= 3 ? 2 : 0;
         for (int r = warp - w0; r >= 0 && r < p.n_regions; r += nwarps - w0) {
             const TmaRegion R = p.reg[r];
-            if (lane == 0) regs[r] = R;
-            if (!band_hits(R, y_band, p.RB)) continue;
+            const bool hits = band_hits(R, y_band, p.RB);
+            if (lane == 0) {
+                regs[r] = R;
+                TileRegion t;
+                t.row_lo = hits ? (R.y0 > y_band ? R.y0 - y_band : 0) : 0;
+                t.row_hi = hits ? (R.y0 + R.h - y_band < p.RB ? R.y0 + R.h - y_band : p.RB) : 0;
+                t.x_lo = R.x0;
+                t.x_hi = R.x0 + R.w;
+                t.sh = (VEC - R.x0 % VEC) % VEC;
+                t.qoff = -R.x0 - t.sh;
+                t.nq = R.wbox / VEC;
+                t.has_mask = R.mask != nullptr ? 1 : 0;
+                t.rbase0 = R.smem_off;
+                t.rrow = static_cast<unsigned>(R.wbox) * sizeof(S);
+                t.rk = static_cast<unsigned>(p.RB) * R.wbox * sizeof(S);
+                t.tabx = static_cast<int>(R.tab_off) - 4 * R.col0;
+                tregs[r] = t;
+            }
+            if (!hits) continue;
+            // row factors of the band's rows: strength * top ramp * bottom ramp
+            float* rowtab = reinterpret_cast<float*>(st + p.rowtab_off) + r * p.RB;
+            for (int i = lane; i < p.RB; i += 32) {
+                const int ty = y_band + i - R.y0;
+                float wrow = R.strength;
+                if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
+                if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
+                rowtab[i] = wrow;
+            }
             float* tab = reinterpret_cast<float*>(st + R.tab_off);
             for (int i = lane; i < R.ncol; i += 32) {
                 const int tx = R.col0 + i - R.x0;
@@ -403,16 +446,13 @@ __global__ void __launch_bounds__(kMaxThreads)
                 for (int q = 0; q < NP; ++q) pos[k][q] = splat2(0.0f);
             }
         }
+        const float* rowtabs = reinterpret_cast<const float*>(st + p.rowtab_off);
         for (int r = 0; r < p.n_regions; ++r) {
-            const TmaRegion& R = regs[r];
-            if (y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w) continue;
-            const int ty = y - R.y0;
-            float wrow = R.strength;
-            if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
-            if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
+            const TileRegion tr = tregs[r];
+            if (row < tr.row_lo || row >= tr.row_hi || x0 + VEC <= tr.x_lo || x0 >= tr.x_hi) continue;
             // weights: row factor times the tabulated column factors (0 outside)
-            const float* tab = reinterpret_cast<const float*>(st + R.tab_off) + (x0 - R.col0);
-            const f2 wr2 = splat2(wrow);
+            const float* tab = reinterpret_cast<const float*>(st + tr.tabx + 4 * x0);
+            const f2 wr2 = splat2(rowtabs[r * p.RB + row]);
             f2 w2[NP];
 #pragma unroll
             for (int q = 0; q < VEC / 4; ++q) {
@@ -420,8 +460,10 @@ __global__ void __launch_bounds__(kMaxThreads)
                 w2[2 * q] = mul2(wr2, mk2(c4.x, c4.y));
                 w2[2 * q + 1] = mul2(wr2, mk2(c4.z, c4.w));
             }
-            const int xs = x0 - R.x0;
-            if (R.mask != nullptr) {
+            if (tr.has_mask) {
+                const TmaRegion& R = regs[r];
+                const int ty = y - R.y0;
+                const int xs = x0 - R.x0;
                 const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
                 float wj[VEC];
 #pragma unroll
@@ -441,13 +483,12 @@ __global__ void __launch_bounds__(kMaxThreads)
             // [0, w) are zeros (TMA fills the box past the slab's width, and
             // vectors outside the box are not read), so no pixel outside the
             // region can bring a non-finite value.
-            const int q0 = floor_div(xs, VEC);
-            const int sh = xs - q0 * VEC;
-            const int nq = R.wbox / VEC;
-            const bool lo_ok = q0 >= 0 && q0 < nq;
-            const bool hi_ok = q0 + 1 >= 0 && q0 + 1 < nq;
-            const unsigned rbase = R.smem_off + static_cast<unsigned>(row) * R.wbox * ES;
-            const unsigned rk = static_cast<unsigned>(p.RB) * R.wbox * ES;
+            const int q0 = (x0 + tr.qoff) / VEC;      // exact: x0 + qoff is a multiple of VEC
+            const int sh = tr.sh;
+            const bool lo_ok = q0 >= 0 && q0 < tr.nq;
+            const bool hi_ok = q0 + 1 >= 0 && q0 + 1 < tr.nq;
+            const unsigned rbase = tr.rbase0 + static_cast<unsigned>(row) * tr.rrow;
+            const unsigned rk = tr.rk;
             switch (sh) {
                 case 0: region_channels<T, VEC, CG, 0>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
                 case 1: region_channels<T, VEC, CG, 1>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
@@ -756,6 +797,9 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
         d.tab_off = off;
         off += round128(static_cast<unsigned>(d.ncol) * 4u);
     }
+    // Row-factor tables (fp32): region r's band rows at rowtab_off + 4 * (r * rb + i).
+    p.rowtab_off = off;
+    off += round128(static_cast<unsigned>(sp.n_regions) * rb * 4u);
     p.tile_bytes = off;
     if (p.tile_bytes > kMaxTileBytes) return GS_OK;
     const unsigned smem = 128u + 128u + p.tile_bytes;   // alignment slack + mbarrier line
