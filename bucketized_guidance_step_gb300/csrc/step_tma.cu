@@ -38,6 +38,7 @@ namespace {
 
 constexpr int kMaxThreads = 256;
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
+constexpr unsigned long long kDrainLimitNs = 10ull * 1000ull * 1000ull;
 constexpr unsigned kMaxTileBytes = 200u * 1024u;
 
 struct TmaRegion {
@@ -130,13 +131,18 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Wait for the phase with the given parity to complete; false after the time limit.
-__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity) {
+// Wait for the phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_for(unsigned bar, unsigned parity,
+                                              unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
+}
+
+__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity) {
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 __device__ __forceinline__ void tma_load_3d(unsigned dst, const CUtensorMap* map, int x, int y,
@@ -221,7 +227,9 @@ __device__ __forceinline__ void region_channels(const unsigned char* st, unsigne
 // remaining warps build, for every region touching the band, a frame-aligned
 // table of its column factors (feather ramps, 0 outside the region), so that a
 // thread's VEC weights are two 16-byte loads.  After a CTA barrier every thread
-// computes CG channels of its VEC pixels from shared memory.
+// computes CG channels of its VEC pixels from shared memory.  With regions in
+// multi-channel tiles the boxes come in two groups on two barriers (see kSplit), so
+// that the regional accumulation overlaps the arrival of x, original and mask.
 struct TileParams {
     float s, one_minus_s, ratio;
     int ok;             // 1 = step this sample, 0 = skip it
@@ -251,6 +259,14 @@ __global__ void __launch_bounds__(kMaxThreads)
     constexpr int VEC = 16 / static_cast<int>(sizeof(S));
     constexpr int NP = VEC / 2;
     constexpr unsigned ES = sizeof(S);
+    // With regions, in tiles of several channels (the shapes of large steps), the
+    // tile's boxes come in two groups, each on its own mbarrier: A = uncond, cond
+    // and the region slabs (all the positive branch and the combine need), B = x,
+    // original and mask (the blend and the Euler update).  The CTA accumulates the
+    // regions while B is still landing.  One-channel tiles (small steps, where the
+    // whole step is one wave of CTAs and latency-bound) keep a single barrier: there
+    // the second wait costs more than the overlap gains.
+    constexpr bool kSplit = REG && CG > 1;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -273,7 +289,8 @@ __global__ void __launch_bounds__(kMaxThreads)
     __shared__ TmaRegion regs[REG ? GS_MAX_REGIONS : 1];
     __shared__ TileRegion tregs[REG ? GS_MAX_REGIONS : 1];
     __shared__ TileParams tp;
-    const unsigned bar = smem_u32(full);
+    const unsigned bar = smem_u32(full);                // A (the only barrier without regions)
+    const unsigned barB = kSplit ? bar + 8u : bar;      // B
     const unsigned s0 = smem_u32(st);
     if (tid == 0) {
         // Every descriptor this tile may use starts on its way now.
@@ -287,7 +304,12 @@ __global__ void __launch_bounds__(kMaxThreads)
         if constexpr (REG) {
             for (int r = 0; r < p.n_regions; ++r) prefetch_map(&p.tm_r[r]);
         }
-        mbar_init(bar, nthreads > 32 ? 2u : 1u);
+        if constexpr (kSplit) {
+            mbar_init(bar, 1u);
+            mbar_init(barB, nthreads > 32 ? 2u : 1u);
+        } else {
+            mbar_init(bar, nthreads > 32 ? 2u : 1u);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -301,8 +323,10 @@ __global__ void __launch_bounds__(kMaxThreads)
     // bytes are added to the barrier before the box is issued, and each feeding
     // thread arrives after its last box, so the phase cannot complete early.
     if (tid == 0) {
-        mbar_add_tx(bar, p.plane_bytes);
-        tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
+        if constexpr (!kSplit) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
+        }
         if (has_u) {
             mbar_add_tx(bar, p.plane_bytes);
             tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
@@ -320,6 +344,13 @@ __global__ void __launch_bounds__(kMaxThreads)
                 tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], 0, y_band - ry0, z, bar);
             }
         }
+        if constexpr (kSplit) {
+            // group A is complete: thread 0 is its only feeder
+            if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+            mbar_arrive(bar);
+            mbar_add_tx(barB, p.plane_bytes);
+            tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, barB);
+        }
     }
 
     // The parameter thread: the step index and the inpaint flag are independent
@@ -334,13 +365,13 @@ __global__ void __launch_bounds__(kMaxThreads)
         if (INP) {
             present = p.present == nullptr || __ldg(p.present + b) != 0;
             if (present) {
-                mbar_add_tx(bar, p.plane_bytes + p.mask_bytes);
-                tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, bar);
-                tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, bar);
+                mbar_add_tx(barB, p.plane_bytes + p.mask_bytes);
+                tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, barB);
+                tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, barB);
             }
         }
         tp.inpaint = present ? 1 : 0;
-        if (ptid != 0) mbar_arrive(bar);
+        if (ptid != 0) mbar_arrive(barB);
         const bool in_range =
             idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
         const int si = in_range ? idx : 0;
@@ -414,16 +445,24 @@ __global__ void __launch_bounds__(kMaxThreads)
 
     if (tid == 0) {
         tp.arrived = 1;
-        if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
-        mbar_arrive(bar);
+        if constexpr (!kSplit) {
+            if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+        }
+        mbar_arrive(barB);
         // ---- wait for the boxes (the rest of the CTA sleeps at the barrier) ----
         if (!mbar_wait(bar, 0)) {
             flag(p.status, GS_DEV_TIMEOUT);
             tp.arrived = 0;
+            // let group B land before the CTA can exit (bounded)
+            if constexpr (kSplit) (void)mbar_wait_for(barB, 0, kDrainLimitNs);
         }
     }
     __syncthreads();
-    if (tp.ok != 1 || tp.arrived != 1 || y >= p.H) return;
+    if (tp.ok != 1 || tp.arrived != 1) return;
+    // rows past H (a ragged last band): no arithmetic, but with regions they still
+    // take part in the second CTA barrier
+    const bool active = y < p.H;
+    if (!kSplit && !active) return;
     const bool inpaint = INP && tp.inpaint != 0;
 
     const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
@@ -431,86 +470,90 @@ __global__ void __launch_bounds__(kMaxThreads)
 
     // positive branch
     f2 pos[CG][NP];
+    const f2 s2 = splat2(tp.s);
+    const f2 oms2 = splat2(tp.one_minus_s);
     if constexpr (REG) {
-        f2 wsum2[NP];
+        if (active) {
+            f2 wsum2[NP];
 #pragma unroll
-        for (int q = 0; q < NP; ++q) wsum2[q] = splat2(has_c ? 1.0f : 0.0f);
+            for (int q = 0; q < NP; ++q) wsum2[q] = splat2(has_c ? 1.0f : 0.0f);
 #pragma unroll
-        for (int k = 0; k < CG; ++k) {
-            if (has_c) {
-                const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_c, k * kstride + pix);
+            for (int k = 0; k < CG; ++k) {
+                if (has_c) {
+                    const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_c, k * kstride + pix);
 #pragma unroll
-                for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(v, q);
-            } else {
+                    for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(v, q);
+                } else {
 #pragma unroll
-                for (int q = 0; q < NP; ++q) pos[k][q] = splat2(0.0f);
+                    for (int q = 0; q < NP; ++q) pos[k][q] = splat2(0.0f);
+                }
             }
-        }
-        const float* rowtabs = reinterpret_cast<const float*>(st + p.rowtab_off);
-        for (int r = 0; r < p.n_regions; ++r) {
-            const TileRegion tr = tregs[r];
-            if (row < tr.row_lo || row >= tr.row_hi || x0 + VEC <= tr.x_lo || x0 >= tr.x_hi) continue;
-            // weights: row factor times the tabulated column factors (0 outside)
-            const float* tab = reinterpret_cast<const float*>(st + tr.tabx + 4 * x0);
-            const f2 wr2 = splat2(rowtabs[r * p.RB + row]);
-            f2 w2[NP];
+            const float* rowtabs = reinterpret_cast<const float*>(st + p.rowtab_off);
+            for (int r = 0; r < p.n_regions; ++r) {
+                const TileRegion tr = tregs[r];
+                if (row < tr.row_lo || row >= tr.row_hi || x0 + VEC <= tr.x_lo || x0 >= tr.x_hi) continue;
+                // weights: row factor times the tabulated column factors (0 outside)
+                const float* tab = reinterpret_cast<const float*>(st + tr.tabx + 4 * x0);
+                const f2 wr2 = splat2(rowtabs[r * p.RB + row]);
+                f2 w2[NP];
 #pragma unroll
-            for (int q = 0; q < VEC / 4; ++q) {
-                const float4 c4 = *reinterpret_cast<const float4*>(tab + 4 * q);
-                w2[2 * q] = mul2(wr2, mk2(c4.x, c4.y));
-                w2[2 * q + 1] = mul2(wr2, mk2(c4.z, c4.w));
-            }
-            if (tr.has_mask) {
-                const TmaRegion& R = regs[r];
-                const int ty = y - R.y0;
-                const int xs = x0 - R.x0;
-                const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
-                float wj[VEC];
+                for (int q = 0; q < VEC / 4; ++q) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(tab + 4 * q);
+                    w2[2 * q] = mul2(wr2, mk2(c4.x, c4.y));
+                    w2[2 * q + 1] = mul2(wr2, mk2(c4.z, c4.w));
+                }
+                if (tr.has_mask) {
+                    const TmaRegion& R = regs[r];
+                    const int ty = y - R.y0;
+                    const int xs = x0 - R.x0;
+                    const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
+                    float wj[VEC];
 #pragma unroll
-                for (int q = 0; q < NP; ++q) {
-                    wj[2 * q] = lo_of(w2[q]);
-                    wj[2 * q + 1] = hi_of(w2[q]);
+                    for (int q = 0; q < NP; ++q) {
+                        wj[2 * q] = lo_of(w2[q]);
+                        wj[2 * q + 1] = hi_of(w2[q]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        if (xs + j >= 0 && xs + j < R.w) wj[j] = wj[j] * __ldg(mrow + xs + j);
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
                 }
 #pragma unroll
-                for (int j = 0; j < VEC; ++j)
-                    if (xs + j >= 0 && xs + j < R.w) wj[j] = wj[j] * __ldg(mrow + xs + j);
-#pragma unroll
-                for (int q = 0; q < NP; ++q) w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
-            }
-#pragma unroll
-            for (int q = 0; q < NP; ++q) wsum2[q] = add2(wsum2[q], w2[q]);
-            // Box row `row` of this region's tile is frame row y.  Columns outside
-            // [0, w) are zeros (TMA fills the box past the slab's width, and
-            // vectors outside the box are not read), so no pixel outside the
-            // region can bring a non-finite value.
-            const int q0 = (x0 + tr.qoff) / VEC;      // exact: x0 + qoff is a multiple of VEC
-            const int sh = tr.sh;
-            const bool lo_ok = q0 >= 0 && q0 < tr.nq;
-            const bool hi_ok = q0 + 1 >= 0 && q0 + 1 < tr.nq;
-            const unsigned rbase = tr.rbase0 + static_cast<unsigned>(row) * tr.rrow;
-            const unsigned rk = tr.rk;
-            switch (sh) {
-                case 0: region_channels<T, VEC, CG, 0>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                case 1: region_channels<T, VEC, CG, 1>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                case 2: region_channels<T, VEC, CG, 2>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                case 3: region_channels<T, VEC, CG, 3>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                default:
-                    if constexpr (VEC == 8) {
-                        switch (sh) {
-                            case 4: region_channels<T, VEC, CG, 4>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                            case 5: region_channels<T, VEC, CG, 5>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                            case 6: region_channels<T, VEC, CG, 6>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                            default: region_channels<T, VEC, CG, 7>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                for (int q = 0; q < NP; ++q) wsum2[q] = add2(wsum2[q], w2[q]);
+                // Box row `row` of this region's tile is frame row y.  Columns outside
+                // [0, w) are zeros (TMA fills the box past the slab's width, and
+                // vectors outside the box are not read), so no pixel outside the
+                // region can bring a non-finite value.
+                const int q0 = (x0 + tr.qoff) / VEC;      // exact: x0 + qoff is a multiple of VEC
+                const int sh = tr.sh;
+                const bool lo_ok = q0 >= 0 && q0 < tr.nq;
+                const bool hi_ok = q0 + 1 >= 0 && q0 + 1 < tr.nq;
+                const unsigned rbase = tr.rbase0 + static_cast<unsigned>(row) * tr.rrow;
+                const unsigned rk = tr.rk;
+                switch (sh) {
+                    case 0: region_channels<T, VEC, CG, 0>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                    case 1: region_channels<T, VEC, CG, 1>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                    case 2: region_channels<T, VEC, CG, 2>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                    case 3: region_channels<T, VEC, CG, 3>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                    default:
+                        if constexpr (VEC == 8) {
+                            switch (sh) {
+                                case 4: region_channels<T, VEC, CG, 4>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                                case 5: region_channels<T, VEC, CG, 5>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                                case 6: region_channels<T, VEC, CG, 6>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                                default: region_channels<T, VEC, CG, 7>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                            }
                         }
-                    }
-                    break;
+                        break;
+                }
             }
-        }
 #pragma unroll
-        for (int q = 0; q < NP; ++q) {
-            const f2 inv = recip_or_zero2(wsum2[q]);
+            for (int q = 0; q < NP; ++q) {
+                const f2 inv = recip_or_zero2(wsum2[q]);
 #pragma unroll
-            for (int k = 0; k < CG; ++k) pos[k][q] = mul2(pos[k][q], inv);
+                for (int k = 0; k < CG; ++k) pos[k][q] = mul2(pos[k][q], inv);
+            }
         }
     } else {
 #pragma unroll
@@ -521,9 +564,26 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
     }
 
-    // combine, inpaint blend, Euler, round and store
-    const f2 s2 = splat2(tp.s);
-    const f2 oms2 = splat2(tp.one_minus_s);
+    if constexpr (kSplit) {
+        // combine while group B lands, then wait for it
+        if (active && has_u) {
+#pragma unroll
+            for (int k = 0; k < CG; ++k) {
+                const Raw<T, VEC> uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    pos[k][q] = fma2(s2, pos[k][q], mul2(oms2, widen2<T, VEC>(uv, q)));
+            }
+        }
+        if (tid == 0 && !mbar_wait(barB, 0)) {
+            flag(p.status, GS_DEV_TIMEOUT);
+            tp.arrived = 0;
+        }
+        __syncthreads();
+        if (tp.arrived != 1 || !active) return;
+    }
+
+    // combine (without regions), inpaint blend, Euler, round and store
     const f2 r2 = splat2(tp.ratio);
     f2 m2[NP], omm2[NP];
     if (INP && inpaint) {
@@ -543,12 +603,12 @@ __global__ void __launch_bounds__(kMaxThreads)
     for (int k = 0; k < CG; ++k) {
         const Raw<T, VEC> xv = ld_smem<T, VEC>(st + p.off_x, k * kstride + pix);
         Raw<T, VEC> uv, ov, xo, dn;
-        if (has_u) uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+        if (!kSplit && has_u) uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
         if (INP && inpaint) ov = ld_smem<T, VEC>(st + p.off_o, k * kstride + pix);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             f2 pred = pos[k][q];
-            if (has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(uv, q)));
+            if (!kSplit && has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(uv, q)));
             f2 den = pred;
             if (INP && inpaint) den = fma2(m2[q], pred, mul2(omm2[q], widen2<T, VEC>(ov, q)));
             const f2 xn = fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den);
