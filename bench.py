@@ -53,12 +53,12 @@ FALLBACK_HBM_GBS = 6800.0
 # capture, with the SHA-256 prefix of the kernel source it was taken on.  A
 # different source hash means the counters are stale: traffic is reported null.
 TRAFFIC = {
-    # profiles/guided_step_tma__bcg_bf16_b16.md: dram read 6,302,976 B + write 0 B
-    "bcg_bf16_b16": (6302976, "eea3af5c160b1a0b"),
+    # profiles/guided_step_tma__bcg_bf16_b16.md: dram read 6,302,720 B + write 0 B
+    "bcg_bf16_b16": (6302720, "ec90ab374bf8d418"),
     # profiles/guided_step_tma__large_steps.md
-    "area_fp16_b8": (2957568, "eea3af5c160b1a0b"),
-    "inpaint_bcg_bf16_b32": (69224192 + 876544, "eea3af5c160b1a0b"),
-    "sweep_bf16_b64": (100664064 + 5113344, "eea3af5c160b1a0b"),
+    "area_fp16_b8": (2957824, "ec90ab374bf8d418"),
+    "inpaint_bcg_bf16_b32": (69224448 + 822272, "ec90ab374bf8d418"),
+    "sweep_bf16_b64": (100664320 + 5597952, "ec90ab374bf8d418"),
 }
 
 
