@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference] [--no-pdl] [--no-tma]
+                    [--buckets N] [--batch B] [--cpu-procs P]
 
 A step is one call of gs_guided_step: the whole per-step path (per-sample
 parameters, regional accumulation, guidance combine, inpaint blend, Euler
@@ -23,6 +24,10 @@ Other keys of the JSON line:
 
 --impl reference times the oracle (the CPU restatement the kernel is checked
 against) on the same workload, metric and unit.
+
+--buckets and --batch change the named workload's bucket count or batch size
+(the sweeps of the measurement plan); --cpu-procs P times the oracle in P
+processes at once (one sample each) instead of one.
 
 With N > 1 every rank runs its own batch of the workload on its own GPU (the
 step is independent per sample and needs no exchange), so the job's throughput
@@ -79,7 +84,35 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--buckets", type=int, default=0,
+                    help="override the workload's bucket count (bucketized guidance only)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (masked samples scale with it)")
+    ap.add_argument("--cpu-procs", type=int, default=1,
+                    help="oracle processes timed at once for cpu_baseline / --impl reference")
     return ap.parse_args()
+
+
+def workload_for(args):
+    """The named workload with the --buckets / --batch overrides applied."""
+    import dataclasses
+
+    from bucketized_guidance_step_gb300.workloads import workload
+    wl = workload(args.workload)
+    name = wl.name
+    if args.buckets > 0:
+        if wl.guidance.cfg is not None:
+            raise SystemExit("--buckets needs a bucketized-guidance workload")
+        wl = dataclasses.replace(wl, guidance=dataclasses.replace(wl.guidance,
+                                                                  num_buckets=args.buckets))
+        name += f"@buckets{args.buckets}"
+    if args.batch > 0:
+        masked = wl.inpaint_samples
+        if masked is not None:
+            masked = max(1, masked * args.batch // wl.B)
+        wl = dataclasses.replace(wl, B=args.batch, inpaint_samples=masked)
+        name += f"@B{args.batch}"
+    return dataclasses.replace(wl, name=name)
 
 
 def kernel_source_hash() -> str:
@@ -310,7 +343,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     gs.load()
-    wl = workload(args.workload)
+    wl = workload_for(args)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
 
@@ -404,7 +437,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, args.cpu_procs)
     if pg is not None:
         pg.barrier()
         pg.destroy_process_group()
@@ -565,51 +598,66 @@ def oracle_sample(wl, n_samples: int, seed: int = 0):
     return x, sig, idx, kw
 
 
-def cpu_baseline(wl, seconds: float):
+def _oracle_timing(job):
+    """Worker: time the oracle on one sample of the workload (seed = worker index) for
+    `seconds` of wall time or exactly `steps` steps; returns (steps, elements, seconds)."""
+    wl, seed, seconds, steps, warm = job
     from oracle import step as O
-    n_s = 1
-    x, sig, idx, kw = oracle_sample(wl, n_s)
-    elems = x.size
-    O.guided_step(x, sig, idx, **kw)                        # warm
+    x, sig, idx, kw = oracle_sample(wl, 1, seed=seed)
+    for _ in range(warm):
+        O.guided_step(x, sig, idx, **kw)
     reps, t0 = 0, time.perf_counter()
     while True:
         O.guided_step(x, sig, idx, **kw)
         reps += 1
         dt = time.perf_counter() - t0
-        if dt >= seconds:
+        if (steps is None and dt >= seconds) or (steps is not None and reps >= steps):
             break
-    return {"value": round(reps * elems / dt / 1e9, 6), "unit": UNIT, "cores": 1,
+    return reps, x.size, dt
+
+
+def time_oracle(wl, procs: int, seconds=None, steps=None, warm: int = 1):
+    """(elements/s, steps per process, elements per step, wall seconds) of the oracle run in
+    `procs` processes at once (a spawned pool: safe after CUDA has been initialised)."""
+    jobs = [(wl, i, seconds, steps, warm) for i in range(procs)]
+    if procs == 1:
+        res = [_oracle_timing(jobs[0])]
+    else:
+        import multiprocessing as mp
+        with mp.get_context("spawn").Pool(procs) as pool:
+            res = pool.map(_oracle_timing, jobs)
+    wall = max(r[2] for r in res)
+    return sum(r[0] * r[1] for r in res) / wall, res[0][0], res[0][1], wall
+
+
+def cpu_baseline(wl, seconds: float, procs: int = 1):
+    rate, reps, elems, dt = time_oracle(wl, procs, seconds=seconds)
+    who = "one thread" if procs == 1 else f"{procs} processes, one sample each"
+    return {"value": round(rate / 1e9, 6), "unit": UNIT, "cores": procs,
             "kind": "oracle",
-            "sample": f"{n_s} of {wl.B} samples ({elems} elements) of {wl.name}, "
-                      f"{reps} oracle steps in {dt:.1f} s, float64 NumPy, one thread"}
+            "sample": f"1 of {wl.B} samples ({elems} elements) of {wl.name} per process, "
+                      f"{reps} oracle steps in {dt:.1f} s, float64 NumPy, {who}"}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    from bucketized_guidance_step_gb300.workloads import workload
-    from oracle import step as O
-    wl = workload(args.workload)
-    n_s = 1
-    x, sig, idx, kw = oracle_sample(wl, n_s)
-    elems = x.size
-    for _ in range(max(3, args.warmup if args.warmup < 20 else 20)):
-        O.guided_step(x, sig, idx, **kw)
+    wl = workload_for(args)
+    procs = max(1, args.cpu_procs)
     K = args.steps
-    t0 = time.perf_counter()
-    for _ in range(K):
-        O.guided_step(x, sig, idx, **kw)
-    dt = time.perf_counter() - t0
-    value = K * elems / dt / 1e9
+    rate, _, elems, dt = time_oracle(wl, procs, steps=K, warm=min(max(args.warmup, 1), 20))
+    value = rate / 1e9
     line = {
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
         "config": {"workload": describe(wl), "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W,
-                   "sample": f"each step runs {n_s} of the {wl.B} samples"},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{n_s} of {wl.B} samples ({elems} elements) per step"},
+                   "sample": f"each step runs 1 of the {wl.B} samples in each of {procs} "
+                             f"process(es)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": procs, "kind": "oracle",
+                         "sample": f"1 of {wl.B} samples ({elems} elements) per step and "
+                                   f"process"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
