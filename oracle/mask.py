@@ -44,3 +44,27 @@ def bilinear_resize(mask, H: int, W: int) -> np.ndarray:
     top = (1.0 - lx) * m[:, :, ylo][:, :, :, xlo] + lx * m[:, :, ylo][:, :, :, xhi]
     bot = (1.0 - lx) * m[:, :, yhi][:, :, :, xlo] + lx * m[:, :, yhi][:, :, :, xhi]
     return (1.0 - ly) * top + ly * bot
+
+
+def row_bits(lat_mask) -> np.ndarray:
+    """Which latent rows of each mask carry any nonzero value, packed 32 rows a word.
+
+    [Bm, 1, H, W] (any float) -> uint32 [Bm, ceil(H / 32)]: bit (y mod 32) of word
+    y // 32 is set when some m[b, 0, y, x] != 0 (a NaN counts as nonzero).
+
+    Where a sample's mask is 0 on a whole row, the inpaint blend of [SAMPLING]
+    "inpaint 与 mask" keeps the original there (den = 0 * pred + 1 * original), so
+    the guided prediction of that row is not needed: this summary says which rows
+    need it.  Written as the definition: one Python loop over rows.
+    """
+    m = np.asarray(lat_mask)
+    Bm, one, H, W = m.shape
+    if one != 1:
+        raise ValueError("mask must have one channel")
+    nw = (H + 31) // 32
+    out = np.zeros((Bm, nw), dtype=np.uint32)
+    for b in range(Bm):
+        for y in range(H):
+            if np.any(m[b, 0, y, :] != 0):
+                out[b, y // 32] |= np.uint32(1) << np.uint32(y % 32)
+    return out

@@ -37,3 +37,41 @@ def test_binary_1024_to_128_takes_quarter_values():
 def test_constant_mask_stays_constant():
     m = np.full((3, 1, 50, 40), 0.375)
     assert np.array_equal(M.bilinear_resize(m, 13, 11), np.full((3, 1, 13, 11), 0.375))
+
+
+def test_row_bits_hand_built():
+    m = np.zeros((3, 1, 70, 9))
+    m[0, 0, 37, 5] = 0.25                    # one pixel: word 1, bit 5
+    m[1, 0, 0, :] = 1.0                      # first row
+    m[1, 0, 69, 8] = -0.5                    # last row of the last, partial word (bit 5 of word 2)
+    m[2, 0, 31, 0] = np.nan                  # NaN counts as nonzero
+    m[2, 0, 32, 3] = -0.0                    # negative zero does not
+    got = M.row_bits(m)
+    want = np.array([[0, 1 << 5, 0],
+                     [1, 0, 1 << 5],
+                     [1 << 31, 0, 0]], dtype=np.uint32)
+    assert got.dtype == np.uint32 and got.shape == (3, 3)
+    assert np.array_equal(got, want)
+    assert np.array_equal(M.row_bits(np.zeros((2, 1, 64, 4))), np.zeros((2, 2), np.uint32))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_row_bits_of_resized_rectangles(seed):
+    """1024 -> 128 bilinear samples pixel rows 8y+3 and 8y+4 for latent row y, so a mask
+    made of rectangles (at least 8 pixels wide) has latent row y nonzero exactly when one
+    of those two pixel rows lies inside some rectangle's rows."""
+    rng = np.random.default_rng(seed)
+    pix = np.zeros((2, 1, 1024, 1024))
+    rects = []
+    for b in range(2):
+        for _ in range(rng.integers(1, 4)):
+            r0 = int(rng.integers(0, 960)); h = int(rng.integers(1, 200))
+            c0 = int(rng.integers(0, 1000)); w = int(rng.integers(8, 24))
+            pix[b, 0, r0:r0 + h, c0:c0 + w] = 1.0
+            rects.append((b, r0, min(r0 + h, 1024)))
+    bits = M.row_bits(M.bilinear_resize(pix, 128, 128))
+    for b in range(2):
+        for y in range(128):
+            covered = any(rb == b and (r0 <= 8 * y + 3 < r1 or r0 <= 8 * y + 4 < r1)
+                          for rb, r0, r1 in rects)
+            assert bool((int(bits[b, y // 32]) >> (y % 32)) & 1) == covered, (b, y)
