@@ -88,6 +88,10 @@ def parse_args():
                     help="override the workload's bucket count (bucketized guidance only)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (masked samples scale with it)")
+    ap.add_argument("--mask-rows", action="store_true",
+                    help="give the step the row summary of the inpaint mask (gs_mask_rows), so "
+                         "bands whose mask is 0 on every row skip reading the prediction; "
+                         "the roofline then counts only the bytes still required")
     ap.add_argument("--cpu-procs", type=int, default=1,
                     help="oracle processes timed at once for cpu_baseline / --impl reference")
     return ap.parse_args()
@@ -219,7 +223,7 @@ def plan(wl, world, dev):
     return sig_np, lut_np
 
 
-def build_sets(wl, R, dev, sig_np, lut_np, seed=0):
+def build_sets(wl, R, dev, sig_np, lut_np, seed=0, mask_rows=False):
     """R rotating input sets on the device, plus the shared per-run state."""
     import torch
 
@@ -275,6 +279,8 @@ def build_sets(wl, R, dev, sig_np, lut_np, seed=0):
         if wl.inpaint:
             st["mask"] = masks[k]
             st["orig"] = origs[k]
+            if mask_rows:
+                st["mask_rows"] = gs.mask_rows(masks[k])      # once per set, outside timing
             if nm < wl.B:
                 pres = torch.zeros(wl.B, dtype=torch.uint8, device=dev)
                 pres[:nm] = 1
@@ -292,6 +298,8 @@ def step_kwargs(wl, st, sig, lut, pdl, tma=True):
         kw["stacked"] = st["stacked"]
     else:
         kw["uncond"] = st["uncond"]
+    if "mask_rows" in st:
+        kw["mask_rows"] = st["mask_rows"]
     if "idx" in st:
         kw["step_idx"] = st["idx"]
     else:
@@ -352,7 +360,9 @@ def run_ours(args, world, rank, local):
     per_set = set_bytes(wl, one[0])
     R = max(2, math.ceil(4 * l2 / per_set))
     del one
-    sets, sig, lut, steps = build_sets(wl, R, dev, sig_np, lut_np, seed=1234 + rank)
+    use_rows = args.mask_rows and wl.inpaint
+    sets, sig, lut, steps = build_sets(wl, R, dev, sig_np, lut_np, seed=1234 + rank,
+                                       mask_rows=use_rows)
     prepared = []
     for st in sets:
         a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, (not args.no_pdl),
@@ -409,12 +419,24 @@ def run_ours(args, world, rank, local):
     from bucketized_guidance_step_gb300.workloads import step_inputs
     proto = step_inputs(wl, 0, B=1)
     abytes = algorithmic_bytes(wl, proto.regions)
+    if use_rows:
+        # required bytes: minus the prediction rows a blended sample's zero mask rows make
+        # unnecessary, averaged over the rotating sets' masks
+        from bucketized_guidance_step_gb300.accounting import skipped_prediction_bytes
+        nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
+        skipped = 0
+        for st in sets:
+            zero = (st["mask"][:nm, 0] == 0).all(dim=-1).cpu().numpy()
+            skipped += skipped_prediction_bytes(zero, wl.C, wl.W, wl.dtype,
+                                                cond=wl.full_frame_cond,
+                                                regions=[(r.y0, r.h, r.w) for r in proto.regions])
+        abytes -= skipped // len(sets)
     elems = wl.elements
     sec_step = ms_max / 1e3 / K
     value = world * elems / sec_step / 1e9
     achieved = abytes / (ms / 1e3 / K) / 1e9
     peak, peak_src = hbm_peak()
-    tr = TRAFFIC.get(wl.name)
+    tr = None if use_rows else TRAFFIC.get(wl.name)
     traffic = tr[0] if tr and tr[1] == kernel_source_hash() else None
 
     line = {
@@ -425,6 +447,9 @@ def run_ours(args, world, rank, local):
                    "l2": f"{R} rotating input sets of {per_set} B (>= 4x L2 of {l2} B)",
                    "launch": "CUDA graph replay" + (", PDL" if (not args.no_pdl) else ""),
                    "kernel": kernel,
+                   "mask_rows": ("row summary given: bands whose mask is 0 on every row skip "
+                                 "the prediction reads; bytes counted as still required")
+                   if use_rows else None,
                    "tuning": {k: os.environ[k] for k in ("GS_TMA_ROWS", "GS_TMA_CHANNELS", "GS_STEP_CHANNELS")
                               if k in os.environ},
                    "parallelism": f"replicas x{world} (independent batches)"},

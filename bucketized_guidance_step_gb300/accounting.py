@@ -31,3 +31,25 @@ def step_bytes(B: int, C: int, H: int, W: int, dtype: str, *, uncond: bool = Tru
     total += sum(B * C * h * w * e for h, w in regions)
     total += inpaint_samples * C * P * e + inpaint_samples * P * 4
     return total
+
+
+def skipped_prediction_bytes(zero_rows, C: int, W: int, dtype: str, *, cond: bool = True,
+                             regions: Iterable[Tuple[int, int, int]] = ()) -> int:
+    """Bytes of the prediction a step need not read once the mask's row summary is
+    given: on every row where a blended sample's mask is 0 everywhere, its uncond row
+    (and full-frame cond row) and the rows of every regional output covering it.
+
+    zero_rows: one sequence of per-row booleans per blended sample (True = the mask is
+    0 on the whole row).  regions: (y0, h, w) of each regional output.  Counted at row
+    granularity, the finest the summary resolves; a kernel that skips whole bands of
+    rows reads at least this much more.
+    """
+    e = ESIZE[dtype]
+    regions = list(regions)
+    frame_row = C * W * e * (2 if cond else 1)
+    total = 0
+    for rows in zero_rows:
+        for y, zero in enumerate(rows):
+            if zero:
+                total += frame_row + sum(C * w * e for y0, h, w in regions if y0 <= y < y0 + h)
+    return total

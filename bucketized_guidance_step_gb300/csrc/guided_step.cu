@@ -594,6 +594,9 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
     if (a->cond == nullptr && a->n_regions == 0) return GS_ERR_INVALID_ARG;
     if (a->inpaint_mask != nullptr && (a->original == nullptr || a->mask_bstride < 0))
         return GS_ERR_INVALID_ARG;
+    if (a->mask_rows != nullptr &&
+        (a->inpaint_mask == nullptr || (reinterpret_cast<uintptr_t>(a->mask_rows) & 3u) != 0))
+        return GS_ERR_INVALID_ARG;
     if (static_cast<long long>(a->B) * a->C * a->H * a->W > (1ll << 46)) return GS_ERR_UNSUPPORTED;
 
     StepParams p = {};
@@ -618,6 +621,7 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
     p.imask_bstride = a->mask_bstride;
     p.present = a->mask_present;
     p.orig = a->inpaint_mask != nullptr ? a->original : nullptr;
+    p.mask_rows = a->mask_rows;        // used by the TMA-fed kernel only
     p.status = a->dev_status;
     p.n_regions = a->n_regions;
     const long long esize = a->dtype == GS_DTYPE_F32 ? 4 : 2;

@@ -10,6 +10,10 @@
 // One thread per output pixel; consecutive threads take consecutive columns.
 // For an 8x downsample each output reads two neighbouring pixels of two source
 // rows, so a warp's loads cover two contiguous 1 KiB row spans.
+//
+// gs_mask_rows summarises a latent mask by row (which rows hold any nonzero
+// value) for the guided step's read skipping: one CTA per 32-row word, one warp
+// per row at a time, each lane reading every 32nd column.
 #include <cuda_runtime.h>
 
 #include "gs.h"
@@ -55,7 +59,42 @@ __global__ void __launch_bounds__(256) mask_prepare_kernel(const float* __restri
     dst[i] = static_cast<float>((1.0 - ty.frac) * top + ty.frac * bottom);
 }
 
+// Bit (y mod 32) of word y/32 of mask b: some m[b][y][x] != 0.  Grid (words, masks),
+// 256 threads: warp w scans rows w, w+8, w+16, w+24 of the word.
+__global__ void __launch_bounds__(256) mask_rows_kernel(const float* __restrict__ m, int H, int W,
+                                                        int words, unsigned* __restrict__ out) {
+    __shared__ unsigned bits;
+    const int wi = blockIdx.x;
+    const long long b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) bits = 0u;
+    __syncthreads();
+    for (int i = warp; i < 32; i += 8) {
+        const int y = wi * 32 + i;
+        if (y >= H) break;
+        const float* row = m + (b * H + y) * static_cast<long long>(W);
+        bool nz = false;
+        for (int x = lane; x < W; x += 32) nz = nz || __ldg(row + x) != 0.0f;
+        if (__any_sync(0xffffffffu, nz) && lane == 0) atomicOr(&bits, 1u << i);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) out[b * words + wi] = bits;
+}
+
 }  // namespace
+
+extern "C" gs_status gs_mask_rows(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
+                                  uint32_t* rows_out, gs_stream stream) {
+    if (lat_mask == nullptr || rows_out == nullptr) return GS_ERR_INVALID_ARG;
+    if (Bm < 1 || H < 1 || W < 1) return GS_ERR_INVALID_ARG;
+    if (Bm > 65535) return GS_ERR_UNSUPPORTED;
+    const int words = (H + 31) / 32;
+    mask_rows_kernel<<<dim3(static_cast<unsigned>(words), static_cast<unsigned>(Bm)), 256, 0,
+                       reinterpret_cast<cudaStream_t>(stream)>>>(lat_mask, H, W, words,
+                                                                 rows_out);
+    if (cudaGetLastError() != cudaSuccess) return GS_ERR_CUDA;
+    return GS_OK;
+}
 
 extern "C" gs_status gs_mask_prepare(const float* pix_mask, int32_t B, int32_t Hp, int32_t Wp,
                                      float* lat_mask, int32_t H, int32_t W, gs_stream stream) {

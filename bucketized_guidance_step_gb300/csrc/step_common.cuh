@@ -54,6 +54,7 @@ struct StepParams {
     long long imask_bstride;
     const unsigned char* present;
     const void* orig;
+    const unsigned* mask_rows;   // row summary of imask (gs_mask_rows) or null
     unsigned int* status;
     int n_sig;
     int step;

@@ -82,6 +82,8 @@ struct TmaParams {
     unsigned tile_bytes, plane_bytes, mask_bytes;
     unsigned off_x, off_u, off_c, off_o, off_m;
     unsigned rowtab_off;
+    const unsigned* mask_rows;   // row summary of the inpaint mask, or null
+    int mask_words;              // words per mask in mask_rows: ceil(H / 32)
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -235,6 +237,7 @@ struct TileParams {
     int ok;             // 1 = step this sample, 0 = skip it
     int inpaint;        // 1 = this sample blends with its original
     int arrived;        // 0 = the wait for the tile gave up
+    int need_pred;      // 0 = the band's mask rows are all zero: prediction not read
 };
 
 // One region as this tile's threads use it, built once per CTA by the region's
@@ -252,9 +255,10 @@ struct __align__(16) TileRegion {
     int tabx;
 };
 
-template <typename T, int CG, bool REG, bool INP>
+template <typename T, int CG, bool REG, bool INP, bool SKIP>
 __global__ void __launch_bounds__(kMaxThreads)
     guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
+    static_assert(INP || !SKIP, "read skipping needs the inpaint inputs");
     using S = typename T::scalar;
     constexpr int VEC = 16 / static_cast<int>(sizeof(S));
     constexpr int NP = VEC / 2;
@@ -319,14 +323,12 @@ __global__ void __launch_bounds__(kMaxThreads)
     grid_dependency_wait();
     grid_dependents_launch();
 
-    // Thread 0: the boxes that need nothing but the tile coordinates.  Each box's
-    // bytes are added to the barrier before the box is issued, and each feeding
-    // thread arrives after its last box, so the phase cannot complete early.
-    if (tid == 0) {
-        if constexpr (!kSplit) {
-            mbar_add_tx(bar, p.plane_bytes);
-            tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
-        }
+    // The prediction boxes (uncond, cond, regions) go on `bar` (group A when split).
+    // With a row summary of the inpaint mask they wait for the parameter thread,
+    // which skips them for a band whose mask rows are all zero in a blended sample.
+    // (SKIP: instances launched only when the row summary is given)
+    constexpr bool defer = SKIP;
+    auto issue_prediction = [&]() {
         if (has_u) {
             mbar_add_tx(bar, p.plane_bytes);
             tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
@@ -344,33 +346,67 @@ __global__ void __launch_bounds__(kMaxThreads)
                 tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], 0, y_band - ry0, z, bar);
             }
         }
+    };
+
+    // Thread 0: the boxes that need nothing but the tile coordinates.  Each box's
+    // bytes are added to the barrier before the box is issued, and each feeding
+    // thread arrives after its last box, so the phase cannot complete early.
+    if (tid == 0) {
+        if constexpr (!kSplit) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
+        }
+        if constexpr (!defer) issue_prediction();
         if constexpr (kSplit) {
-            // group A is complete: thread 0 is its only feeder
-            if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
-            mbar_arrive(bar);
+            if constexpr (!defer) {
+                // group A is complete: thread 0 is its only feeder
+                if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+                mbar_arrive(bar);
+            }
             mbar_add_tx(barB, p.plane_bytes);
             tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, barB);
         }
     }
 
-    // The parameter thread: the step index and the inpaint flag are independent
-    // loads issued together; the original and mask boxes go out as soon as the
-    // flag is known, then the scale and sigmas (which depend on the index) are read.
-    // With a single warp, thread 0 plays both parts (frame boxes first) and
-    // arrives once.
+    // The parameter thread: the step index, the inpaint flag and (with a row
+    // summary) the band's mask rows are independent loads issued together; the
+    // deferred prediction boxes and the original and mask boxes go out as soon as
+    // those are known, then the scale and sigmas (which depend on the index) are
+    // read.  With a single warp, thread 0 plays both parts (its boxes first) and
+    // arrives once on each barrier.
     const int ptid = nthreads > 32 ? 32 : 0;
     if (tid == ptid) {
         const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
-        bool present = false;
-        if (INP) {
-            present = p.present == nullptr || __ldg(p.present + b) != 0;
-            if (present) {
-                mbar_add_tx(barB, p.plane_bytes + p.mask_bytes);
-                tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, barB);
-                tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, barB);
+        const bool present = INP && (p.present == nullptr || __ldg(p.present + b) != 0);
+        bool need_pred = true;
+        if (defer && present) {
+            // rows y_band .. y_end-1 of this sample's mask: any nonzero?
+            const unsigned* words = p.mask_rows + (p.mask_shared ? 0 : b) * p.mask_words;
+            const int y_end = y_band + p.RB < p.H ? y_band + p.RB : p.H;
+            unsigned any = 0u;
+            for (int w = y_band >> 5; w <= (y_end - 1) >> 5; ++w) {
+                const int lo = y_band > w * 32 ? y_band - w * 32 : 0;
+                const int hi = y_end < w * 32 + 32 ? y_end - w * 32 : 32;   // rows [lo, hi)
+                const unsigned sel = (hi == 32 ? ~0u : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+                any |= __ldg(words + w) & sel;
+            }
+            need_pred = any != 0u;
+        }
+        if constexpr (defer) {
+            if (need_pred) issue_prediction();
+            if constexpr (kSplit) {
+                // group A is complete: with deferral this thread is its only feeder
+                if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+                mbar_arrive(bar);
             }
         }
+        if (INP && present) {
+            mbar_add_tx(barB, p.plane_bytes + p.mask_bytes);
+            tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, barB);
+            tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, barB);
+        }
         tp.inpaint = present ? 1 : 0;
+        if constexpr (defer) tp.need_pred = need_pred ? 1 : 0;
         if (ptid != 0) mbar_arrive(barB);
         const bool in_range =
             idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
@@ -464,6 +500,39 @@ __global__ void __launch_bounds__(kMaxThreads)
     const bool active = y < p.H;
     if (!kSplit && !active) return;
     const bool inpaint = INP && tp.inpaint != 0;
+    if (SKIP && tp.need_pred == 0) {
+        // A blended band whose mask is 0 on every row: den = original (up to the sign
+        // of zero), so the prediction was not loaded.  Only x and the original remain.
+        if constexpr (kSplit) {
+            if (tid == 0 && !mbar_wait(barB, 0)) {
+                flag(p.status, GS_DEV_TIMEOUT);
+                tp.arrived = 0;
+            }
+            __syncthreads();
+            if (tp.arrived != 1) return;
+        }
+        if (!active) return;
+        const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
+        const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
+        const long long plane = static_cast<long long>(p.H) * p.W;
+        const long long gbase =
+            static_cast<long long>(z) * plane + static_cast<long long>(y) * p.W + x0;
+        const f2 r2 = splat2(tp.ratio);
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+            const Raw<T, VEC> xv = ld_smem<T, VEC>(st + p.off_x, k * kstride + pix);
+            const Raw<T, VEC> ov = ld_smem<T, VEC>(st + p.off_o, k * kstride + pix);
+            Raw<T, VEC> xo;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const f2 den = widen2<T, VEC>(ov, q);
+                narrow2<T, VEC>(xo, q, fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den));
+            }
+            store_raw<T, VEC>(p.x_out, gbase + k * plane, xo);
+            if (p.den_out != nullptr) store_raw<T, VEC>(p.den_out, gbase + k * plane, ov);
+        }
+        return;
+    }
 
     const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
     const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
@@ -666,9 +735,9 @@ int gcd_int(int a, int b) {
     return a;
 }
 
-template <typename T, int CG, bool REG, bool INP>
+template <typename T, int CG, bool REG, bool INP, bool SKIP>
 gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stream, unsigned flags) {
-    auto kern = guided_step_tma_kernel<T, CG, REG, INP>;
+    auto kern = guided_step_tma_kernel<T, CG, REG, INP, SKIP>;
     static std::mutex mu;
     static unsigned smem_set[64] = {0};
     int dev = 0;
@@ -706,21 +775,25 @@ gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stre
     return GS_OK;
 }
 
-template <typename T, bool REG, bool INP>
+template <typename T, bool REG, bool INP, bool SKIP>
 gs_status launch_cg(TmaParams& p, int cg, int threads, unsigned smem, gs_stream stream,
                     unsigned flags) {
-    if (cg == 4) return launch_kernel<T, 4, REG, INP>(p, threads, smem, stream, flags);
-    if (cg == 2) return launch_kernel<T, 2, REG, INP>(p, threads, smem, stream, flags);
-    return launch_kernel<T, 1, REG, INP>(p, threads, smem, stream, flags);
+    if (cg == 4) return launch_kernel<T, 4, REG, INP, SKIP>(p, threads, smem, stream, flags);
+    if (cg == 2) return launch_kernel<T, 2, REG, INP, SKIP>(p, threads, smem, stream, flags);
+    return launch_kernel<T, 1, REG, INP, SKIP>(p, threads, smem, stream, flags);
 }
 
 template <typename T>
 gs_status launch_features(TmaParams& p, int cg, int threads, unsigned smem, bool reg, bool inp,
                           gs_stream stream, unsigned flags) {
-    if (reg && inp) return launch_cg<T, true, true>(p, cg, threads, smem, stream, flags);
-    if (reg) return launch_cg<T, true, false>(p, cg, threads, smem, stream, flags);
-    if (inp) return launch_cg<T, false, true>(p, cg, threads, smem, stream, flags);
-    return launch_cg<T, false, false>(p, cg, threads, smem, stream, flags);
+    // read skipping (a row summary of the inpaint mask) has instances of its own
+    const bool skip = inp && p.mask_rows != nullptr;
+    if (reg && skip) return launch_cg<T, true, true, true>(p, cg, threads, smem, stream, flags);
+    if (reg && inp) return launch_cg<T, true, true, false>(p, cg, threads, smem, stream, flags);
+    if (reg) return launch_cg<T, true, false, false>(p, cg, threads, smem, stream, flags);
+    if (skip) return launch_cg<T, false, true, true>(p, cg, threads, smem, stream, flags);
+    if (inp) return launch_cg<T, false, true, false>(p, cg, threads, smem, stream, flags);
+    return launch_cg<T, false, false, false>(p, cg, threads, smem, stream, flags);
 }
 
 }  // namespace
@@ -813,6 +886,8 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     p.has_c = sp.c != nullptr;
     p.mask_shared = inp && sp.imask_bstride == 0;
     p.test_wait_timeout = (flags & GS_LAUNCH_TEST_WAIT_TIMEOUT) ? 1 : 0;
+    p.mask_rows = inp ? sp.mask_rows : nullptr;
+    p.mask_words = (H + 31) / 32;
     p.n_regions = sp.n_regions;
 
     // stage layout

@@ -36,9 +36,9 @@ GS_MAX_REGIONS = 16
 GS_LAUNCH_PDL = 1
 GS_LAUNCH_NO_TMA = 2
 GS_LAUNCH_TEST_WAIT_TIMEOUT = 4
-GS_ABI_VERSION = 1
+GS_ABI_VERSION = 2
 
-EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_guided_step",
+EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_guided_step",
            "gs_step_kernel_kind", "gs_status_from_word", "gs_status_string", "gs_abi_version")
 GS_KERNEL_SCALAR, GS_KERNEL_VECTOR, GS_KERNEL_TMA = 0, 1, 2
 KERNEL_NAMES = {0: "scalar", 1: "vector", 2: "tma"}
@@ -91,7 +91,8 @@ class StepArgs(ctypes.Structure):
                 ("cfg", ctypes.c_float),
                 ("inpaint_mask", ctypes.c_void_p), ("mask_bstride", ctypes.c_int64),
                 ("mask_present", ctypes.c_void_p), ("original", ctypes.c_void_p),
-                ("dev_status", ctypes.c_void_p), ("launch_flags", ctypes.c_uint32)]
+                ("dev_status", ctypes.c_void_p), ("launch_flags", ctypes.c_uint32),
+                ("mask_rows", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -117,13 +118,14 @@ def load() -> ctypes.CDLL:
         lib.gs_sigmas.argtypes = [ctypes.POINTER(ScheduleDesc), p, i32, p, p]
         lib.gs_bucket_plan.argtypes = [i32, i32, ctypes.POINTER(CurveDesc), p, p, p]
         lib.gs_mask_prepare.argtypes = [p, i32, i32, i32, p, i32, i32, p]
+        lib.gs_mask_rows.argtypes = [p, i32, i32, i32, p, p]
         lib.gs_guided_step.argtypes = [ctypes.POINTER(StepArgs), p]
         lib.gs_step_kernel_kind.argtypes = [ctypes.POINTER(StepArgs), p]
         lib.gs_status_from_word.argtypes = [ctypes.c_uint32]
         lib.gs_status_string.argtypes = [i32]
         lib.gs_status_string.restype = ctypes.c_char_p
         lib.gs_abi_version.argtypes = []
-        for f in ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_guided_step",
+        for f in ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_guided_step",
                   "gs_step_kernel_kind", "gs_status_from_word", "gs_abi_version"):
             getattr(lib, f).restype = i32
         if lib.gs_abi_version() != GS_ABI_VERSION:
@@ -226,6 +228,25 @@ def mask_prepare(pix_mask, H: int, W: int, out=None, stream=None):
     return out
 
 
+def mask_rows(lat_mask, out=None, stream=None):
+    """gs_mask_rows: [Bm,1,H,W] fp32 latent mask -> [Bm, ceil(H/32)] int32 words whose
+    bit (y mod 32) of word y // 32 says whether row y holds any nonzero value (the
+    bits of a uint32, stored as int32)."""
+    torch = _torch()
+    Bm, one, H, W = lat_mask.shape
+    if one != 1:
+        raise ValueError("latent mask must have one channel")
+    words = (H + 31) // 32
+    if out is None:
+        out = torch.empty((Bm, words), dtype=torch.int32, device=lat_mask.device)
+    elif tuple(out.shape) != (Bm, words):
+        raise ValueError(f"out must be [{Bm}, {words}]")
+    _check("gs_mask_rows", load().gs_mask_rows(
+        _dptr(lat_mask, "lat_mask", torch.float32), Bm, H, W, _dptr(out, "out", torch.int32),
+        _stream_ptr(stream)))
+    return out
+
+
 @dataclass
 class Region:
     """One regional conditioning output for ``guided_step`` (see gs_region)."""
@@ -256,7 +277,7 @@ def _dtype_code(t) -> int:
 def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=None,
                    step: int = 0, scale_lut=None, cfg: float = 1.0,
                    regions: Sequence[Region] = (), inpaint_mask=None, mask_present=None,
-                   original=None, x_out=None, denoised_out=None, status=None,
+                   original=None, mask_rows=None, x_out=None, denoised_out=None, status=None,
                    pdl: bool = False, tma: bool = True, test_wait_timeout: bool = False):
     """Build a gs_step_args (and the region array it points to) from tensors."""
     torch = _torch()
@@ -323,6 +344,12 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
     a.mask_present = _dptr(mask_present, "mask_present", torch.uint8)
     a.original = _dptr(original, "original", dt)
     a.dev_status = _dptr(status, "status", torch.int32)
+    if mask_rows is not None:
+        if inpaint_mask is None:
+            raise ValueError("mask_rows needs inpaint_mask")
+        if tuple(mask_rows.shape) != (inpaint_mask.shape[0], (H + 31) // 32):
+            raise ValueError("mask_rows must be [masks, ceil(H/32)] (from mask_rows())")
+    a.mask_rows = _dptr(mask_rows, "mask_rows", torch.int32)
     a.launch_flags = ((GS_LAUNCH_PDL if pdl else 0) | (0 if tma else GS_LAUNCH_NO_TMA) |
                       (GS_LAUNCH_TEST_WAIT_TIMEOUT if test_wait_timeout else 0))
     return a, reg_arr
@@ -346,8 +373,10 @@ def guided_step(x, *, sigmas, stream=None, **kw):
     Keyword arguments follow gs_step_args: uncond / cond or stacked, regions,
     step_idx (int32 [B]) or step, scale_lut (fp32) or cfg, inpaint_mask
     ([B or 1, 1, H, W] fp32), mask_present (uint8 [B]), original, x_out,
-    denoised_out, status (int32 [1], device flags OR-ed in), pdl, tma (False forces
-    the register-streaming kernel).
+    denoised_out, status (int32 [1], device flags OR-ed in), mask_rows (the row
+    summary of inpaint_mask from ``mask_rows()``: bands whose mask is 0 on every row
+    then skip reading the prediction), pdl, tma (False forces the register-streaming
+    kernel).
     """
     args, _keep = make_step_args(x, sigmas=sigmas, **kw)
     launch_step(args, stream)

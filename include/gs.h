@@ -170,6 +170,23 @@ gs_status gs_bucket_plan(int32_t steps, int32_t num_buckets, const gs_curve_desc
 gs_status gs_mask_prepare(const float* pix_mask, int32_t B, int32_t Hp, int32_t Wp,
                           float* lat_mask, int32_t H, int32_t W, gs_stream stream);
 
+/*
+ * gs_mask_rows -- which rows of a latent mask carry any nonzero value.
+ *
+ * Where a sample's mask is 0 on a whole row, the inpaint blend keeps the original
+ * there (den = 0 * pred + 1 * original, [SAMPLING] "inpaint 与 mask"), so the guided
+ * prediction of that row is not needed.  This summary, computed once per run,
+ * lets gs_guided_step skip reading it (gs_step_args.mask_rows).
+ *
+ * lat_mask: device float[Bm][1][H][W] (row pitch W).
+ * rows_out: device uint32[Bm][ceil(H/32)]: bit (y mod 32) of word y/32 of mask b
+ *           is 1 when some lat_mask[b][0][y][x] != 0 (NaN counts as nonzero,
+ *           -0 as zero).  Caller-owned.
+ * Errors: GS_ERR_INVALID_ARG (NULL pointers, sizes < 1), GS_ERR_CUDA.
+ */
+gs_status gs_mask_rows(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
+                       uint32_t* rows_out, gs_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* The guided step (device, one kernel launch per call).                     */
 /* ------------------------------------------------------------------------ */
@@ -253,6 +270,16 @@ typedef struct gs_step_args {
 
     uint32_t* dev_status;       /* device uint32 or NULL: GS_DEV_* bits OR-ed in         */
     uint32_t  launch_flags;     /* GS_LAUNCH_*                                           */
+
+    /* Optional row summary of inpaint_mask from gs_mask_rows: device
+       uint32[.][ceil(H/32)], one row of words per mask, sample b's at
+       b * ceil(H/32) words (0 when mask_bstride is 0); NULL = not given.  Given it,
+       the TMA-fed kernels read neither uncond, cond nor any region output for a
+       band of rows in which a blended sample's mask is 0 on every row: there
+       den = original exactly, whatever the prediction (the prediction is taken as
+       0, so a non-finite prediction there does not propagate).  The caller keeps
+       it in step with inpaint_mask. */
+    const uint32_t* mask_rows;
 } gs_step_args;
 
 /*
@@ -325,7 +352,7 @@ gs_status gs_status_from_word(uint32_t word);
 const char* gs_status_string(gs_status status);
 
 /* ABI version of this header (bumped on any layout change). */
-#define GS_ABI_VERSION 1
+#define GS_ABI_VERSION 2
 int32_t gs_abi_version(void);
 
 #ifdef __cplusplus

@@ -237,3 +237,21 @@ def test_bounded_wait_expires_with_status(kernel_choice):
     gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=out, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and not torch.equal(out, sentinel)
+
+
+@pytest.mark.parametrize("shape", [(4, 4, 16, 16), (32, 8, 64, 128)], ids=["small", "large"])
+def test_mask_rows_with_shared_mask(shape, kernel_choice):
+    """One mask shared by every sample (mask_bstride 0): its row summary is one row of
+    words, and the step with it equals the step without it bit for bit."""
+    B, C, H, W = shape
+    x, u, c, o = (rnd(shape, s, torch.bfloat16) for s in (46, 47, 48, 49))
+    m = torch.zeros((1, 1, H, W), device=DEV)
+    m[0, 0, H // 4:H // 2, W // 3:W // 2] = 0.75          # most rows zero
+    rows = gs.mask_rows(m)
+    a, b = torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=a, inpaint_mask=m,
+                   original=o)
+    gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=b, inpaint_mask=m,
+                   original=o, mask_rows=rows)
+    torch.cuda.synchronize()
+    assert same_bits(a, b)

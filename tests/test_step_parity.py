@@ -31,8 +31,17 @@ def _cuda(t):
 def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None,
              step: int = None, region_masks: bool = False, offset: int = 0,
              uncond_none: bool = False, want_den: bool = False, pitch_align: int = 8,
-             tma: bool = True, expect_kernel: str = None):
-    """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok)."""
+             tma: bool = True, expect_kernel: str = None, mask_rows: bool = False,
+             poison: bool = False):
+    """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok).
+
+    mask_rows: pass the row summary of the latent mask (gs_mask_rows), so that bands
+    whose mask is 0 on every row skip reading the prediction.  poison: on the GPU
+    side only, fill uncond, cond and the region slabs with NaN on every 32-row block
+    of a blended sample whose mask is 0 there; the kernel must not read them (a read
+    would carry NaN through 0 * pred into the output), and the oracle, which sees
+    the clean values, must agree.
+    """
     inp = step_inputs(wl, step_seed, B=B, C=C, H=H, W=W, region_masks=region_masks,
                       pitch_align=pitch_align)
     dt = DTYPES[wl.dtype]
@@ -63,13 +72,39 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
         view.copy_(t.to(DEV))
         return view
 
+    u_gpu, c_gpu = u, inp.cond
+    reg_outs = [r.out for r in inp.regions]
+    if poison:
+        assert lat is not None and mask_rows
+        present_np = (np.ones(Bn, bool) if inp.mask_present is None
+                      else inp.mask_present.numpy().astype(bool))
+        m_np = lat.numpy()
+        u_gpu = None if u is None else u.clone()
+        c_gpu = None if inp.cond is None else inp.cond.clone()
+        reg_outs = [o.clone() for o in reg_outs]
+        nan = float("nan")
+        for bi in range(Bn):
+            if not present_np[bi]:
+                continue
+            mb = m_np[bi if m_np.shape[0] > 1 else 0, 0]
+            for y0 in range(0, Hn, 32):
+                if mb[y0:y0 + 32].any():
+                    continue
+                if u_gpu is not None:
+                    u_gpu[bi, :, y0:y0 + 32] = nan
+                if c_gpu is not None:
+                    c_gpu[bi, :, y0:y0 + 32] = nan
+                for r, o in zip(inp.regions, reg_outs):
+                    lo, hi = max(y0, r.y0), min(y0 + 32, r.y0 + r.h)
+                    if lo < hi:
+                        o[bi, :, lo - r.y0:hi - r.y0] = nan
     xd = dev_latent(x)
     outd = dev_latent(torch.full_like(x, float("nan")))
     dend = dev_latent(torch.full_like(x, float("nan"))) if want_den else None
-    regs = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, _cuda(r.out),
-                      _cuda(r.mask)) for r in inp.regions]
+    regs = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, _cuda(o),
+                      _cuda(r.mask)) for r, o in zip(inp.regions, reg_outs)]
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    kw = dict(uncond=dev_latent(u), cond=dev_latent(inp.cond), regions=regs,
+    kw = dict(uncond=dev_latent(u_gpu), cond=dev_latent(c_gpu), regions=regs,
               sigmas=torch.from_numpy(sig).to(DEV), x_out=outd, denoised_out=dend,
               status=status, tma=tma)
     if inp.step_idx is not None:
@@ -83,6 +118,8 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     if lat is not None:
         kw.update(inpaint_mask=_cuda(lat), original=dev_latent(inp.original),
                   mask_present=_cuda(inp.mask_present))
+        if mask_rows:
+            kw["mask_rows"] = gs.mask_rows(kw["inpaint_mask"])
     args, _keep = gs.make_step_args(xd, **kw)
     kind = gs.kernel_kind(args)
     if expect_kernel is not None:
@@ -220,3 +257,29 @@ def test_large_fp32_fp16(dtype, regions, tma):
     rep, *_ = run_case(wl, region_masks=regions > 0, want_den=True, tma=tma,
                        expect_kernel="tma" if tma else "vector")
     assert rep.n == wl.elements
+
+
+@pytest.mark.parametrize("poison", [False, True], ids=["clean", "poisoned"])
+@pytest.mark.parametrize("wl", [WORKLOADS[3], WORKLOADS[4]], ids=["inpaint", "sweep"])
+def test_mask_rows_skip_reads(wl, poison):
+    """Read skipping with the mask's row summary: the full-size inpaint and sweep steps
+    match the oracle; with the skipped bands' prediction poisoned (NaN) they still do
+    (the kernel never read it); and the output equals the step without the summary
+    bit for bit."""
+    rep, got, ref, ok = run_case(wl, mask_rows=True, poison=poison, expect_kernel="tma")
+    assert rep.n == wl.elements and np.isfinite(got).all()
+    _, plain, _, _ = run_case(wl, expect_kernel="tma")
+    assert np.array_equal(got.view(np.uint64), plain.view(np.uint64))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16"])
+def test_mask_rows_skip_reads_other_shapes(dtype):
+    """Read skipping in small-step tiles (one channel, 8 or 16 rows, one barrier) with
+    region masks, a denoised output and a ragged last band, poisoned."""
+    base = WORKLOADS[4]
+    wl = Workload("skip", 24, 8, 70, 64, dtype, base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=3, region_side=(8, 60), inpaint=True,
+                  inpaint_samples=16, seed=17)
+    rep, got, _, _ = run_case(wl, region_masks=True, want_den=True, mask_rows=True,
+                              poison=True, expect_kernel="tma")
+    assert rep.n == wl.elements and np.isfinite(got).all()
