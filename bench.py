@@ -59,11 +59,14 @@ FALLBACK_HBM_GBS = 6800.0
 # different source hash means the counters are stale: traffic is reported null.
 TRAFFIC = {
     # profiles/guided_step_tma__bcg_bf16_b16.md: dram read 6,302,720 B + write 0 B
-    "bcg_bf16_b16": (6302720, "ec90ab374bf8d418"),
+    "bcg_bf16_b16": (6302720, "bef684dc0774f685"),
     # profiles/guided_step_tma__large_steps.md
-    "area_fp16_b8": (2957824, "ec90ab374bf8d418"),
-    "inpaint_bcg_bf16_b32": (69224448 + 822272, "ec90ab374bf8d418"),
-    "sweep_bf16_b64": (100664320 + 5597952, "ec90ab374bf8d418"),
+    "area_fp16_b8": (2958080, "bef684dc0774f685"),
+    "inpaint_bcg_bf16_b32": (69224192 + 688896, "bef684dc0774f685"),
+    "sweep_bf16_b64": (100664832 + 5042944, "bef684dc0774f685"),
+    # with --mask-rows (profiles/guided_step_tma__read_skipping.md)
+    "inpaint_bcg_bf16_b32+mask_rows": (51107328 + 92160, "bef684dc0774f685"),
+    "sweep_bf16_b64+mask_rows": (88788224 + 3634432, "bef684dc0774f685"),
 }
 
 
@@ -436,7 +439,7 @@ def run_ours(args, world, rank, local):
     value = world * elems / sec_step / 1e9
     achieved = abytes / (ms / 1e3 / K) / 1e9
     peak, peak_src = hbm_peak()
-    tr = None if use_rows else TRAFFIC.get(wl.name)
+    tr = TRAFFIC.get(wl.name + ("+mask_rows" if use_rows else ""))
     traffic = tr[0] if tr and tr[1] == kernel_source_hash() else None
 
     line = {
