@@ -21,6 +21,13 @@ Readings taken where the pages are silent:
 * A bucket's scale is the curve sampled at the bucket's midpoint progress,
   (b + 1/2) / N.  The C ABI also accepts an explicit table, which makes the
   step independent of this choice.
+* Section 2 also allows "simple linear interpolation" inside a segment: then a
+  step's scale is the straight line between the curve's values at its bucket's
+  two edges, b/N and (b+1)/N, evaluated at the step's progress.
+* Section 5 names three curve shapes: linear decay, front-high-flat (strong for
+  the first 20 % of steps) and a middle peak (stronger guidance in the middle
+  stage).  The middle peak is read as a tent: the base value at progress 0 and 1,
+  rising linearly to the peak value at progress `apex`.
 """
 
 from __future__ import annotations
@@ -47,6 +54,15 @@ def step_curve(v_hi: float, v_lo: float, edge: float):
     return lambda p: v_hi if p < edge else v_lo
 
 
+def peak_curve(v_peak: float, v_base: float, apex: float):
+    """Middle peak: v_base at progress 0 and 1, linear to v_peak at progress apex (0 < apex < 1)."""
+    def c(p):
+        if p <= apex:
+            return v_base + (v_peak - v_base) * (p / apex)
+        return v_base + (v_peak - v_base) * ((1.0 - p) / (1.0 - apex))
+    return c
+
+
 def bucket_table(curve, num_buckets: int) -> np.ndarray:
     """table[b] = curve((b + 1/2) / N), float64."""
     return np.array([curve((b + 0.5) / num_buckets) for b in range(num_buckets)],
@@ -61,4 +77,21 @@ def plan(steps: int, num_buckets: int, table) -> tuple[np.ndarray, np.ndarray]:
     ids = np.array([bucket_of_step(i, steps, num_buckets) for i in range(steps)],
                    dtype=np.int32)
     scales = table[ids].astype(np.float32)
+    return ids, scales
+
+
+def plan_interpolated(steps: int, num_buckets: int, curve) -> tuple[np.ndarray, np.ndarray]:
+    """Per-step bucket ids and scales with linear interpolation inside each bucket:
+    scale(i) = c(b/N) + (c((b+1)/N) - c(b/N)) * f, f = binary64(i/S) * N - b, rounded
+    to float32."""
+    ids = np.array([bucket_of_step(i, steps, num_buckets) for i in range(steps)],
+                   dtype=np.int32)
+    scales = np.empty(steps, dtype=np.float32)
+    for i in range(steps):
+        b = int(ids[i])
+        p = float(i) / float(steps)
+        lo = curve(b / num_buckets)
+        hi = curve((b + 1) / num_buckets)
+        f = p * num_buckets - b
+        scales[i] = np.float32(lo + (hi - lo) * f)
     return ids, scales

@@ -92,3 +92,40 @@ def test_plan_linear_8_buckets_50_steps():
 def test_plan_rejects_wrong_table():
     with pytest.raises(ValueError):
         Bk.plan(10, 4, [1.0, 2.0])
+
+
+def test_peak_curve_hand_values():
+    c = Bk.peak_curve(3.0, 1.0, 0.5)
+    assert [c(p) for p in (0.0, 0.25, 0.5, 0.75, 1.0)] == [1.0, 2.0, 3.0, 2.0, 1.0]
+    a = Bk.peak_curve(3.0, 1.0, 0.25)
+    assert [a(0.125), a(0.25), a(0.625)] == [2.0, 3.0, 2.0]
+    assert list(Bk.bucket_table(c, 4)) == [1.5, 2.5, 2.5, 1.5]
+
+
+def test_interpolated_linear_curve_is_the_curve():
+    """Interpolating a straight line between bucket edges gives the line itself: every
+    step's scale is the exact-rational v0 + (v1 - v0) i/S within one float32 ulp."""
+    for S, N in ((50, 8), (28, 16), (37, 5)):
+        _, s = Bk.plan_interpolated(S, N, Bk.linear_curve(2.0, 1.2))
+        for i in range(S):
+            exact = Fraction(2) + (Fraction(6, 5) - 2) * Fraction(i, S)
+            want = np.float32(float(exact))
+            assert abs(float(s[i]) - float(want)) <= float(np.spacing(want)), (S, N, i)
+
+
+def test_interpolated_one_step_per_bucket_samples_the_curve():
+    """With as many buckets as steps every step starts its bucket (f = 0): its scale is
+    the curve at i/S exactly."""
+    c = Bk.peak_curve(2.5, 1.0, 0.4)
+    ids, s = Bk.plan_interpolated(20, 20, c)
+    assert list(ids) == list(range(20))
+    assert all(s[i] == np.float32(c(i / 20)) for i in range(20))
+
+
+def test_interpolated_step_curve_ramps_inside_the_edge_bucket():
+    # S = 10, N = 2, edge 0.3: bucket 0 spans progress [0, 0.5) and holds the edge, so its
+    # steps ramp from c(0) = 3.0 to c(0.5) = 1.5; bucket 1 is flat at 1.5
+    ids, s = Bk.plan_interpolated(10, 2, Bk.step_curve(3.0, 1.5, 0.3))
+    assert list(ids) == [0] * 5 + [1] * 5
+    want = [3.0, 2.7, 2.4, 2.1, 1.8] + [1.5] * 5
+    assert np.array_equal(s, np.array(want, dtype=np.float32))
