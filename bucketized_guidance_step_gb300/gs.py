@@ -31,7 +31,7 @@ GS_ERR_TIMEOUT = 8
 GS_DEV_STEP_RANGE, GS_DEV_NEED_UNCOND, GS_DEV_SIGMA, GS_DEV_TIMEOUT = 1, 2, 4, 8
 GS_DTYPE_F32, GS_DTYPE_BF16, GS_DTYPE_F16 = 0, 1, 2
 GS_SCHED_KARRAS, GS_SCHED_NORMAL = 0, 1
-GS_CURVE_LINEAR, GS_CURVE_STEP, GS_CURVE_TABLE = 0, 1, 2
+GS_CURVE_LINEAR, GS_CURVE_STEP, GS_CURVE_TABLE, GS_CURVE_PEAK = 0, 1, 2, 3
 GS_MAX_REGIONS = 16
 GS_LAUNCH_PDL = 1
 GS_LAUNCH_NO_TMA = 2
@@ -68,7 +68,7 @@ class ScheduleDesc(ctypes.Structure):
 
 class CurveDesc(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("v0", ctypes.c_double), ("v1", ctypes.c_double),
-                ("edge", ctypes.c_double)]
+                ("edge", ctypes.c_double), ("interp", ctypes.c_int32)]
 
 
 class RegionDesc(ctypes.Structure):
@@ -175,12 +175,17 @@ def sigmas(kind: str, steps: int, *, sigma_min: float = 0.0292, sigma_max: float
 
 
 def bucket_plan(steps: int, num_buckets: int, *, curve: str = "linear", v0: float = 0.0,
-                v1: float = 0.0, edge: float = 0.0,
+                v1: float = 0.0, edge: float = 0.0, interp: bool = False,
                 table: Optional[Sequence[float]] = None) -> Tuple[np.ndarray, np.ndarray]:
-    """gs_bucket_plan: per-step bucket ids (int32) and scales (float32)."""
+    """gs_bucket_plan: per-step bucket ids (int32) and scales (float32).
+
+    curve: "linear" (v0 -> v1), "step" (v0 before progress edge, v1 after), "peak"
+    (v1 at both ends, v0 at progress edge) or "table"; interp: linear interpolation
+    inside each bucket between the curve's values at its edges."""
     lib = load()
-    kind = {"linear": GS_CURVE_LINEAR, "step": GS_CURVE_STEP, "table": GS_CURVE_TABLE}.get(curve, -1)
-    c = CurveDesc(kind, v0, v1, edge)
+    kind = {"linear": GS_CURVE_LINEAR, "step": GS_CURVE_STEP, "table": GS_CURVE_TABLE,
+            "peak": GS_CURVE_PEAK}.get(curve, -1)
+    c = CurveDesc(kind, v0, v1, edge, 1 if interp else 0)
     tab = None if table is None else np.ascontiguousarray(table, dtype=np.float64)
     ids = np.zeros(max(int(steps), 1), dtype=np.int32)
     lut = np.zeros(max(int(steps), 1), dtype=np.float32)

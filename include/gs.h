@@ -117,15 +117,24 @@ gs_status gs_sigmas(const gs_schedule_desc* desc, float* out, int32_t cap,
 /* Bucket plan (host).                                                       */
 /* ------------------------------------------------------------------------ */
 
-enum { GS_CURVE_LINEAR = 0, GS_CURVE_STEP = 1, GS_CURVE_TABLE = 2 };
+enum { GS_CURVE_LINEAR = 0, GS_CURVE_STEP = 1, GS_CURVE_TABLE = 2, GS_CURVE_PEAK = 3 };
 
 typedef struct gs_curve_desc {
     int32_t kind;   /* GS_CURVE_LINEAR: v0 at progress 0 -> v1 at progress 1
                        GS_CURVE_STEP:   v0 while progress < edge, v1 afterwards
+                                        ([BCG] section 5 "front high, then flat")
+                       GS_CURVE_PEAK:   v1 at progress 0 and 1, rising linearly to v0 at
+                                        progress edge, 0 < edge < 1 ([BCG] section 5
+                                        "middle peak")
                        GS_CURVE_TABLE:  the table argument gives one scale per bucket */
     double  v0;
     double  v1;
     double  edge;
+    int32_t interp; /* 0: a bucket's scale is the curve at its midpoint progress;
+                       1: "simple linear interpolation" inside a bucket ([BCG] section
+                       2): a step's scale is the straight line between the curve's
+                       values at its bucket's edges b/N and (b+1)/N, at the step's
+                       progress.  Not with GS_CURVE_TABLE. */
 } gs_curve_desc;
 
 /*
@@ -136,7 +145,8 @@ typedef struct gs_curve_desc {
  * is cut into num_buckets constant segments.  Section 4 stage 1: each step
  * reads its scale from the per-bucket table.  A bucket's scale is the curve at
  * the bucket's midpoint progress (b + 1/2)/num_buckets, unless an explicit
- * table is given.
+ * table is given or curve->interp asks for interpolation inside the bucket
+ * (then step i's scale is c(b/N) + (c((b+1)/N) - c(b/N)) * (i/steps * N - b)).
  *
  * steps:           the schedule's step count (n_sigmas - 1), >= 1.
  * num_buckets:     >= 1.
@@ -145,7 +155,7 @@ typedef struct gs_curve_desc {
  * bucket_of_step:  host int32[steps], may be NULL.
  * scale_of_step:   host float[steps] (the scale LUT the step kernel reads),
  *                  may be NULL.
- * Errors: GS_ERR_INVALID_ARG.
+ * Errors: GS_ERR_INVALID_ARG (also: interp with a table, a peak apex outside (0, 1)).
  */
 gs_status gs_bucket_plan(int32_t steps, int32_t num_buckets, const gs_curve_desc* curve,
                          const double* table, int32_t* bucket_of_step, float* scale_of_step);

@@ -78,3 +78,35 @@ def test_bucket_explicit_table():
     ids, lut = gs.bucket_plan(10, 4, curve="table", table=table)
     wids, wlut = OB.plan(10, 4, table)
     assert ids.tolist() == wids.tolist() and np.array_equal(lut, wlut)
+
+
+def _oracle_curve(curve, v0, v1, edge):
+    if curve == "linear":
+        return OB.linear_curve(v0, v1)
+    if curve == "step":
+        return OB.step_curve(v0, v1, edge)
+    return OB.peak_curve(v0, v1, edge)
+
+
+@pytest.mark.parametrize("S,N,curve,v0,v1,edge", [
+    (50, 8, "peak", 3.0, 1.0, 0.5), (28, 16, "peak", 2.4, 1.2, 0.3), (37, 37, "peak", 5.0, 1.0, 0.7),
+    (50, 8, "linear", 2.0, 1.2, 0.0), (28, 16, "step", 3.0, 1.5, 0.2), (10, 2, "step", 3.0, 1.5, 0.3)])
+@pytest.mark.parametrize("interp", [False, True], ids=["midpoint", "interpolated"])
+def test_bucket_lut_variants_match_oracle(S, N, curve, v0, v1, edge, interp):
+    """The middle-peak curve and within-bucket interpolation: bit-exact against the oracle
+    (both evaluate the same binary64 expressions, rounded to float32)."""
+    ids, lut = gs.bucket_plan(S, N, curve=curve, v0=v0, v1=v1, edge=edge, interp=interp)
+    c = _oracle_curve(curve, v0, v1, edge)
+    if interp:
+        wids, wlut = OB.plan_interpolated(S, N, c)
+    else:
+        wids, wlut = OB.plan(S, N, OB.bucket_table(c, N))
+    assert ids.tolist() == wids.tolist()
+    assert np.array_equal(lut, wlut)
+
+
+def test_bucket_plan_rejects_bad_variants():
+    with pytest.raises(gs.GSError):
+        gs.bucket_plan(10, 4, curve="peak", v0=2.0, v1=1.0, edge=1.0)     # apex not inside (0, 1)
+    with pytest.raises(gs.GSError):
+        gs.bucket_plan(10, 4, curve="table", table=[1.0] * 4, interp=True)
