@@ -25,6 +25,10 @@ Readings taken where the pages are silent:
   region covers (zero summed weight) gets cond = 0.
 * A full-frame cond given together with regions joins the sum as one more
   region of strength 1 with no feather and no mask.
+* Timestep validity ("判断当前 timestep 是否有效" in the same passage): a region
+  may carry a progress range [t_start, t_end); it takes part for sample b only
+  when t_start <= i_b / S < t_end (binary64, S the schedule's step count, the
+  same progress the guidance buckets use).  t_end <= t_start means no range.
 * Inpaint blend in the denoised (x0) space: den = m * pred + (1 - m) * orig,
   m = 1 meaning "regenerate"; samples without a mask use m = 1.
 * Euler (Karras et al. 2022, Algorithm 1 without churn):
@@ -57,6 +61,16 @@ class Region:
     feather: int
     out: np.ndarray
     mask: Optional[np.ndarray] = None
+    t_start: float = 0.0
+    t_end: float = 0.0
+
+
+def region_active(r: Region, i: int, steps: int) -> bool:
+    """Whether region r takes part at step i of `steps`: no range, or t_start <= i/steps < t_end."""
+    if r.t_end <= r.t_start:
+        return True
+    p = float(i) / float(steps)
+    return r.t_start <= p < r.t_end
 
 
 def feather_factor(h: int, w: int, y0: int, x0: int, H: int, W: int, F: int) -> np.ndarray:
@@ -89,8 +103,11 @@ def region_weight(r: Region, B: int, H: int, W: int) -> np.ndarray:
 
 
 def positive_branch(B: int, C: int, H: int, W: int, cond=None,
-                    regions: Sequence[Region] = ()) -> np.ndarray:
-    """Full-frame cond, or the weight-normalised sum of the regional outputs."""
+                    regions: Sequence[Region] = (), active=None) -> np.ndarray:
+    """Full-frame cond, or the weight-normalised sum of the regional outputs.
+
+    active: None (every region takes part) or bool [B, len(regions)]: region r
+    contributes to sample b only where active[b, r]."""
     if cond is not None and not regions:
         return np.asarray(cond, dtype=np.float64)
     if not regions:
@@ -100,13 +117,15 @@ def positive_branch(B: int, C: int, H: int, W: int, cond=None,
     if cond is not None:
         acc += np.asarray(cond, dtype=np.float64)
         wsum += 1.0
-    for r in regions:
+    for k, r in enumerate(regions):
         if not (0 <= r.y0 and r.y0 + r.h <= H and 0 <= r.x0 and r.x0 + r.w <= W):
             raise ValueError("region outside the latent frame")
         wgt = region_weight(r, B, H, W)
         out = np.asarray(r.out, dtype=np.float64)[:, :, :, : r.w]
-        acc[:, :, r.y0:r.y0 + r.h, r.x0:r.x0 + r.w] += wgt * out
-        wsum[:, :, r.y0:r.y0 + r.h, r.x0:r.x0 + r.w] += wgt
+        on = (np.ones(B, dtype=bool) if active is None
+              else np.asarray(active, dtype=bool)[:, k]).reshape(B, 1, 1, 1)
+        acc[:, :, r.y0:r.y0 + r.h, r.x0:r.x0 + r.w] += np.where(on, wgt * out, 0.0)
+        wsum[:, :, r.y0:r.y0 + r.h, r.x0:r.x0 + r.w] += np.where(on, wgt, 0.0)
     pos = np.zeros_like(acc)
     covered = np.broadcast_to(wsum > 0.0, acc.shape)
     np.divide(acc, np.broadcast_to(wsum, acc.shape), out=pos, where=covered)
@@ -162,7 +181,10 @@ def guided_step(x, sigmas, step_idx, *, uncond=None, cond=None, cfg: float = 1.0
     if uncond is None:
         ok &= s == 1.0
 
-    pos = positive_branch(B, C, H, W, cond=cond, regions=regions)
+    steps = len(sig) - 1
+    active = np.array([[region_active(r, int(safe[b]), steps) for r in regions]
+                       for b in range(B)], dtype=bool).reshape(B, len(regions))
+    pos = positive_branch(B, C, H, W, cond=cond, regions=regions, active=active)
     pred = pos if uncond is None else combine(uncond, pos, s)
 
     den = pred

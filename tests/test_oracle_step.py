@@ -212,3 +212,32 @@ def test_region_outside_frame_rejected():
     r = O.Region(0, 5, 2, 4, 1.0, 0, np.zeros((1, 1, 2, 4)))
     with pytest.raises(ValueError):
         O.positive_branch(1, 1, 4, 8, regions=[r])
+
+
+def test_region_timestep_range_boundaries():
+    """[t_start, t_end) in progress i/S: start included, end excluded; no range = always."""
+    r = O.Region(0, 0, 1, 1, 1.0, 0, np.zeros((1, 1, 1, 1)), t_start=0.3, t_end=0.5)
+    assert [i for i in range(10) if O.region_active(r, i, 10)] == [3, 4]
+    always = O.Region(0, 0, 1, 1, 1.0, 0, np.zeros((1, 1, 1, 1)))
+    assert all(O.region_active(always, i, 7) for i in range(7))
+    reversed_range = O.Region(0, 0, 1, 1, 1.0, 0, np.zeros((1, 1, 1, 1)), t_start=0.6, t_end=0.2)
+    assert all(O.region_active(reversed_range, i, 7) for i in range(7))
+
+
+def test_region_timestep_range_is_per_sample():
+    """Two samples at different steps: the region counts for the one inside its range only,
+    so that sample equals the step with the region and the other the step without it."""
+    B, C, H, W = 2, 2, 6, 7
+    sig = np.array([5.0, 3.0, 2.0, 1.0, 0.5, 0.0])
+    x, u, c = rnd((B, C, H, W), 1), rnd((B, C, H, W), 2), rnd((B, C, H, W), 3)
+    out = rnd((B, C, 3, 4), 4)
+    ranged = O.Region(1, 2, 3, 4, 1.3, 2, out, t_start=0.0, t_end=0.4)   # steps 0, 1 of 5
+    plain = O.Region(1, 2, 3, 4, 1.3, 2, out)
+    idx = [1, 3]
+    got, _, ok = O.guided_step(x, sig, idx, uncond=u, cond=c, cfg=2.5, regions=[ranged])
+    with_r, _, _ = O.guided_step(x, sig, idx, uncond=u, cond=c, cfg=2.5, regions=[plain])
+    without, _, _ = O.guided_step(x, sig, idx, uncond=u, cond=c, cfg=2.5, regions=[])
+    assert ok.all()
+    assert np.array_equal(got[0], with_r[0])
+    assert np.array_equal(got[1], without[1])
+    assert not np.array_equal(with_r[1], without[1])
