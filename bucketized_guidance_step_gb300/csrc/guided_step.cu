@@ -43,19 +43,35 @@ using namespace gs_detail;
 
 constexpr int kThreads = 128;
 
+// The first step index i in [0, S] whose progress binary64(i / S) is >= t (S if
+// none): progress is non-decreasing in i, so a region with range [t0, t1) takes
+// part exactly at first_step_at(t0) <= i < first_step_at(t1).
+int first_step_at(double t, int S) {
+    int lo = 0, hi = S;
+    while (lo < hi) {
+        const int mid = lo + (hi - lo) / 2;
+        if (static_cast<double>(mid) / static_cast<double>(S) >= t)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
 // ---------------------------------------------------------------------------
 // Regional accumulation for one item: pos += w_r * out_r, wsum += w_r over the
 // regions that touch the item's pixels ([SAMPLING] calc_cond_batch).
 // ---------------------------------------------------------------------------
 template <typename T, int VEC, int CH>
 __device__ __forceinline__ void accumulate_regions(const StepParams& p, const DevRegion* regs,
-                                                   int b, int cc, long long p0,
+                                                   int b, int idx, int cc, long long p0,
                                                    float (&pos)[CH][VEC], float (&wsum)[VEC]) {
     const int y = static_cast<int>(p0 / p.W);
     const int x0 = static_cast<int>(p0 - static_cast<long long>(y) * p.W);
     for (int r = 0; r < p.n_regions; ++r) {
         const DevRegion& R = regs[r];
         if (y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w) continue;
+        if (idx < R.step_lo || idx >= R.step_hi) continue;      // outside its timestep range
         const int ty = y - R.y0;
         float wrow = R.strength;
         if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
@@ -207,7 +223,7 @@ __device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* 
         for (int k = 0; k < CH; ++k)
 #pragma unroll
             for (int j = 0; j < VEC; ++j) pos[k][j] = has_c ? widen<T, VEC>(cr[k], j) : 0.0f;
-        accumulate_regions<T, VEC, CH>(p, regs, b, cc, p0, pos, wsum);
+        accumulate_regions<T, VEC, CH>(p, regs, b, idx, cc, p0, pos, wsum);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             const float inv = recip_or_zero(wsum[j]);
@@ -246,7 +262,7 @@ __device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* 
 // ---------------------------------------------------------------------------
 template <typename T, int VEC, int CH>
 __device__ __forceinline__ void accumulate_regions_vec(const StepParams& p, const DevRegion* regs,
-                                                       int b, int cc,
+                                                       int b, int idx, int cc,
                                                        long long p0, f2 (&pos)[CH][VEC / 2],
                                                        float (&wsum)[VEC]) {
     constexpr int NP = VEC / 2;
@@ -268,7 +284,8 @@ __device__ __forceinline__ void accumulate_regions_vec(const StepParams& p, cons
                 for (int t = 0; t < kW; ++t) lo[i][k].w[t] = hi[i][k].w[t] = 0u;
             if (r >= p.n_regions) continue;
             const DevRegion& R = regs[r];
-            hit[i] = !(y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w);
+            hit[i] = !(y < R.y0 || y >= R.y0 + R.h || x0 + VEC <= R.x0 || x0 >= R.x0 + R.w) &&
+                     idx >= R.step_lo && idx < R.step_hi;
             if (!hit[i] || !R.vec_ok) continue;
             const int xs = x0 - R.x0;
             const int q0 = floor_div(xs, VEC);
@@ -413,7 +430,7 @@ __device__ __forceinline__ void step_item_vec(const StepParams& p, const DevRegi
         for (int k = 0; k < CH; ++k)
 #pragma unroll
             for (int q = 0; q < NP; ++q) pos[k][q] = has_c ? widen2<T, VEC>(cr[k], q) : splat2(0.0f);
-        accumulate_regions_vec<T, VEC, CH>(p, regs, b, cc, p0, pos, wsum);
+        accumulate_regions_vec<T, VEC, CH>(p, regs, b, idx, cc, p0, pos, wsum);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             const float i0 = recip_or_zero(wsum[2 * q]);
@@ -652,6 +669,15 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
         d.pitch = s.pitch;
         d.mask = s.mask;
         d.mask_bstride = s.mask_bstride;
+        // timestep range -> step-index range, with the binary64 predicate of gs.h
+        if (s.t_start != s.t_start || s.t_end != s.t_end) return GS_ERR_INVALID_ARG;   // NaN
+        if (s.t_end <= s.t_start) {
+            d.step_lo = 0;
+            d.step_hi = 0x7fffffff;
+        } else {
+            d.step_lo = first_step_at(s.t_start, a->n_sigmas - 1);
+            d.step_hi = first_step_at(s.t_end, a->n_sigmas - 1);
+        }
     }
 
     // 16-byte vectors need every latent-shaped base (and the mask rows) aligned.

@@ -27,6 +27,7 @@ struct DevRegion {
     int vec_ok;              // out is 16-byte aligned and pitch is a multiple of VEC
     int feather;             // F
     int pad_;
+    int step_lo, step_hi;    // the region takes part at step indices step_lo <= i < step_hi
     const void* out;         // [B][C][h][pitch]
     long long pitch;
     const float* mask;       // [.][h][w] or nullptr

@@ -48,7 +48,7 @@ struct TmaRegion {
     int edges;
     int feather;              // F (ramp width in pixels; 0 = none)
     int wbox;                 // box width in elements (w rounded up to whole 16-byte vectors)
-    int pad_;
+    int step_lo;              // the region takes part at step indices step_lo <= i < step_hi
     const float* mask;
     long long mask_bstride;
     unsigned smem_off;        // byte offset of the region's box inside the tile
@@ -56,10 +56,10 @@ struct TmaRegion {
     int col0;                 // frame column of column-table entry 0 (x0 rounded down to VEC)
     int ncol;                 // column-table length (multiple of VEC)
     unsigned tab_off;         // byte offset of the column table inside the tile
-    int pad2_;
+    int step_hi;
 };
 
-static_assert(sizeof(TmaRegion) % 8 == 0, "region descriptors keep 8-byte alignment in arrays");
+static_assert(sizeof(TmaRegion) == 80, "region descriptors: 80 bytes (shared memory per CTA is tight)");
 
 struct TmaParams {
     CUtensorMap tm_x, tm_u, tm_c, tm_o, tm_m;
@@ -83,6 +83,7 @@ struct TmaParams {
     unsigned off_x, off_u, off_c, off_o, off_m;
     unsigned rowtab_off;
     const unsigned* mask_rows;   // row summary of the inpaint mask, or null
+    int ranged;                  // some region has a timestep range (else all take part)
     int mask_words;              // words per mask in mask_rows: ceil(H / 32)
 };
 
@@ -439,9 +440,15 @@ __global__ void __launch_bounds__(kMaxThreads)
         // the barrier, so with three or more warps the others take this work.
         const int warp = tid >> 5, lane = tid & 31, nwarps = (nthreads + 31) >> 5;
         const int w0 = nwarps >= 3 ? 2 : 0;
+        // the sample's step index decides which regions' timestep ranges hold; a
+        // region outside its range is recorded as touching no row of the band
+        const int sidx = p.ranged && warp >= w0 && warp - w0 < p.n_regions
+                             ? (p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step)
+                             : 0;
         for (int r = warp - w0; r >= 0 && r < p.n_regions; r += nwarps - w0) {
             const TmaRegion R = p.reg[r];
-            const bool hits = band_hits(R, y_band, p.RB);
+            const bool hits =
+                band_hits(R, y_band, p.RB) && sidx >= R.step_lo && sidx < R.step_hi;
             if (lane == 0) {
                 regs[r] = R;
                 TileRegion t;
@@ -887,6 +894,8 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     p.mask_shared = inp && sp.imask_bstride == 0;
     p.test_wait_timeout = (flags & GS_LAUNCH_TEST_WAIT_TIMEOUT) ? 1 : 0;
     p.mask_rows = inp ? sp.mask_rows : nullptr;
+    for (int r = 0; r < sp.n_regions; ++r)
+        if (sp.reg[r].step_lo > 0 || sp.reg[r].step_hi < 0x7fffffff) p.ranged = 1;
     p.mask_words = (H + 31) / 32;
     p.n_regions = sp.n_regions;
 
@@ -920,6 +929,8 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
         d.wbox = (R.w + vec - 1) / vec * vec;
         d.mask = R.mask;
         d.mask_bstride = R.mask_bstride;
+        d.step_lo = R.step_lo;
+        d.step_hi = R.step_hi;
         d.tile_bytes = static_cast<unsigned>(cg) * rb * d.wbox * es;
         d.smem_off = off;
         off += round128(d.tile_bytes);

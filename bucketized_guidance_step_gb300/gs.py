@@ -75,7 +75,8 @@ class RegionDesc(ctypes.Structure):
     _fields_ = [("y0", ctypes.c_int32), ("x0", ctypes.c_int32), ("h", ctypes.c_int32),
                 ("w", ctypes.c_int32), ("strength", ctypes.c_float), ("feather", ctypes.c_int32),
                 ("mask", ctypes.c_void_p), ("mask_bstride", ctypes.c_int64),
-                ("out", ctypes.c_void_p), ("pitch", ctypes.c_int64)]
+                ("out", ctypes.c_void_p), ("pitch", ctypes.c_int64),
+                ("t_start", ctypes.c_double), ("t_end", ctypes.c_double)]
 
 
 class StepArgs(ctypes.Structure):
@@ -264,6 +265,8 @@ class Region:
     out: object                       # CUDA tensor [B, C, h, pitch], the latent dtype
     mask: object = None               # CUDA fp32 [h, w] or [B, h, w], or None
     pitch: Optional[int] = None       # defaults to out.shape[-1]
+    t_start: float = 0.0              # timestep range [t_start, t_end) in progress i/S;
+    t_end: float = 0.0                # t_end <= t_start: every step
 
 
 _DT = {}
@@ -323,7 +326,8 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
                 mstride = r.h * r.w
         reg_arr[i] = RegionDesc(int(r.y0), int(r.x0), int(r.h), int(r.w), float(r.strength),
                                 int(r.feather), _dptr(r.mask, "region mask", torch.float32),
-                                mstride, _dptr(r.out, "region out", dt), pitch)
+                                mstride, _dptr(r.out, "region out", dt), pitch,
+                                float(r.t_start), float(r.t_end))
     mstride = 0
     if inpaint_mask is not None:
         mstride = 0 if inpaint_mask.shape[0] == 1 else H * W

@@ -213,6 +213,12 @@ gs_status gs_mask_rows(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
  *            mask + b * mask_bstride (mask_bstride 0 = one mask for all samples).
  *   out:     device, storage dtype, [B][C][h][pitch], pitch >= w; columns
  *            w..pitch-1 are never read.
+ *   t_start, t_end: the region's timestep range ([SAMPLING] "calc_cond_batch()":
+ *            each entry first checks whether the current timestep is valid for it):
+ *            the region takes part for sample b only when t_start <= i/S < t_end,
+ *            i = the sample's step index, S = n_sigmas - 1, evaluated in binary64
+ *            (the progress the guidance buckets use).  t_end <= t_start (a zeroed
+ *            struct) means no range: every step.
  */
 typedef struct gs_region {
     int32_t     y0, x0, h, w;
@@ -222,6 +228,7 @@ typedef struct gs_region {
     int64_t     mask_bstride;
     const void* out;
     int64_t     pitch;
+    double      t_start, t_end;
 } gs_region;
 
 /* launch_flags */

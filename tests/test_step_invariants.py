@@ -255,3 +255,25 @@ def test_mask_rows_with_shared_mask(shape, kernel_choice):
                    original=o, mask_rows=rows)
     torch.cuda.synchronize()
     assert same_bits(a, b)
+
+
+@pytest.mark.parametrize("shape", [(4, 4, 16, 16), (32, 8, 64, 128)], ids=["small", "large"])
+def test_region_outside_its_timestep_range_drops_out(shape, kernel_choice):
+    """A region whose timestep range excludes every sample's step equals no region at all;
+    one whose range holds it equals a region without a range."""
+    B, C, H, W = shape
+    x, u, c = (rnd(shape, s, torch.bfloat16) for s in (50, 51, 52))
+    out = rnd((B, C, H // 2, W // 2), 53, torch.bfloat16)
+    sg = sig(9.0, 4.0, 2.0, 1.0, 0.0)                        # S = 4
+    idx = torch.tensor([0, 1] * (B // 2), dtype=torch.int32, device=DEV)   # progress 0, 0.25
+    base = dict(sigmas=sg, uncond=u, cond=c, cfg=3.0, step_idx=idx)
+    a, b, d, e = (torch.empty_like(x) for _ in range(4))
+    outside = gs.Region(2, 3, H // 2, W // 2, 1.2, 2, out, t_start=0.5, t_end=1.0)
+    inside = gs.Region(2, 3, H // 2, W // 2, 1.2, 2, out, t_start=0.0, t_end=0.5)
+    plain = gs.Region(2, 3, H // 2, W // 2, 1.2, 2, out)
+    gs.guided_step(x, x_out=a, regions=[outside], **base)
+    gs.guided_step(x, x_out=b, **base)
+    gs.guided_step(x, x_out=d, regions=[inside], **base)
+    gs.guided_step(x, x_out=e, regions=[plain], **base)
+    torch.cuda.synchronize()
+    assert same_bits(a, b) and same_bits(d, e) and not same_bits(b, e)

@@ -32,7 +32,7 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
              step: int = None, region_masks: bool = False, offset: int = 0,
              uncond_none: bool = False, want_den: bool = False, pitch_align: int = 8,
              tma: bool = True, expect_kernel: str = None, mask_rows: bool = False,
-             poison: bool = False):
+             poison: bool = False, region_ranges=None):
     """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok).
 
     mask_rows: pass the row summary of the latent mask (gs_mask_rows), so that bands
@@ -40,7 +40,8 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     side only, fill uncond, cond and the region slabs with NaN on every 32-row block
     of a blended sample whose mask is 0 there; the kernel must not read them (a read
     would carry NaN through 0 * pred into the output), and the oracle, which sees
-    the clean values, must agree.
+    the clean values, must agree.  region_ranges: (t_start, t_end) per region, given
+    to both sides.
     """
     inp = step_inputs(wl, step_seed, B=B, C=C, H=H, W=W, region_masks=region_masks,
                       pitch_align=pitch_align)
@@ -101,8 +102,10 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     xd = dev_latent(x)
     outd = dev_latent(torch.full_like(x, float("nan")))
     dend = dev_latent(torch.full_like(x, float("nan"))) if want_den else None
-    regs = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, _cuda(o),
-                      _cuda(r.mask)) for r, o in zip(inp.regions, reg_outs)]
+    ranges = region_ranges or [(0.0, 0.0)] * len(inp.regions)
+    regs = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, _cuda(o), _cuda(r.mask),
+                      t_start=t0, t_end=t1)
+            for r, o, (t0, t1) in zip(inp.regions, reg_outs, ranges)]
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     kw = dict(uncond=dev_latent(u_gpu), cond=dev_latent(c_gpu), regions=regs,
               sigmas=torch.from_numpy(sig).to(DEV), x_out=outd, denoised_out=dend,
@@ -132,8 +135,9 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
 
     # --- oracle ---
     oregs = [O.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, to64(r.out),
-                      None if r.mask is None else r.mask.numpy().astype(np.float64))
-             for r in inp.regions]
+                      None if r.mask is None else r.mask.numpy().astype(np.float64),
+                      t_start=t0, t_end=t1)
+             for r, (t0, t1) in zip(inp.regions, ranges)]
     present = (np.ones(Bn, bool) if inp.mask_present is None
                else inp.mask_present.numpy().astype(bool))
     ref, den, ok = O.guided_step(to64(x), sig, idx, uncond=to64(u), cond=to64(inp.cond), cfg=cfg,
@@ -283,3 +287,18 @@ def test_mask_rows_skip_reads_other_shapes(dtype):
     rep, got, _, _ = run_case(wl, region_masks=True, want_den=True, mask_rows=True,
                               poison=True, expect_kernel="tma")
     assert rep.n == wl.elements and np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
+@pytest.mark.parametrize("wl", [WORKLOADS[4], WORKLOADS[2]], ids=["sweep", "area"])
+def test_region_timestep_ranges(wl, tma):
+    """Regions with timestep ranges ([t_start, t_end) of progress i/S): on the staggered
+    sweep batch each region takes part for some samples only; on the area step (one
+    shared step index) a region whose range excludes the step drops out."""
+    if wl.n_regions == 3:
+        ranges = [(0.0, 0.3), (0.2, 0.8), (0.0, 0.0)]
+    else:
+        ranges = [(0.0, 0.5), (0.25, 1.0), (0.9, 1.0), (0.0, 0.0)]
+    rep, *_ = run_case(wl, tma=tma, region_ranges=ranges, step=7,
+                       expect_kernel="tma" if tma else "vector")
+    assert rep.n == wl.elements
