@@ -14,7 +14,9 @@ sigma_next = sig[i + 1] and guidance scale s_b:
    prediction is replaced by the original latent; the mask is broadcast over
    channels.
 4. Euler update between adjacent sigmas ([SAMPLING] "先分清四个概念": the sampler
-   is the update rule between neighbouring schedule points).
+   is the update rule between neighbouring schedule points), or its ancestral form
+   (the sampler object maps names such as Euler-ancestral onto k-diffusion
+   functions, [SAMPLING] "sampler_object"), which adds fresh noise.
 
 Readings taken where the pages are silent:
 
@@ -154,14 +156,57 @@ def euler(x, den, sigma, sigma_next) -> np.ndarray:
     return x + (sigma_next - sigma) * d
 
 
+def ancestral_sigmas(sigma, sigma_next):
+    """Euler-ancestral split of the step (Karras et al. 2022 / k-diffusion, eta = 1):
+    sigma_up = min(sigma_next, sqrt(sigma_next^2 (sigma^2 - sigma_next^2) / sigma^2)),
+    sigma_down = sqrt(sigma_next^2 - sigma_up^2); float64, per sample."""
+    sigma = np.asarray(sigma, dtype=np.float64)
+    sigma_next = np.asarray(sigma_next, dtype=np.float64)
+    up = np.minimum(sigma_next,
+                    np.sqrt(np.maximum(sigma_next ** 2 * (sigma ** 2 - sigma_next ** 2), 0.0)
+                            / sigma ** 2))
+    down = np.sqrt(np.maximum(sigma_next ** 2 - up ** 2, 0.0))
+    return up, down
+
+
+def euler_ancestral(x, den, sigma, sigma_next, noise) -> np.ndarray:
+    """Ancestral Euler step: deterministic Euler to sigma_down, then fresh noise of
+    standard deviation sigma_up: x + (sigma_down - sigma) (x - den) / sigma + sigma_up noise."""
+    x = np.asarray(x, dtype=np.float64)
+    up, down = ancestral_sigmas(sigma, sigma_next)
+    B = x.shape[0]
+    sigma = np.asarray(sigma, dtype=np.float64).reshape(B, 1, 1, 1)
+    d = (x - den) / sigma
+    return x + (down.reshape(B, 1, 1, 1) - sigma) * d + up.reshape(B, 1, 1, 1) * \
+        np.asarray(noise, dtype=np.float64)
+
+
+def model_input(x_next, original, orig_noise, sigma_next, inpaint_mask, mask_present=None):
+    """The next model call's input under the inpaint wrapper ([SAMPLING] "inpaint 与 mask":
+    every step the unmasked region is replaced by the original latent, and the noise is
+    kept to the masked region): m x_next + (1 - m) (original + sigma_next * orig_noise),
+    where orig_noise is the run's fixed noise; samples without a mask take x_next."""
+    x_next = np.asarray(x_next, dtype=np.float64)
+    B, C, H, W = x_next.shape
+    m = np.asarray(inpaint_mask, dtype=np.float64)
+    m = np.broadcast_to(m.reshape((m.shape[0], 1, H, W)), (B, 1, H, W))
+    sn = np.asarray(sigma_next, dtype=np.float64).reshape(B, 1, 1, 1)
+    noised = np.asarray(original, dtype=np.float64) + sn * np.asarray(orig_noise, np.float64)
+    out = m * x_next + (1.0 - m) * noised
+    present = (np.ones(B, dtype=bool) if mask_present is None
+               else np.asarray(mask_present).astype(bool).reshape(B))
+    return np.where(present.reshape(B, 1, 1, 1), out, x_next)
+
+
 def guided_step(x, sigmas, step_idx, *, uncond=None, cond=None, cfg: float = 1.0,
                 scale_lut=None, regions: Sequence[Region] = (), inpaint_mask=None,
-                mask_present=None, original=None):
+                mask_present=None, original=None, sampler: str = "euler", noise=None):
     """The whole step.  Returns (x_next, den, ok), float64 / float64 / bool[B].
 
     x, uncond, cond, original: [B, C, H, W].  sigmas: 1-D.  step_idx: [B] ints.
     scale_lut: per-step scale table (float32 values) or None for the scalar cfg.
     inpaint_mask: [B or 1, 1, H, W]; mask_present: [B] bools or None (= all).
+    sampler: "euler" or "euler_ancestral" (which needs noise, [B, C, H, W]).
     """
     x = np.asarray(x, dtype=np.float64)
     B, C, H, W = x.shape
@@ -198,7 +243,14 @@ def guided_step(x, sigmas, step_idx, *, uncond=None, cond=None, cfg: float = 1.0
         blended = inpaint_blend(pred, original, m)
         den = np.where(present.reshape(B, 1, 1, 1), blended, pred)
 
-    x_next = euler(x, den, np.where(ok, sigma, 1.0), sigma_next)
+    if sampler == "euler":
+        x_next = euler(x, den, np.where(ok, sigma, 1.0), sigma_next)
+    elif sampler == "euler_ancestral":
+        if noise is None:
+            raise ValueError("the ancestral sampler needs a noise tensor")
+        x_next = euler_ancestral(x, den, np.where(ok, sigma, 1.0), sigma_next, noise)
+    else:
+        raise ValueError(f"unknown sampler {sampler!r}")
     okb = ok.reshape(B, 1, 1, 1)
     x_next = np.where(okb, x_next, x)
     den = np.where(okb, den, np.nan)

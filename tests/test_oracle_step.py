@@ -241,3 +241,38 @@ def test_region_timestep_range_is_per_sample():
     assert np.array_equal(got[0], with_r[0])
     assert np.array_equal(got[1], without[1])
     assert not np.array_equal(with_r[1], without[1])
+
+
+def test_ancestral_split_hand_values_and_variance():
+    up, down = O.ancestral_sigmas([2.0], [1.0])
+    assert up[0] ** 2 == 0.75 and down[0] == 0.5          # sqrt(1 * (4 - 1) / 4), sqrt(1 - 0.75)
+    sig = np.array([14.6, 7.0, 3.0, 0.9, 0.03])
+    nxt = np.array([7.0, 3.0, 0.9, 0.03, 0.0])
+    up, down = O.ancestral_sigmas(sig, nxt)
+    np.testing.assert_allclose(up ** 2 + down ** 2, nxt ** 2, rtol=1e-13, atol=0)
+    assert np.all(up <= nxt) and up[-1] == 0.0 and down[-1] == 0.0
+
+
+def test_ancestral_step_closed_forms():
+    """A perfect denoiser (x = den + sigma e) moves to den + sigma_down e + sigma_up n; with
+    sigma_next = 0 the step lands on den exactly."""
+    B, C, H, W = 2, 3, 4, 5
+    den, e, n = rnd((B, C, H, W), 1), rnd((B, C, H, W), 2), rnd((B, C, H, W), 3)
+    sig = np.array([2.0, 0.5]); nxt = np.array([1.0, 0.2])
+    x = den + sig.reshape(B, 1, 1, 1) * e
+    up, down = O.ancestral_sigmas(sig, nxt)
+    got = O.euler_ancestral(x, den, sig, nxt, n)
+    want = den + down.reshape(B, 1, 1, 1) * e + up.reshape(B, 1, 1, 1) * n
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(O.euler_ancestral(x, den, sig, np.zeros(2), n), den.astype(np.float64))
+
+
+def test_model_input_blend_hand_values():
+    xn = np.full((1, 1, 1, 3), 2.0)
+    orig = np.full((1, 1, 1, 3), 1.0)
+    on = np.full((1, 1, 1, 3), -1.0)
+    m = np.array([[[[1.0, 0.0, 0.25]]]])
+    got = O.model_input(xn, orig, on, [0.5], m)
+    # m = 1: x_next; m = 0: orig + 0.5 * (-1) = 0.5; m = 1/4: 0.5 + 0.75 * 0.5 = 0.875
+    assert got.ravel().tolist() == [2.0, 0.5, 0.875]
+    assert np.array_equal(O.model_input(xn, orig, on, [0.5], m, mask_present=[False]), xn)
