@@ -245,7 +245,8 @@ def test_region_timestep_range_is_per_sample():
 
 def test_ancestral_split_hand_values_and_variance():
     up, down = O.ancestral_sigmas([2.0], [1.0])
-    assert up[0] ** 2 == 0.75 and down[0] == 0.5          # sqrt(1 * (4 - 1) / 4), sqrt(1 - 0.75)
+    # sqrt(1 * (4 - 1) / 4) and sqrt(1 - up^2), the latter within one rounding of 1/2
+    assert up[0] == np.sqrt(0.75) and abs(down[0] - 0.5) <= 2.0 ** -52
     sig = np.array([14.6, 7.0, 3.0, 0.9, 0.03])
     nxt = np.array([7.0, 3.0, 0.9, 0.03, 0.0])
     up, down = O.ancestral_sigmas(sig, nxt)
