@@ -95,6 +95,12 @@ def parse_args():
                     help="give the step the row summary of the inpaint mask (gs_mask_rows), so "
                          "bands whose mask is 0 on every row skip reading the prediction; "
                          "the roofline then counts only the bytes still required")
+    ap.add_argument("--sampler", choices=["euler", "euler_ancestral"], default="euler",
+                    help="the sampler of the step: the deterministic Euler update (default) or "
+                         "Euler-ancestral (eta 1, a fresh noise tensor read per step)")
+    ap.add_argument("--model-in", action="store_true",
+                    help="also write the next model input under the inpaint wrapper (inpaint "
+                         "workloads; reads the run's fixed noise for the blended samples)")
     ap.add_argument("--cpu-procs", type=int, default=1,
                     help="oracle processes timed at once for cpu_baseline / --impl reference")
     return ap.parse_args()
@@ -119,6 +125,14 @@ def workload_for(args):
             masked = max(1, masked * args.batch // wl.B)
         wl = dataclasses.replace(wl, B=args.batch, inpaint_samples=masked)
         name += f"@B{args.batch}"
+    if args.sampler != "euler":
+        wl = dataclasses.replace(wl, sampler=args.sampler)
+        name += f"@{args.sampler}"
+    if args.model_in:
+        if not wl.inpaint:
+            raise SystemExit("--model-in needs an inpaint workload")
+        wl = dataclasses.replace(wl, model_input=True)
+        name += "@model_in"
     return dataclasses.replace(wl, name=name)
 
 
@@ -256,6 +270,9 @@ def build_sets(wl, R, dev, sig_np, lut_np, seed=0, mask_rows=False):
     branch = arena((2 * wl.B,) + shape[1:]) if wl.full_frame_cond else arena(shape)
     slabs = [arena((wl.B, wl.C, r.h, r.pitch)) for r in proto.regions]
     masks = origs = None
+    fresh = arena(shape) if wl.sampler == "euler_ancestral" else None
+    fixed = arena(shape) if wl.model_input else None
+    model_in = torch.empty((R,) + shape, dtype=dt, device=dev) if wl.model_input else None
     nm = 0
     if wl.inpaint:
         nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
@@ -290,6 +307,11 @@ def build_sets(wl, R, dev, sig_np, lut_np, seed=0, mask_rows=False):
                 st["present"] = pres
         if idxs is not None:
             st["idx"] = idxs[k]
+        if fresh is not None:
+            st["noise"] = fresh[k]
+        if fixed is not None:
+            st["orig_noise"] = fixed[k]
+            st["model_in"] = model_in[k]
         sets.append(st)
     torch.cuda.synchronize(dev)
     return sets, sig, lut, steps
@@ -313,6 +335,10 @@ def step_kwargs(wl, st, sig, lut, pdl, tma=True):
         kw["cfg"] = wl.guidance.cfg
     if "mask" in st:
         kw.update(inpaint_mask=st["mask"], original=st["orig"], mask_present=st.get("present"))
+    if "noise" in st:
+        kw.update(sampler="euler_ancestral", noise=st["noise"])
+    if "model_in" in st:
+        kw.update(model_in_out=st["model_in"], orig_noise=st["orig_noise"])
     return kw
 
 
@@ -328,7 +354,8 @@ def algorithmic_bytes(wl, proto_regions) -> int:
     if wl.inpaint:
         nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
     return step_bytes(wl.B, wl.C, wl.H, wl.W, wl.dtype, uncond=True, cond=wl.full_frame_cond,
-                      regions=[(r.h, r.w) for r in proto_regions], inpaint_samples=nm)
+                      regions=[(r.h, r.w) for r in proto_regions], inpaint_samples=nm,
+                      noise=wl.sampler == "euler_ancestral", model_input=wl.model_input)
 
 
 def capture(launches, stream):
@@ -487,7 +514,8 @@ def run_e2e(args, wl, sets, sig, lut, stream, dev, pg):
 
     from bucketized_guidance_step_gb300 import gs
 
-    keys = [k for k in ("x", "stacked", "uncond", "orig", "idx") if k in sets[0]]
+    keys = [k for k in ("x", "stacked", "uncond", "orig", "idx", "noise", "orig_noise")
+            if k in sets[0]]
     host_in = []
     for j in range(2):
         h = {k: torch.empty_like(sets[j][k], device="cpu").pin_memory() for k in keys}
@@ -495,13 +523,15 @@ def run_e2e(args, wl, sets, sig, lut, stream, dev, pg):
             h[k].copy_(sets[j][k])
         hr = [r.out.to("cpu").pin_memory() for r in sets[j]["regions"]]
         host_in.append((h, hr))
-    out_h = [torch.empty_like(sets[0]["x"], device="cpu").pin_memory() for _ in range(2)]
+    out_keys = ["x"] + (["model_in"] if "model_in" in sets[0] else [])
+    out_h = [{k: torch.empty_like(sets[0][k], device="cpu").pin_memory() for k in out_keys}
+             for _ in range(2)]
     prepared = [gs.make_step_args(sets[j]["x"], **step_kwargs(wl, sets[j], sig, lut, False,
                                                               not args.no_tma))
                 for j in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in[0][0].values()) + \
         sum(t.numel() * t.element_size() for t in host_in[0][1])
-    d2h = out_h[0].numel() * out_h[0].element_size()
+    d2h = sum(t.numel() * t.element_size() for t in out_h[0].values())
 
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
@@ -529,7 +559,8 @@ def run_e2e(args, wl, sets, sig, lut, stream, dev, pg):
             ev_step[j].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_step[j])
-                out_h[j].copy_(st["x"], non_blocking=True)
+                for key in out_keys:
+                    out_h[j][key].copy_(st[key], non_blocking=True)
                 ev_out[j].record(s_out)
         # join
         stream.wait_stream(s_in)
@@ -580,6 +611,10 @@ def describe(wl) -> str:
         parts.append("inpaint mask+original" +
                      (f" on {wl.inpaint_samples} samples" if wl.inpaint_samples else ""))
     parts.append("per-sample step index" if wl.staggered else "shared step")
+    if wl.sampler != "euler":
+        parts.append(f"sampler {wl.sampler} (fresh noise read per step)")
+    if wl.model_input:
+        parts.append("next model input written (fixed noise read for the blended samples)")
     return ", ".join(parts)
 
 
@@ -623,20 +658,38 @@ def oracle_sample(wl, n_samples: int, seed: int = 0):
               cfg=g.cfg if g.cfg is not None else 1.0, regions=regs, inpaint_mask=lat,
               mask_present=None if inp.mask_present is None else inp.mask_present.numpy(),
               original=f64(inp.original))
+    if wl.sampler != "euler":
+        kw.update(sampler=wl.sampler, noise=f64(inp.fresh_noise))
+    if wl.model_input:
+        kw["model_input"] = f64(inp.orig_noise)
     return x, sig, idx, kw
+
+
+def oracle_call(x, sig, idx, kw):
+    """One oracle step on an oracle_sample, with the next model input where asked."""
+    import numpy as np
+
+    from oracle import step as O
+    kw = dict(kw)
+    orig_noise = kw.pop("model_input", None)
+    x_next, den, ok = O.guided_step(x, sig, idx, **kw)
+    if orig_noise is not None:
+        sn = np.asarray(sig, dtype=np.float64)[np.minimum(np.asarray(idx) + 1, len(sig) - 1)]
+        O.model_input(x_next, kw["original"], orig_noise, sn, kw["inpaint_mask"],
+                      kw["mask_present"])
+    return x_next
 
 
 def _oracle_timing(job):
     """Worker: time the oracle on one sample of the workload (seed = worker index) for
     `seconds` of wall time or exactly `steps` steps; returns (steps, elements, seconds)."""
     wl, seed, seconds, steps, warm = job
-    from oracle import step as O
     x, sig, idx, kw = oracle_sample(wl, 1, seed=seed)
     for _ in range(warm):
-        O.guided_step(x, sig, idx, **kw)
+        oracle_call(x, sig, idx, kw)
     reps, t0 = 0, time.perf_counter()
     while True:
-        O.guided_step(x, sig, idx, **kw)
+        oracle_call(x, sig, idx, kw)
         reps += 1
         dt = time.perf_counter() - t0
         if (steps is None and dt >= seconds) or (steps is not None and reps >= steps):

@@ -6,6 +6,9 @@ Every latent-shaped input is read once and every output written once:
           + |T| B C sum_r h_r w_r                  (regional outputs)
           + |T| Bm C P + 4 Bm P                    (original latent and fp32 mask of the
                                                      Bm samples that carry a mask)
+          + |T| B C P [ancestral]                  (the step's fresh noise)
+          + |T| B C P + |T| Bm C P [model input]   (the next model input written, the
+                                                     run's fixed noise of the Bm samples read)
 
 with P = H W; the 2 is the read of x and the write of x_out.  Sigmas, the scale
 table and the step indices (under 1 KiB) are left out.
@@ -20,7 +23,8 @@ ESIZE = {"fp32": 4, "bf16": 2, "fp16": 2}
 
 def step_bytes(B: int, C: int, H: int, W: int, dtype: str, *, uncond: bool = True,
                cond: bool = True, regions: Iterable[Tuple[int, int]] = (),
-               inpaint_samples: int = 0, denoised_out: bool = False) -> int:
+               inpaint_samples: int = 0, denoised_out: bool = False, noise: bool = False,
+               model_input: bool = False) -> int:
     e = ESIZE[dtype]
     P = H * W
     full = B * C * P * e
@@ -30,6 +34,8 @@ def step_bytes(B: int, C: int, H: int, W: int, dtype: str, *, uncond: bool = Tru
     total += full if denoised_out else 0
     total += sum(B * C * h * w * e for h, w in regions)
     total += inpaint_samples * C * P * e + inpaint_samples * P * 4
+    total += full if noise else 0
+    total += full + inpaint_samples * C * P * e if model_input else 0
     return total
 
 

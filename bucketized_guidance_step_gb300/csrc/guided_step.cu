@@ -58,6 +58,26 @@ int first_step_at(double t, int S) {
     return lo;
 }
 
+// Euler-ancestral split of a step (eta = 1), fp32: sigma_up and sigma_down / sigma,
+// for 0 <= sigma_next (the caller flags a negative one).  With r = sigma_next / sigma
+// the definitions reduce to sigma_up = r sqrt((sigma - sigma_next)(sigma + sigma_next))
+// and sigma_down / sigma = r^2 (sigma_down^2 = sigma_next^2 - sigma_up^2 =
+// sigma_next^4 / sigma^2).  This form has no cancellation when the two sigmas are
+// close and no overflow of the squares; each result is within a few roundings of the
+// exact split.  sigma_next > sigma has no split (the variance under the root would be
+// negative): the clamped definitions give sigma_up = 0, i.e. the deterministic step.
+__device__ __forceinline__ void ancestral_split(float sigma, float sigma_next, float& up,
+                                                float& rdown) {
+    const float r = __fdiv_rn(sigma_next, sigma);
+    if (sigma_next <= sigma) {
+        up = r * (__fsqrt_rn(sigma - sigma_next) * __fsqrt_rn(sigma + sigma_next));
+        rdown = r * r;
+    } else {
+        up = 0.0f;
+        rdown = r;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Regional accumulation for one item: pos += w_r * out_r, wsum += w_r over the
 // regions that touch the item's pixels ([SAMPLING] calc_cond_batch).
@@ -142,9 +162,11 @@ __device__ __forceinline__ void accumulate_regions(const StepParams& p, const De
 // One work item: sample b, channels c0 .. c0+CH-1, pixels p0 .. p0+VEC-1 (one row).
 // REG: regional conditioning present.  INP: an inpaint mask is given.
 // ---------------------------------------------------------------------------
-template <typename T, int VEC, int CH, bool REG, bool INP>
+template <typename T, int VEC, int CH, bool REG, bool INP, bool NZ>
 __device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* regs,
                                           long long item) {
+    const bool anc = NZ && p.sampler == GS_SAMPLER_EULER_ANCESTRAL;
+    const bool want_mi = NZ && p.model_in != nullptr;
     const long long g = item % p.groups;
     const long long rest = item / p.groups;
     const int cc = static_cast<int>(rest % p.chunks);
@@ -190,6 +212,17 @@ __device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* 
             }
         }
     }
+    Raw<T, VEC> nr[CH], onr[CH];
+    if constexpr (NZ) {
+        if (anc) {
+#pragma unroll
+            for (int k = 0; k < CH; ++k) nr[k] = load_raw<T, VEC>(p.noise, off0 + k * p.P);
+        }
+        if (want_mi && inpaint) {
+#pragma unroll
+            for (int k = 0; k < CH; ++k) onr[k] = load_raw<T, VEC>(p.orig_noise, off0 + k * p.P);
+        }
+    }
 
     // 2. Per-sample step parameters.
     const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
@@ -198,7 +231,9 @@ __device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* 
     const float s = p.lut != nullptr ? __ldg(p.lut + si) : p.cfg;
     const float sigma = __ldg(p.sig + si);
     const float sigma_next = __ldg(p.sig + si + 1);
-    const bool sigma_ok = sigma > 0.0f && sigma <= 3.402823466e38f;
+    // (the ancestral split takes sigma_next as a standard deviation: >= 0)
+    const bool sigma_ok =
+        sigma > 0.0f && sigma <= 3.402823466e38f && (!anc || sigma_next >= 0.0f);
     const bool uncond_ok = has_u || s == 1.0f;
     if (!(in_range && sigma_ok && uncond_ok)) {
         if (p.status != nullptr && g == 0 && cc == 0) {
@@ -238,9 +273,11 @@ __device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* 
     }
 
     // 4. Combine, inpaint blend, Euler update, round and store.
+    float up = 0.0f, r = ratio;
+    if (anc) ancestral_split(sigma, sigma_next, up, r);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        float xo[VEC], dn[VEC];
+        float xo[VEC], dn[VEC], mi[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             float pred = pos[k][j];
@@ -248,11 +285,21 @@ __device__ __forceinline__ void step_item(const StepParams& p, const DevRegion* 
             float den = pred;
             if (INP && inpaint) den = fmaf(m[j], pred, (1.0f - m[j]) * widen<T, VEC>(orr[k], j));
             const float xv = widen<T, VEC>(xr[k], j);
-            xo[j] = fmaf(ratio, xv - den, den);
+            xo[j] = fmaf(r, xv - den, den);
+            if (NZ && anc) xo[j] = fmaf(up, widen<T, VEC>(nr[k], j), xo[j]);
             dn[j] = den;
+            if (NZ && want_mi) {
+                mi[j] = xo[j];
+                if (INP && inpaint) {
+                    const float noised = fmaf(sigma_next, widen<T, VEC>(onr[k], j),
+                                              widen<T, VEC>(orr[k], j));
+                    mi[j] = fmaf(m[j], xo[j], (1.0f - m[j]) * noised);
+                }
+            }
         }
         store_vec<T, VEC>(p.x_out, off0 + k * p.P, xo);
         if (p.den_out != nullptr) store_vec<T, VEC>(p.den_out, off0 + k * p.P, dn);
+        if (NZ && want_mi) store_vec<T, VEC>(p.model_in, off0 + k * p.P, mi);
     }
 }
 
@@ -364,10 +411,12 @@ __device__ __forceinline__ void accumulate_regions_vec(const StepParams& p, cons
     }
 }
 
-template <typename T, int VEC, int CH, bool REG, bool INP>
+template <typename T, int VEC, int CH, bool REG, bool INP, bool NZ>
 __device__ __forceinline__ void step_item_vec(const StepParams& p, const DevRegion* regs,
                                               long long item) {
     constexpr int NP = VEC / 2;
+    const bool anc = NZ && p.sampler == GS_SAMPLER_EULER_ANCESTRAL;
+    const bool want_mi = NZ && p.model_in != nullptr;
     const long long g = item % p.groups;
     const long long rest = item / p.groups;
     const int cc = static_cast<int>(rest % p.chunks);
@@ -408,6 +457,17 @@ __device__ __forceinline__ void step_item_vec(const StepParams& p, const DevRegi
             }
         }
     }
+    Raw<T, VEC> nr[CH], onr[CH];
+    if constexpr (NZ) {
+        if (anc) {
+#pragma unroll
+            for (int k = 0; k < CH; ++k) nr[k] = load_raw<T, VEC>(p.noise, off0 + k * p.P);
+        }
+        if (want_mi && inpaint) {
+#pragma unroll
+            for (int k = 0; k < CH; ++k) onr[k] = load_raw<T, VEC>(p.orig_noise, off0 + k * p.P);
+        }
+    }
 
     // 2. Per-sample step parameters.
     const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
@@ -416,7 +476,9 @@ __device__ __forceinline__ void step_item_vec(const StepParams& p, const DevRegi
     const float s = p.lut != nullptr ? __ldg(p.lut + si) : p.cfg;
     const float sigma = __ldg(p.sig + si);
     const float sigma_next = __ldg(p.sig + si + 1);
-    const bool sigma_ok = sigma > 0.0f && sigma <= 3.402823466e38f;
+    // (the ancestral split takes sigma_next as a standard deviation: >= 0)
+    const bool sigma_ok =
+        sigma > 0.0f && sigma <= 3.402823466e38f && (!anc || sigma_next >= 0.0f);
     const bool uncond_ok = has_u || s == 1.0f;
 
     // 3. Positive branch (regional loads are issued here, before the check below
@@ -458,7 +520,11 @@ __device__ __forceinline__ void step_item_vec(const StepParams& p, const DevRegi
     }
     const f2 s2 = splat2(s);
     const f2 oms2 = splat2(1.0f - s);
-    const f2 r2 = splat2(__fdiv_rn(sigma_next, sigma));
+    float up = 0.0f, r = __fdiv_rn(sigma_next, sigma);
+    if (anc) ancestral_split(sigma, sigma_next, up, r);
+    const f2 r2 = splat2(r);
+    const f2 up2 = splat2(up);
+    const f2 sn2 = splat2(sigma_next);
     f2 m2[NP], omm2[NP];
     if (INP && inpaint) {
 #pragma unroll
@@ -471,23 +537,33 @@ __device__ __forceinline__ void step_item_vec(const StepParams& p, const DevRegi
     // 4. Combine, inpaint blend, Euler update, round and store.
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        Raw<T, VEC> xo, dn;
+        Raw<T, VEC> xo, dn, mi;
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             f2 pred = pos[k][q];
             if (has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(ur[k], q)));
             f2 den = pred;
             if (INP && inpaint) den = fma2(m2[q], pred, mul2(omm2[q], widen2<T, VEC>(orr[k], q)));
-            const f2 xn = fma2(r2, sub2(widen2<T, VEC>(xr[k], q), den), den);
+            f2 xn = fma2(r2, sub2(widen2<T, VEC>(xr[k], q), den), den);
+            if (NZ && anc) xn = fma2(up2, widen2<T, VEC>(nr[k], q), xn);
             narrow2<T, VEC>(xo, q, xn);
             if (p.den_out != nullptr) narrow2<T, VEC>(dn, q, den);
+            if (NZ && want_mi) {
+                f2 v = xn;
+                if (INP && inpaint) {
+                    const f2 noised = fma2(sn2, widen2<T, VEC>(onr[k], q), widen2<T, VEC>(orr[k], q));
+                    v = fma2(m2[q], xn, mul2(omm2[q], noised));
+                }
+                narrow2<T, VEC>(mi, q, v);
+            }
         }
         store_raw<T, VEC>(p.x_out, off0 + k * p.P, xo);
         if (p.den_out != nullptr) store_raw<T, VEC>(p.den_out, off0 + k * p.P, dn);
+        if (NZ && want_mi) store_raw<T, VEC>(p.model_in, off0 + k * p.P, mi);
     }
 }
 
-template <typename T, int VEC, int CH, bool REG, bool INP>
+template <typename T, int VEC, int CH, bool REG, bool INP, bool NZ>
 __global__ void __launch_bounds__(kThreads) guided_step_kernel(const __grid_constant__ StepParams p) {
     // The region table lives in kernel parameters; a loop over it with a
     // runtime index would take one constant-cache miss per region, serially.
@@ -505,15 +581,15 @@ __global__ void __launch_bounds__(kThreads) guided_step_kernel(const __grid_cons
     const long long it = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
     if (it >= p.n_items) return;
     if constexpr (VEC >= 2)
-        step_item_vec<T, VEC, CH, REG, INP>(p, regs, it);
+        step_item_vec<T, VEC, CH, REG, INP, NZ>(p, regs, it);
     else
-        step_item<T, VEC, CH, REG, INP>(p, regs, it);
+        step_item<T, VEC, CH, REG, INP, NZ>(p, regs, it);
 }
 
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-template <typename T, int VEC, int CH, bool REG, bool INP>
+template <typename T, int VEC, int CH, bool REG, bool INP, bool NZ>
 gs_status launch(StepParams& p, gs_stream stream, unsigned int flags) {
     p.groups = p.P / VEC;
     p.chunks = p.C / CH;
@@ -536,7 +612,7 @@ gs_status launch(StepParams& p, gs_stream stream, unsigned int flags) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, guided_step_kernel<T, VEC, CH, REG, INP>, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, guided_step_kernel<T, VEC, CH, REG, INP, NZ>, p);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return GS_ERR_CUDA;
@@ -557,28 +633,37 @@ int channel_override() {
     return v;
 }
 
-template <typename T, int VEC, bool REG, bool INP>
+template <typename T, int VEC, bool REG, bool INP, bool NZ>
 gs_status launch_ch(StepParams& p, gs_stream stream, unsigned int flags) {
     if constexpr (VEC == 1) {
-        return launch<T, 1, 1, REG, INP>(p, stream, flags);
+        return launch<T, 1, 1, REG, INP, NZ>(p, stream, flags);
     } else {
         int ch = p.C % 2 == 0 ? 2 : 1;
         const int o = channel_override();
         if (o != 0 && p.C % o == 0) ch = o;
-        if (ch == 4) return launch<T, VEC, 4, REG, INP>(p, stream, flags);
-        if (ch == 2) return launch<T, VEC, 2, REG, INP>(p, stream, flags);
-        return launch<T, VEC, 1, REG, INP>(p, stream, flags);
+        if (ch == 4) return launch<T, VEC, 4, REG, INP, NZ>(p, stream, flags);
+        if (ch == 2) return launch<T, VEC, 2, REG, INP, NZ>(p, stream, flags);
+        return launch<T, VEC, 1, REG, INP, NZ>(p, stream, flags);
     }
 }
 
-template <typename T, int VEC>
-gs_status launch_features(StepParams& p, gs_stream stream, unsigned int flags) {
+template <typename T, int VEC, bool NZ>
+gs_status launch_features_nz(StepParams& p, gs_stream stream, unsigned int flags) {
     const bool reg = p.n_regions > 0;
     const bool inp = p.imask != nullptr;
-    if (reg && inp) return launch_ch<T, VEC, true, true>(p, stream, flags);
-    if (reg) return launch_ch<T, VEC, true, false>(p, stream, flags);
-    if (inp) return launch_ch<T, VEC, false, true>(p, stream, flags);
-    return launch_ch<T, VEC, false, false>(p, stream, flags);
+    if (reg && inp) return launch_ch<T, VEC, true, true, NZ>(p, stream, flags);
+    if (reg) return launch_ch<T, VEC, true, false, NZ>(p, stream, flags);
+    if (inp) return launch_ch<T, VEC, false, true, NZ>(p, stream, flags);
+    return launch_ch<T, VEC, false, false, NZ>(p, stream, flags);
+}
+
+// The sampler options and the model-input output are compiled in only where
+// they are asked for, so the plain Euler step carries none of their code.
+template <typename T, int VEC>
+gs_status launch_features(StepParams& p, gs_stream stream, unsigned int flags) {
+    if (p.sampler != GS_SAMPLER_EULER || p.model_in != nullptr)
+        return launch_features_nz<T, VEC, true>(p, stream, flags);
+    return launch_features_nz<T, VEC, false>(p, stream, flags);
 }
 
 template <typename T>
@@ -615,6 +700,11 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
         (a->inpaint_mask == nullptr || (reinterpret_cast<uintptr_t>(a->mask_rows) & 3u) != 0))
         return GS_ERR_INVALID_ARG;
     if (static_cast<long long>(a->B) * a->C * a->H * a->W > (1ll << 46)) return GS_ERR_UNSUPPORTED;
+    if (a->sampler != GS_SAMPLER_EULER && a->sampler != GS_SAMPLER_EULER_ANCESTRAL)
+        return GS_ERR_INVALID_ARG;
+    if (a->sampler == GS_SAMPLER_EULER_ANCESTRAL && a->noise == nullptr) return GS_ERR_INVALID_ARG;
+    if (a->model_in_out != nullptr && (a->inpaint_mask == nullptr || a->orig_noise == nullptr))
+        return GS_ERR_INVALID_ARG;
 
     StepParams p = {};
     p.B = a->B;
@@ -639,6 +729,10 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
     p.present = a->mask_present;
     p.orig = a->inpaint_mask != nullptr ? a->original : nullptr;
     p.mask_rows = a->mask_rows;        // used by the TMA-fed kernel only
+    p.sampler = a->sampler;
+    p.noise = a->sampler == GS_SAMPLER_EULER_ANCESTRAL ? a->noise : nullptr;
+    p.model_in = a->model_in_out;
+    p.orig_noise = a->model_in_out != nullptr ? a->orig_noise : nullptr;
     p.status = a->dev_status;
     p.n_regions = a->n_regions;
     const long long esize = a->dtype == GS_DTYPE_F32 ? 4 : 2;
@@ -687,6 +781,8 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
     if (a->cond != nullptr) vec = vec && aligned16(a->cond);
     if (a->inpaint_mask != nullptr)
         vec = vec && aligned16(a->original) && aligned16(a->inpaint_mask) && a->mask_bstride % 4 == 0;
+    if (p.noise != nullptr) vec = vec && aligned16(p.noise);
+    if (p.model_in != nullptr) vec = vec && aligned16(p.model_in) && aligned16(p.orig_noise);
 
     bool used_tma = false;
     const gs_status st =

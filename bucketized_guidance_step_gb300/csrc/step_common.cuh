@@ -56,6 +56,10 @@ struct StepParams {
     const unsigned char* present;
     const void* orig;
     const unsigned* mask_rows;   // row summary of imask (gs_mask_rows) or null
+    int sampler;                 // GS_SAMPLER_*
+    const void* noise;           // ancestral noise or null
+    void* model_in;              // second output (next model input) or null
+    const void* orig_noise;      // the run's fixed noise (with model_in)
     unsigned int* status;
     int n_sig;
     int step;

@@ -810,6 +810,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
                           bool* used, bool dry_run) {
     *used = false;
     if (flags & GS_LAUNCH_NO_TMA) return GS_OK;
+    if (sp.sampler != GS_SAMPLER_EULER || sp.model_in != nullptr) return GS_OK;
     if (encoder() == nullptr) return GS_OK;
     const unsigned es = dtype == GS_DTYPE_F32 ? 4u : 2u;
     const int vec = static_cast<int>(16u / es);

@@ -36,12 +36,13 @@ GS_MAX_REGIONS = 16
 GS_LAUNCH_PDL = 1
 GS_LAUNCH_NO_TMA = 2
 GS_LAUNCH_TEST_WAIT_TIMEOUT = 4
-GS_ABI_VERSION = 2
+GS_ABI_VERSION = 3
 
 EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_guided_step",
            "gs_step_kernel_kind", "gs_status_from_word", "gs_status_string", "gs_abi_version")
 GS_KERNEL_SCALAR, GS_KERNEL_VECTOR, GS_KERNEL_TMA = 0, 1, 2
 KERNEL_NAMES = {0: "scalar", 1: "vector", 2: "tma"}
+SAMPLERS = {"euler": 0, "euler_ancestral": 1}
 
 
 class GSLibraryError(RuntimeError):
@@ -93,7 +94,9 @@ class StepArgs(ctypes.Structure):
                 ("inpaint_mask", ctypes.c_void_p), ("mask_bstride", ctypes.c_int64),
                 ("mask_present", ctypes.c_void_p), ("original", ctypes.c_void_p),
                 ("dev_status", ctypes.c_void_p), ("launch_flags", ctypes.c_uint32),
-                ("mask_rows", ctypes.c_void_p)]
+                ("mask_rows", ctypes.c_void_p),
+                ("sampler", ctypes.c_int32), ("noise", ctypes.c_void_p),
+                ("model_in_out", ctypes.c_void_p), ("orig_noise", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -286,6 +289,7 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
                    step: int = 0, scale_lut=None, cfg: float = 1.0,
                    regions: Sequence[Region] = (), inpaint_mask=None, mask_present=None,
                    original=None, mask_rows=None, x_out=None, denoised_out=None, status=None,
+                   sampler: str = "euler", noise=None, model_in_out=None, orig_noise=None,
                    pdl: bool = False, tma: bool = True, test_wait_timeout: bool = False):
     """Build a gs_step_args (and the region array it points to) from tensors."""
     torch = _torch()
@@ -299,7 +303,8 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
     dt = x.dtype
     shape = tuple(x.shape)
     for name, t in (("x_out", x_out), ("denoised_out", denoised_out), ("uncond", uncond),
-                    ("cond", cond), ("original", original)):
+                    ("cond", cond), ("original", original), ("noise", noise),
+                    ("model_in_out", model_in_out), ("orig_noise", orig_noise)):
         if t is not None and tuple(t.shape) != shape:
             raise ValueError(f"{name} must have the shape of x {shape}, got {tuple(t.shape)}")
     if inpaint_mask is not None and (inpaint_mask.dim() != 4 or inpaint_mask.shape[0] not in (1, B)
@@ -359,6 +364,16 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
         if tuple(mask_rows.shape) != (inpaint_mask.shape[0], (H + 31) // 32):
             raise ValueError("mask_rows must be [masks, ceil(H/32)] (from mask_rows())")
     a.mask_rows = _dptr(mask_rows, "mask_rows", torch.int32)
+    if sampler not in SAMPLERS:
+        raise ValueError(f"sampler must be one of {tuple(SAMPLERS)}")
+    if sampler == "euler_ancestral" and noise is None:
+        raise ValueError("the ancestral sampler needs noise")
+    if model_in_out is not None and (inpaint_mask is None or orig_noise is None):
+        raise ValueError("model_in_out needs inpaint_mask, original and orig_noise")
+    a.sampler = SAMPLERS[sampler]
+    a.noise = _dptr(noise, "noise", dt)
+    a.model_in_out = _dptr(model_in_out, "model_in_out", dt)
+    a.orig_noise = _dptr(orig_noise, "orig_noise", dt)
     a.launch_flags = ((GS_LAUNCH_PDL if pdl else 0) | (0 if tma else GS_LAUNCH_NO_TMA) |
                       (GS_LAUNCH_TEST_WAIT_TIMEOUT if test_wait_timeout else 0))
     return a, reg_arr
@@ -384,7 +399,9 @@ def guided_step(x, *, sigmas, stream=None, **kw):
     ([B or 1, 1, H, W] fp32), mask_present (uint8 [B]), original, x_out,
     denoised_out, status (int32 [1], device flags OR-ed in), mask_rows (the row
     summary of inpaint_mask from ``mask_rows()``: bands whose mask is 0 on every row
-    then skip reading the prediction), pdl, tma (False forces the register-streaming
+    then skip reading the prediction), sampler ("euler" or "euler_ancestral"), noise
+    (the ancestral step's fresh noise), model_in_out and orig_noise (the next model
+    input under the inpaint wrapper), pdl, tma (False forces the register-streaming
     kernel).
     """
     args, _keep = make_step_args(x, sigmas=sigmas, **kw)

@@ -84,6 +84,8 @@ class Workload:
     mask_rects: Tuple[int, int] = (1, 3)
     staggered: bool = True                   # per-sample step index (else one shared step)
     seed: int = 0
+    sampler: str = "euler"                   # "euler" | "euler_ancestral" (fresh noise per step)
+    model_input: bool = False                # also the next model input (inpaint wrapper)
 
     @property
     def elements(self) -> int:
@@ -156,6 +158,8 @@ class StepInputs:
     mask_present: Optional[torch.Tensor] = None   # [B] uint8, or None = all samples
     original: Optional[torch.Tensor] = None       # [B, C, H, W]
     step_idx: Optional[torch.Tensor] = None       # [B] int32, or None = shared step
+    fresh_noise: Optional[torch.Tensor] = None    # [B, C, H, W] N(0,1): the ancestral step's
+    orig_noise: Optional[torch.Tensor] = None     # [B, C, H, W] N(0,1): the run's fixed noise
 
 
 def draw_region(B: int, C: int, H: int, W: int, wl: Workload, seed: int, dtype,
@@ -226,4 +230,11 @@ def step_inputs(wl: Workload, step_seed: int = 0, *, B: Optional[int] = None,
         g = _gen(base + 5)
         idx = torch.randint(0, wl.schedule.steps, (B,), generator=g, dtype=torch.int64)
         idx = idx.to(torch.int32)
-    return StepInputs(noise, stacked, uncond, cond, regions, pm, present, orig, idx)
+    fresh = normal((B, C, H, W), base + 6, dt) if wl.sampler == "euler_ancestral" else None
+    orig_noise = None
+    if wl.model_input:
+        if not wl.inpaint:
+            raise ValueError("the model input output needs an inpaint workload")
+        orig_noise = normal((B, C, H, W), base + 7, dt)
+    return StepInputs(noise, stacked, uncond, cond, regions, pm, present, orig, idx, fresh,
+                      orig_noise)

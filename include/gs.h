@@ -231,6 +231,9 @@ typedef struct gs_region {
     double      t_start, t_end;
 } gs_region;
 
+/* samplers (gs_step_args.sampler) */
+enum { GS_SAMPLER_EULER = 0, GS_SAMPLER_EULER_ANCESTRAL = 1 };
+
 /* launch_flags */
 #define GS_LAUNCH_PDL    1u  /* launch with programmatic dependent launch: the kernel
                                 may be scheduled before the previous kernel in the
@@ -297,6 +300,26 @@ typedef struct gs_step_args {
        0, so a non-finite prediction there does not propagate).  The caller keeps
        it in step with inpaint_mask. */
     const uint32_t* mask_rows;
+
+    /* Sampler ([SAMPLING] "sampler_object": names map onto k-diffusion functions).
+       GS_SAMPLER_EULER (0, default): x' = den + (sigma_next/sigma) (x - den).
+       GS_SAMPLER_EULER_ANCESTRAL (1, eta = 1): x' = den + (sigma_down/sigma) (x - den)
+       + sigma_up * noise, sigma_up = min(sigma_next, sqrt(sigma_next^2 (sigma^2 -
+       sigma_next^2) / sigma^2)), sigma_down = sqrt(sigma_next^2 - sigma_up^2), per sample
+       in fp32.  Needs `noise`.  A sample whose sigma_next is negative (or NaN) has no
+       split: it is flagged GS_DEV_SIGMA and left unwritten, like sigma <= 0.
+       Any other value of `sampler` is GS_ERR_INVALID_ARG. */
+    int32_t     sampler;
+    const void* noise;          /* device [B][C][H][W], storage dtype: this step's fresh
+                                   noise (the random numbers are an input)              */
+    /* Optional second output under the inpaint wrapper ([SAMPLING] "inpaint 与 mask":
+       each step the unmasked region is replaced by the original, the noise kept to the
+       mask): the next model call's input m * x' + (1 - m) * (original + sigma_next *
+       orig_noise), x' for samples without a mask.  Needs inpaint_mask, original and
+       orig_noise.  The sampler options and this output run on the register-streaming
+       kernel. */
+    void*       model_in_out;   /* device [B][C][H][W] or NULL                           */
+    const void* orig_noise;     /* device [B][C][H][W]: the run's fixed noise            */
 } gs_step_args;
 
 /*
@@ -369,7 +392,7 @@ gs_status gs_status_from_word(uint32_t word);
 const char* gs_status_string(gs_status status);
 
 /* ABI version of this header (bumped on any layout change). */
-#define GS_ABI_VERSION 2
+#define GS_ABI_VERSION 3
 int32_t gs_abi_version(void);
 
 #ifdef __cplusplus

@@ -243,6 +243,9 @@ def guided_step(x, sigmas, step_idx, *, uncond=None, cond=None, cfg: float = 1.0
         blended = inpaint_blend(pred, original, m)
         den = np.where(present.reshape(B, 1, 1, 1), blended, pred)
 
+    if sampler == "euler_ancestral":
+        # the split treats sigma_next as a standard deviation: a negative one has none
+        ok &= sigma_next >= 0.0
     if sampler == "euler":
         x_next = euler(x, den, np.where(ok, sigma, 1.0), sigma_next)
     elif sampler == "euler_ancestral":

@@ -22,6 +22,13 @@ k = n_regions + 16.  An element passes when
                of T).
 
 Elements that pass only through the floor are counted and reported.
+
+Ancestral step (x' = den + rd (x - den) + up noise, rd = sigma_down / sigma): the
+kernel forms rd = r^2 (3 roundings) and up = r sqrt(d) sqrt(t) (about 6), then one
+more fma, so M takes rd in place of r plus up |noise|, and k grows by 8.  Model
+input (mi = m x' + (1 - m)(orig + sigma_next orig_noise)): the error of x' scaled by
+m plus 4 roundings of magnitude at most (1 - m)(|orig| + sigma_next |orig_noise|),
+so Mmi = m M + (1 - m)(|orig| + sigma_next |orig_noise|) with k grown by 4 more.
 """
 
 from __future__ import annotations
@@ -122,8 +129,8 @@ class GateReport:
 
 
 def gate(g: np.ndarray, ref: np.ndarray, M: np.ndarray, dtype: str, n_regions: int,
-         what: str = "") -> GateReport:
-    k = n_regions + 16
+         what: str = "", extra: int = 0) -> GateReport:
+    k = n_regions + 16 + extra
     err = np.abs(g - ref)
     floor = k * U * M
     if dtype == "fp32":

@@ -119,3 +119,61 @@ def test_host_entry_points_reject_invalid_arguments(lib):
     buf = (ctypes.c_float * 4)()
     assert lib.gs_sigmas(ctypes.byref(d), buf, 4, ctypes.byref(n), None) == gs.GS_ERR_CAPACITY
     assert n.value == 11
+
+
+def test_step_rejects_invalid_sampler_arguments(lib):
+    a = _valid_args()
+    a.sampler = 2                                                        # unknown sampler
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+    a = _valid_args()
+    a.sampler = gs.SAMPLERS["euler_ancestral"]                           # ancestral, no noise
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+    a = _valid_args()
+    a.model_in_out = 0x5000                                              # model input, no mask
+    a.orig_noise = 0x6000
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+    a = _valid_args()
+    a.inpaint_mask, a.original, a.model_in_out = 0x3000, 0x4000, 0x5000  # ... no orig_noise
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+
+
+_LAYOUT_PROBE = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "gs.h"
+#define F(S, m) printf(#S " " #m " %zu\n", offsetof(S, m));
+int main(void) {
+    printf("gs_step_args sizeof %zu\n", sizeof(gs_step_args));
+    printf("gs_region sizeof %zu\n", sizeof(gs_region));
+    printf("gs_curve_desc sizeof %zu\n", sizeof(gs_curve_desc));
+    printf("gs_schedule_desc sizeof %zu\n", sizeof(gs_schedule_desc));
+    %FIELDS%
+    return 0;
+}
+"""
+
+
+def test_ctypes_structs_match_the_header_layout(tmp_path):
+    """Every ctypes mirror in the binding has the C compiler's offsets and size."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    pairs = {"gs_step_args": gs.StepArgs, "gs_region": gs.RegionDesc,
+             "gs_curve_desc": gs.CurveDesc, "gs_schedule_desc": gs.ScheduleDesc}
+    fields = "\n    ".join(f"F({c}, {f})" for c, py in pairs.items() for f, _ in py._fields_)
+    src = tmp_path / "layout.c"
+    src.write_text(_LAYOUT_PROBE.replace("%FIELDS%", fields))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                               text=True).stdout.splitlines():
+        s, m, v = line.split()
+        got[(s, m)] = int(v)
+    for c, py in pairs.items():
+        assert got[(c, "sizeof")] == ctypes.sizeof(py), c
+        for f, _ in py._fields_:
+            assert got[(c, f)] == getattr(py, f).offset, (c, f)

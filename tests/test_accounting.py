@@ -11,6 +11,10 @@ def test_step_bytes_hand_counts():
                    denoised_out=True)
     frame = 3 * 2 * 24 * 4
     assert b == 4 * frame + 3 * 2 * 15 * 4 + 2 * 2 * 24 * 4 + 2 * 24 * 4
+    # ancestral noise read, model input written, fixed noise of the 2 blended samples read
+    b2 = step_bytes(3, 2, 4, 6, "fp32", cond=False, regions=[(3, 5)], inpaint_samples=2,
+                    denoised_out=True, noise=True, model_input=True)
+    assert b2 - b == frame + frame + 2 * 2 * 24 * 4
 
 
 def test_skipped_prediction_bytes_hand_count():

@@ -277,3 +277,28 @@ def test_model_input_blend_hand_values():
     # m = 1: x_next; m = 0: orig + 0.5 * (-1) = 0.5; m = 1/4: 0.5 + 0.75 * 0.5 = 0.875
     assert got.ravel().tolist() == [2.0, 0.5, 0.875]
     assert np.array_equal(O.model_input(xn, orig, on, [0.5], m, mask_present=[False]), xn)
+
+
+def test_ancestral_split_reduced_forms_and_edges():
+    """sigma_down = sigma_next^2 / sigma (from sigma_up^2 + sigma_down^2 = sigma_next^2 and
+    the definition of sigma_up); a step up in sigma has no split (sigma_up = 0, the
+    deterministic step); equal sigmas give sigma_up = 0, sigma_down = sigma."""
+    sig = np.array([14.6, 7.0, 3.0, 0.9, 5.0])
+    nxt = np.array([7.0, 3.0, 0.9, 0.03, 3.0])
+    up, down = O.ancestral_sigmas(sig, nxt)
+    np.testing.assert_allclose(down, nxt ** 2 / sig, rtol=1e-13, atol=0)
+    assert abs(up[-1] - 2.4) <= 4e-16 and abs(down[-1] - 1.8) <= 4e-16
+    up, down = O.ancestral_sigmas([2.0, 3.0], [3.0, 3.0])
+    assert up.tolist() == [0.0, 0.0] and down.tolist() == [3.0, 3.0]
+
+
+def test_ancestral_negative_sigma_next_is_skipped():
+    """A negative sigma_next is no standard deviation: the ancestral step flags the
+    sample (ok = False, x unchanged) while the deterministic step takes it."""
+    B, C, H, W = 2, 1, 2, 2
+    x, c, n = rnd((B, C, H, W), 4), rnd((B, C, H, W), 5), rnd((B, C, H, W), 6)
+    sig = np.array([4.0, 2.0, -1.0])
+    xa, _, ok = O.guided_step(x, sig, [0, 1], cond=c, sampler="euler_ancestral", noise=n)
+    assert ok.tolist() == [True, False] and np.array_equal(xa[1], x[1])
+    _, _, ok = O.guided_step(x, sig, [0, 1], cond=c)
+    assert ok.tolist() == [True, True]

@@ -277,3 +277,97 @@ def test_region_outside_its_timestep_range_drops_out(shape, kernel_choice):
     gs.guided_step(x, x_out=e, regions=[plain], **base)
     torch.cuda.synchronize()
     assert same_bits(a, b) and same_bits(d, e) and not same_bits(b, e)
+
+
+# Euler-ancestral (eta = 1) and the next model input under the inpaint wrapper.  The
+# split's closed forms: sigma_up = sigma_next sqrt(1 - sigma_next^2 / sigma^2) and
+# sigma_down / sigma = (sigma_next / sigma)^2; at sigma = 5, sigma_next = 3 they are
+# 2.4 and 0.36.
+REL = {torch.float32: 1e-6, torch.bfloat16: 2.0 ** -7, torch.float16: 2.0 ** -10}
+
+
+def close_to(got, want64, dtype):
+    g = got.to(torch.float64)
+    tol = REL[dtype] * want64.abs() + (2.0 ** -24 if dtype == torch.float16 else 0.0)
+    return bool(((g - want64).abs() <= tol).all())
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_ancestral_last_step_lands_on_denoised(dtype, shape):
+    """sigma_next = 0: sigma_up = sigma_down = 0, so the ancestral step lands on den
+    whatever the noise, bit for bit like the deterministic step."""
+    x, u, c, n = (rnd(shape, s, dtype) for s in (40, 41, 42, 43))
+    a, b, den = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(4.0, 0.0), uncond=u, cond=c, cfg=3.0, x_out=a,
+                   denoised_out=den, sampler="euler_ancestral", noise=n)
+    gs.guided_step(x, sigmas=sig(4.0, 0.0), uncond=u, cond=c, cfg=3.0, x_out=b)
+    torch.cuda.synchronize()
+    assert same_bits(a, den) and same_bits(a, b)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_ancestral_split_closed_forms(dtype, shape):
+    """With a zero prediction (den = 0): x = 0 leaves sigma_up * noise, and zero noise
+    leaves (sigma_down / sigma) * x."""
+    x, n = rnd(shape, 44, dtype), rnd(shape, 45, dtype)
+    z = torch.zeros_like(x)
+    out = torch.empty_like(x)
+    gs.guided_step(z, sigmas=sig(5.0, 3.0), uncond=z, cond=z, cfg=2.0, x_out=out,
+                   sampler="euler_ancestral", noise=n)
+    torch.cuda.synchronize()
+    assert close_to(out, 2.4 * n.to(torch.float64), dtype)
+    gs.guided_step(x, sigmas=sig(5.0, 3.0), uncond=z, cond=z, cfg=2.0, x_out=out,
+                   sampler="euler_ancestral", noise=z)
+    torch.cuda.synchronize()
+    assert close_to(out, 0.36 * x.to(torch.float64), dtype)
+
+
+@pytest.mark.parametrize("shape", [(4, 2, 8, 8), (4, 32, 128, 128)], ids=["small", "large"])
+def test_ancestral_negative_sigma_next_is_flagged(shape):
+    """A negative sigma_next has no ancestral split: the sample is flagged as a sigma
+    error and left unwritten; the deterministic step takes the same table."""
+    x, u, c, n = (rnd(shape, s, torch.bfloat16) for s in (46, 47, 48, 49))
+    sentinel = torch.full_like(x, 7.0)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idx = torch.tensor([0, 1, 0, 1], dtype=torch.int32, device=DEV)
+    sg = sig(4.0, 2.0, -1.0)
+    out = sentinel.clone()
+    gs.guided_step(x, sigmas=sg, uncond=u, cond=c, step_idx=idx, cfg=2.0, x_out=out,
+                   status=st, sampler="euler_ancestral", noise=n)
+    torch.cuda.synchronize()
+    assert int(st.item()) == gs.GS_DEV_SIGMA
+    assert torch.equal(out[1], sentinel[1]) and torch.equal(out[3], sentinel[3])
+    assert not torch.equal(out[0], sentinel[0]) and not torch.equal(out[2], sentinel[2])
+    st.zero_()
+    gs.guided_step(x, sigmas=sg, uncond=u, cond=c, step_idx=idx, cfg=2.0, x_out=out,
+                   status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("sampler", ["euler", "euler_ancestral"])
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_model_input_follows_the_mask(dtype, shape, sampler):
+    """Where the mask is 1, and for samples without a mask, the next model input is
+    x' bit for bit; where it is 0 it is original + sigma_next * orig_noise."""
+    B, C, H, W = shape
+    x, u, c, o, on, n = (rnd(shape, s, dtype) for s in (50, 51, 52, 53, 54, 55))
+    present = torch.zeros(B, dtype=torch.uint8, device=DEV)
+    present[: (B + 1) // 2] = 1
+    kw = dict(sigmas=sig(5.0, 2.0), uncond=u, cond=c, cfg=3.0, original=o, orig_noise=on,
+              mask_present=present, sampler=sampler, noise=n)
+    out, mi = torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, x_out=out, model_in_out=mi, inpaint_mask=torch.ones((B, 1, H, W),
+                                                                          device=DEV), **kw)
+    torch.cuda.synchronize()
+    assert same_bits(mi, out)
+    gs.guided_step(x, x_out=out, model_in_out=mi, inpaint_mask=torch.zeros((1, 1, H, W),
+                                                                           device=DEV), **kw)
+    torch.cuda.synchronize()
+    k = (B + 1) // 2
+    assert same_bits(mi[k:], out[k:])
+    want = o[:k].to(torch.float64) + 2.0 * on[:k].to(torch.float64)
+    assert close_to(mi[:k], want, dtype)

@@ -10,6 +10,8 @@ pointers and partial masks.  The acceptance gate is described in
 
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -32,7 +34,8 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
              step: int = None, region_masks: bool = False, offset: int = 0,
              uncond_none: bool = False, want_den: bool = False, pitch_align: int = 8,
              tma: bool = True, expect_kernel: str = None, mask_rows: bool = False,
-             poison: bool = False, region_ranges=None):
+             poison: bool = False, region_ranges=None, sampler: str = "euler",
+             model_in: bool = False, sigmas=None):
     """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok).
 
     mask_rows: pass the row summary of the latent mask (gs_mask_rows), so that bands
@@ -41,13 +44,18 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     of a blended sample whose mask is 0 there; the kernel must not read them (a read
     would carry NaN through 0 * pred into the output), and the oracle, which sees
     the clean values, must agree.  region_ranges: (t_start, t_end) per region, given
-    to both sides.
+    to both sides.  sampler: "euler" or "euler_ancestral" (fresh seeded noise, the
+    same on both sides).  model_in: also produce the next model input under the
+    inpaint wrapper (needs an inpaint workload) and gate it against the oracle's.
+    sigmas: a schedule (float32) in place of the workload's.
     """
+    if sampler != wl.sampler or model_in != wl.model_input:
+        wl = dataclasses.replace(wl, sampler=sampler, model_input=model_in)
     inp = step_inputs(wl, step_seed, B=B, C=C, H=H, W=W, region_masks=region_masks,
                       pitch_align=pitch_align)
     dt = DTYPES[wl.dtype]
     Bn, Cn, Hn, Wn = inp.noise.shape
-    sig = oracle_sigmas(wl)
+    sig = oracle_sigmas(wl) if sigmas is None else np.asarray(sigmas, dtype=np.float32)
     lut = oracle_lut(wl, len(sig) - 1)
     if inp.step_idx is not None:
         idx = inp.step_idx.numpy().astype(np.int64)
@@ -110,6 +118,13 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     kw = dict(uncond=dev_latent(u_gpu), cond=dev_latent(c_gpu), regions=regs,
               sigmas=torch.from_numpy(sig).to(DEV), x_out=outd, denoised_out=dend,
               status=status, tma=tma)
+    noise, orig_noise = inp.fresh_noise, inp.orig_noise
+    mid = dev_latent(torch.full_like(x, float("nan"))) if model_in else None
+    if sampler != "euler":
+        kw.update(sampler=sampler, noise=dev_latent(noise))
+    if model_in:
+        assert lat is not None
+        kw.update(model_in_out=mid, orig_noise=dev_latent(orig_noise))
     if inp.step_idx is not None:
         kw["step_idx"] = _cuda(inp.step_idx)
     else:
@@ -144,15 +159,24 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
                                  scale_lut=lut, regions=oregs,
                                  inpaint_mask=None if lat is None else lat.numpy(),
                                  mask_present=present if lat is not None else None,
-                                 original=to64(inp.original))
+                                 original=to64(inp.original), sampler=sampler,
+                                 noise=to64(noise))
     s = lut[idx] if lut is not None else np.full(Bn, np.float32(cfg))
     sg = sig[idx].astype(np.float64)
     sn = sig[np.minimum(idx + 1, len(sig) - 1)].astype(np.float64)
-    M = error_scale(to64(x), to64(u), to64(inp.cond), oregs, s, sn / sg,
+    r = sn / sg
+    extra = 0
+    if sampler == "euler_ancestral":
+        up, down = O.ancestral_sigmas(sg, sn)
+        r = down / sg
+        extra = 8
+    M = error_scale(to64(x), to64(u), to64(inp.cond), oregs, s, r,
                     None if lat is None else lat.numpy().astype(np.float64), present,
                     to64(inp.original), Hn, Wn)
+    if sampler == "euler_ancestral":
+        M = M + np.abs(up).reshape(Bn, 1, 1, 1) * np.abs(to64(noise))
     okb = ok.reshape(-1)
-    rep = gate(got[okb], ref[okb], M[okb], wl.dtype, len(oregs), what=wl.name)
+    rep = gate(got[okb], ref[okb], M[okb], wl.dtype, len(oregs), what=wl.name, extra=extra)
     if wl.dtype == "fp32":
         assert rep.normwise <= 1e-5
     assert int(status.item()) == 0
@@ -160,6 +184,15 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
         gd = to64(dend)
         Md = M  # den's own scale is bounded by M as well
         gate(gd[okb], den[okb], Md[okb], wl.dtype, len(oregs), what=wl.name + " denoised")
+    if model_in:
+        ref_mi = O.model_input(ref, to64(inp.original), to64(orig_noise), sn, lat.numpy(),
+                               present)
+        m4 = np.broadcast_to(lat.numpy().astype(np.float64), (Bn, 1, Hn, Wn))
+        Mmi = m4 * M + (1.0 - m4) * (np.abs(to64(inp.original)) +
+                                      np.abs(sn).reshape(Bn, 1, 1, 1) * np.abs(to64(orig_noise)))
+        Mmi = np.where(present.reshape(Bn, 1, 1, 1), Mmi, M)
+        gate(to64(mid)[okb], ref_mi[okb], Mmi[okb], wl.dtype, len(oregs),
+             what=wl.name + " model input", extra=extra + 4)
     return rep, got, ref, ok
 
 
@@ -302,3 +335,41 @@ def test_region_timestep_ranges(wl, tma):
     rep, *_ = run_case(wl, tma=tma, region_ranges=ranges, step=7,
                        expect_kernel="tma" if tma else "vector")
     assert rep.n == wl.elements
+
+
+@pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_ancestral_full_size(wl):
+    """The Euler-ancestral step (eta = 1) at each workload's full size, with the next
+    model input under the inpaint wrapper where the workload inpaints."""
+    rep, got, *_ = run_case(wl, sampler="euler_ancestral", model_in=wl.inpaint,
+                            want_den=True, expect_kernel="vector")
+    assert rep.n == wl.elements and np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("sampler", ["euler", "euler_ancestral"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+@pytest.mark.parametrize("shape,offset", [((3, 3, 13, 11), 0), ((2, 6, 7, 24), 0),
+                                          ((5, 2, 16, 16), 1), ((2, 4, 37, 64), 0)])
+def test_sampler_options_ragged(dtype, shape, offset, sampler):
+    """Both samplers with the model-input output on ragged shapes, on the vector and
+    the scalar path (an unaligned base), with regions and a partial inpaint batch."""
+    B, C, H, W = shape
+    base = WORKLOADS[4]
+    wl = Workload("samplers", B, C, H, W, dtype, base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=2, region_side=(1, max(1, min(H, W))),
+                  feather=2, inpaint=True, inpaint_samples=max(1, B // 2), seed=18)
+    run_case(wl, region_masks=True, want_den=True, sampler=sampler, model_in=True,
+             offset=offset, expect_kernel="scalar" if offset else None)
+
+
+def test_ancestral_close_sigmas():
+    """Adjacent sigmas within a few ulps of each other, a step up (sigma_next > sigma:
+    no split, the deterministic step) and a last step to 0, on one staggered batch."""
+    sig = np.array([10.0, np.nextafter(np.float32(10.0), np.float32(0.0)), 9.999,
+                    10.5, 3.0, 0.0], dtype=np.float32)
+    base = WORKLOADS[4]
+    wl = Workload("close", 40, 4, 16, 32, "fp32", base.schedule.__class__("karras", 5),
+                  base.guidance.__class__(cfg=5.0), staggered=True, seed=19)
+    assert set(step_inputs(wl).step_idx.tolist()) == set(range(5))
+    rep, *_ = run_case(wl, sampler="euler_ancestral", sigmas=sig)
+    assert rep.normwise <= 1e-5
