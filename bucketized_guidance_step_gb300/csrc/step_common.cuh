@@ -197,6 +197,26 @@ __device__ __forceinline__ void grid_dependents_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Euler-ancestral split of a step (eta = 1), fp32: sigma_up and sigma_down / sigma,
+// for 0 <= sigma_next (the caller flags a negative one).  With r = sigma_next / sigma
+// the definitions reduce to sigma_up = r sqrt((sigma - sigma_next)(sigma + sigma_next))
+// and sigma_down / sigma = r^2 (sigma_down^2 = sigma_next^2 - sigma_up^2 =
+// sigma_next^4 / sigma^2).  This form has no cancellation when the two sigmas are
+// close and no overflow of the squares; each result is within a few roundings of the
+// exact split.  sigma_next > sigma has no split (the variance under the root would be
+// negative): the clamped definitions give sigma_up = 0, i.e. the deterministic step.
+__device__ __forceinline__ void ancestral_split(float sigma, float sigma_next, float& up,
+                                                float& rdown) {
+    const float r = __fdiv_rn(sigma_next, sigma);
+    if (sigma_next <= sigma) {
+        up = r * (__fsqrt_rn(sigma - sigma_next) * __fsqrt_rn(sigma + sigma_next));
+        rdown = r * r;
+    } else {
+        up = 0.0f;
+        rdown = r;
+    }
+}
+
 // Ramp factor at 0-based distance t from a feathered edge: min(1, (t + 1) / F),
 // exactly 1 from t = F - 1 on, else (t + 1) times 1/F precomputed on the host
 // (exact for power-of-two F).

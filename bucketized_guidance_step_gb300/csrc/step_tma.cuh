@@ -1,0 +1,829 @@
+// TMA-fed variant of the fused guided step (sm_103a).
+//
+// Same arithmetic as the register-streaming kernel in guided_step.cu (see the
+// formulas in include/gs.h); a different way to move the bytes.  Each CTA owns
+// one tile = (sample b, a group of CG channels, a band of RB full rows), and
+// every input of the tile arrives as one 3-D TMA box into shared memory:
+//
+//   * x, uncond, cond and original as [CG][RB][W] boxes of their [B*C][H][W]
+//     tensors, and the inpaint mask as a [RB][W] box of [B or 1][H][W];
+//   * every regional output that overlaps the band as a [CG][RB][wbox] box of
+//     its [B*C][h][pitch] slab, started at slab row band*RB - y0 so that box row
+//     i is frame row band*RB + i.  TMA zero-fills rows outside the slab, so a
+//     region arrives row-aligned with the frame whatever its origin, and only
+//     regions that touch the band are fetched at all.
+//
+// Thread 0 arms the CTA's mbarrier with the tile's byte count and issues the
+// boxes; no register holds a load in flight.  Every thread then computes VEC
+// pixels x CG channels of one row from shared memory (region weights and the
+// mask once per pixel, reused over the channels; packed fp32-pair math) and
+// writes x_out with 16-byte stores.  Several tile-CTAs are resident per SM, so
+// the loads of some overlap the arithmetic of others, and the CTA scheduler
+// hands out tiles as SMs drain.
+//
+// The mbarrier wait is bounded (200 ms of %globaltimer); on expiry the thread
+// sets GS_DEV_TIMEOUT in the status word and returns.
+//
+// This header holds the launch parameters, the kernel template and its launch
+// templates; step_tma.cu builds the parameters and launches the deterministic
+// Euler instances, step_tma_sampler.cu compiles the instances with the sampler
+// options (ancestral noise, the next model input), so the two compile in parallel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "step_common.cuh"
+
+namespace gs_detail {
+
+constexpr int kMaxThreads = 256;
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
+constexpr unsigned long long kDrainLimitNs = 10ull * 1000ull * 1000ull;
+constexpr unsigned kMaxTileBytes = 200u * 1024u;
+
+struct TmaRegion {
+    int y0, x0, h, w;
+    float strength;
+    float inv_feather;
+    int edges;
+    int feather;              // F (ramp width in pixels; 0 = none)
+    int wbox;                 // box width in elements (w rounded up to whole 16-byte vectors)
+    int step_lo;              // the region takes part at step indices step_lo <= i < step_hi
+    const float* mask;
+    long long mask_bstride;
+    unsigned smem_off;        // byte offset of the region's box inside the tile
+    unsigned tile_bytes;      // CG * RB * wbox * element size
+    int col0;                 // frame column of column-table entry 0 (x0 rounded down to VEC)
+    int ncol;                 // column-table length (multiple of VEC)
+    unsigned tab_off;         // byte offset of the column table inside the tile
+    int step_hi;
+};
+
+static_assert(sizeof(TmaRegion) == 80, "region descriptors: 80 bytes (shared memory per CTA is tight)");
+
+struct TmaParams {
+    CUtensorMap tm_x, tm_u, tm_c, tm_o, tm_m;
+    CUtensorMap tm_n, tm_on;     // the ancestral step's noise, the run's fixed noise
+    CUtensorMap tm_r[GS_MAX_REGIONS];
+    TmaRegion reg[GS_MAX_REGIONS];
+    void* x_out;
+    void* den_out;
+    const float* sig;
+    const int* step_idx;
+    const float* lut;
+    const unsigned char* present;
+    unsigned int* status;
+    long long n_tiles;
+    int B, C, H, W;
+    int RB, nbands, ncg;
+    int n_regions, n_sig, step, n_lut;
+    float cfg;
+    int has_u, has_c, mask_shared;
+    int test_wait_timeout;
+    unsigned tile_bytes, plane_bytes, mask_bytes;
+    unsigned off_x, off_u, off_c, off_o, off_m;
+    unsigned rowtab_off;
+    const unsigned* mask_rows;   // row summary of the inpaint mask, or null
+    int ranged;                  // some region has a timestep range (else all take part)
+    int mask_words;              // words per mask in mask_rows: ceil(H / 32)
+    int sampler;                 // GS_SAMPLER_*
+    void* model_in;              // next model input under the inpaint wrapper, or null
+    unsigned off_n, off_on;      // stage offsets of the noise and fixed-noise boxes
+};
+
+// Launch the instances with the sampler options (ancestral noise and/or the next
+// model input); defined in step_tma_sampler.cu.
+gs_status tma_launch_sampler(TmaParams& p, int dtype, int cg, int threads, unsigned smem,
+                             bool reg, bool inp, gs_stream stream, unsigned flags);
+
+namespace {
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Add bytes the current phase must receive before it can complete (no arrival).
+__device__ __forceinline__ void mbar_add_tx(unsigned bar, unsigned bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about kSuspendNs pass, instead of spinning on issue slots
+// that co-resident CTAs could use.
+constexpr unsigned kSuspendNs = 1000000u;
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_for(unsigned bar, unsigned parity,
+                                              unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity) {
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
+}
+
+__device__ __forceinline__ void tma_load_3d(unsigned dst, const CUtensorMap* map, int x, int y,
+                                            int z, unsigned bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<unsigned long long>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<unsigned long long>(map))
+                 : "memory");
+}
+
+__device__ __forceinline__ void flag(unsigned int* status, unsigned bits) {
+    if (status != nullptr) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ bool band_hits(const TmaRegion& R, int y_band, int RB) {
+    return y_band < R.y0 + R.h && y_band + RB > R.y0;
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ Raw<T, VEC> ld_smem(const unsigned char* base, unsigned byte_off) {
+    Raw<T, VEC> r;
+    const uint4 v = *reinterpret_cast<const uint4*>(base + byte_off);
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+    r.w[2] = v.z;
+    r.w[3] = v.w;
+    return r;
+}
+
+// Accumulate one region into pos over CG channels: the region's box row for this
+// thread is at byte rbase (channel stride rk); the thread's window starts SH
+// elements into aligned vector q0 (SH is the same for every thread of the tile,
+// so it is a template parameter and the switch that picks it runs once per region).
+template <typename T, int VEC, int CG, int SH>
+__device__ __forceinline__ void region_channels(const unsigned char* st, unsigned rbase,
+                                                unsigned rk, int q0, bool lo_ok, bool hi_ok,
+                                                const f2 (&w2)[VEC / 2], f2 (&pos)[CG][VEC / 2]) {
+    constexpr int kW = Raw<T, VEC>::kWords;
+#pragma unroll
+    for (int k = 0; k < CG; ++k) {
+        Raw<T, VEC> lo, hi;
+#pragma unroll
+        for (int i = 0; i < kW; ++i) lo.w[i] = hi.w[i] = 0u;
+        if (lo_ok) lo = ld_smem<T, VEC>(st, rbase + k * rk + q0 * 16);
+        if (SH != 0 && hi_ok) hi = ld_smem<T, VEC>(st, rbase + k * rk + (q0 + 1) * 16);
+        Raw<T, VEC> win;
+        unsigned cat[2 * kW];
+#pragma unroll
+        for (int i = 0; i < kW; ++i) {
+            cat[i] = lo.w[i];
+            cat[kW + i] = hi.w[i];
+        }
+        if constexpr (sizeof(typename T::scalar) == 4) {
+#pragma unroll
+            for (int i = 0; i < kW; ++i) win.w[i] = cat[i + SH];
+        } else {
+#pragma unroll
+            for (int i = 0; i < kW; ++i)
+                win.w[i] = (SH & 1) ? __funnelshift_r(cat[i + SH / 2], cat[i + SH / 2 + 1], 16)
+                                    : cat[i + SH / 2];
+        }
+#pragma unroll
+        for (int q = 0; q < VEC / 2; ++q) pos[k][q] = fma2(w2[q], widen2<T, VEC>(win, q), pos[k][q]);
+    }
+}
+
+// ---- the kernel ---------------------------------------------------------------
+// One CTA per tile; grid (band, channel group, sample), block (pixel group, row).
+// Before the grid-dependency wait the CTA only prefetches its tensor maps and
+// initialises its mbarrier.  After it, two threads feed the barrier, each
+// arriving once: thread 0 issues the boxes that need only the tile coordinates
+// (x, uncond, cond, regions); the parameter thread loads the sample's step index
+// and inpaint flag together, issues the original and mask boxes if the sample
+// carries a mask, and then finishes the step parameters.  No box waits on a
+// global load that another box does not need.  While the boxes are in flight the
+// remaining warps build, for every region touching the band, a frame-aligned
+// table of its column factors (feather ramps, 0 outside the region), so that a
+// thread's VEC weights are two 16-byte loads.  After a CTA barrier every thread
+// computes CG channels of its VEC pixels from shared memory.  With regions in
+// multi-channel tiles the boxes come in two groups on two barriers (see kSplit), so
+// that the regional accumulation overlaps the arrival of x, original and mask.
+struct TileParams {
+    float s, one_minus_s, ratio;   // ratio: sigma_next / sigma, or sigma_down / sigma
+    float up, sigma_next;          // sigma_up (ancestral), sigma_next (model input)
+    int ok;             // 1 = step this sample, 0 = skip it
+    int inpaint;        // 1 = this sample blends with its original
+    int arrived;        // 0 = the wait for the tile gave up
+    int need_pred;      // 0 = the band's mask rows are all zero: prediction not read
+};
+
+// One region as this tile's threads use it, built once per CTA by the region's
+// warp, so that a thread reads three 16-byte words per region instead of the
+// descriptor's fields one by one.  Tile rows [row_lo, row_hi) and frame columns
+// [x_lo, x_hi) are the region's; a thread whose VEC pixels start at frame column
+// x0 finds its first box vector at q0 = (x0 + qoff) / VEC (an exact division)
+// and its window sh elements into it; box row i starts at byte rbase0 + i*rrow of
+// the tile, channel k at k*rk further; column-factor entry of frame column x is
+// at byte tabx + 4x of the tile.
+struct __align__(16) TileRegion {
+    int row_lo, row_hi, x_lo, x_hi;
+    int qoff, sh, nq, has_mask;
+    unsigned rbase0, rrow, rk;
+    int tabx;
+};
+
+template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ>
+__global__ void __launch_bounds__(kMaxThreads)
+    guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
+    static_assert(INP || !SKIP, "read skipping needs the inpaint inputs");
+    static_assert(!(NZ && SKIP), "the sampler options are not combined with read skipping");
+    using S = typename T::scalar;
+    constexpr int VEC = 16 / static_cast<int>(sizeof(S));
+    constexpr int NP = VEC / 2;
+    constexpr unsigned ES = sizeof(S);
+    // With regions, in tiles of several channels (the shapes of large steps), the
+    // tile's boxes come in two groups, each on its own mbarrier: A = uncond, cond
+    // and the region slabs (all the positive branch and the combine need), B = x,
+    // original and mask (the blend and the Euler update).  The CTA accumulates the
+    // regions while B is still landing.  One-channel tiles (small steps, where the
+    // whole step is one wave of CTAs and latency-bound) keep a single barrier: there
+    // the second wait costs more than the overlap gains.
+    constexpr bool kSplit = REG && CG > 1;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<unsigned long long>(smem_raw) + 127ull) & ~127ull);
+    unsigned long long* full = reinterpret_cast<unsigned long long*>(smem);
+    unsigned char* st = smem + 128;
+
+    const int band = blockIdx.x;
+    const int cgi = blockIdx.y;
+    const int b = blockIdx.z;
+    const int nthreads = blockDim.x * blockDim.y;
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+    const int row = threadIdx.y;
+    const int x0 = threadIdx.x * VEC;
+    const int y_band = band * p.RB;
+    const int y = y_band + row;
+    const int z = b * p.C + cgi * CG;
+    const bool has_u = p.has_u != 0, has_c = p.has_c != 0;
+    // sampler options (NZ instances only): ancestral noise (a box in x's group) and
+    // the next model input (the fixed noise a box in the original's group)
+    const bool anc = NZ && p.sampler == GS_SAMPLER_EULER_ANCESTRAL;
+    const bool want_mi = NZ && p.model_in != nullptr;
+
+    __shared__ TmaRegion regs[REG ? GS_MAX_REGIONS : 1];
+    __shared__ TileRegion tregs[REG ? GS_MAX_REGIONS : 1];
+    __shared__ TileParams tp;
+    const unsigned bar = smem_u32(full);                // A (the only barrier without regions)
+    const unsigned barB = kSplit ? bar + 8u : bar;      // B
+    const unsigned s0 = smem_u32(st);
+    if (tid == 0) {
+        // Every descriptor this tile may use starts on its way now.
+        prefetch_map(&p.tm_x);
+        if (has_u) prefetch_map(&p.tm_u);
+        if (has_c) prefetch_map(&p.tm_c);
+        if (INP) {
+            prefetch_map(&p.tm_o);
+            prefetch_map(&p.tm_m);
+        }
+        if (anc) prefetch_map(&p.tm_n);
+        if (INP && want_mi) prefetch_map(&p.tm_on);
+        if constexpr (REG) {
+            for (int r = 0; r < p.n_regions; ++r) prefetch_map(&p.tm_r[r]);
+        }
+        if constexpr (kSplit) {
+            mbar_init(bar, 1u);
+            mbar_init(barB, nthreads > 32 ? 2u : 1u);
+        } else {
+            mbar_init(bar, nthreads > 32 ? 2u : 1u);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // Everything above touches only kernel parameters; with programmatic
+    // dependent launch it overlaps the tail of the previous kernel.  Inputs
+    // (which a preceding kernel may produce) are read only after this wait.
+    grid_dependency_wait();
+    grid_dependents_launch();
+
+    // The prediction boxes (uncond, cond, regions) go on `bar` (group A when split).
+    // With a row summary of the inpaint mask they wait for the parameter thread,
+    // which skips them for a band whose mask rows are all zero in a blended sample.
+    // (SKIP: instances launched only when the row summary is given)
+    constexpr bool defer = SKIP;
+    auto issue_prediction = [&]() {
+        if (has_u) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
+        }
+        if (has_c) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_c, &p.tm_c, 0, y_band, z, bar);
+        }
+        if constexpr (REG) {
+            // only the four fields the issue needs, read straight from the parameters
+            for (int r = 0; r < p.n_regions; ++r) {
+                const int ry0 = p.reg[r].y0, rh = p.reg[r].h;
+                if (y_band >= ry0 + rh || y_band + p.RB <= ry0) continue;
+                mbar_add_tx(bar, p.reg[r].tile_bytes);
+                tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], 0, y_band - ry0, z, bar);
+            }
+        }
+    };
+
+    // Thread 0: the boxes that need nothing but the tile coordinates.  Each box's
+    // bytes are added to the barrier before the box is issued, and each feeding
+    // thread arrives after its last box, so the phase cannot complete early.
+    if (tid == 0) {
+        if constexpr (!kSplit) {
+            mbar_add_tx(bar, p.plane_bytes);
+            tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
+            if (anc) {
+                mbar_add_tx(bar, p.plane_bytes);
+                tma_load_3d(s0 + p.off_n, &p.tm_n, 0, y_band, z, bar);
+            }
+        }
+        if constexpr (!defer) issue_prediction();
+        if constexpr (kSplit) {
+            if constexpr (!defer) {
+                // group A is complete: thread 0 is its only feeder
+                if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+                mbar_arrive(bar);
+            }
+            mbar_add_tx(barB, p.plane_bytes);
+            tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, barB);
+            if (anc) {
+                mbar_add_tx(barB, p.plane_bytes);
+                tma_load_3d(s0 + p.off_n, &p.tm_n, 0, y_band, z, barB);
+            }
+        }
+    }
+
+    // The parameter thread: the step index, the inpaint flag and (with a row
+    // summary) the band's mask rows are independent loads issued together; the
+    // deferred prediction boxes and the original and mask boxes go out as soon as
+    // those are known, then the scale and sigmas (which depend on the index) are
+    // read.  With a single warp, thread 0 plays both parts (its boxes first) and
+    // arrives once on each barrier.
+    const int ptid = nthreads > 32 ? 32 : 0;
+    if (tid == ptid) {
+        const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
+        const bool present = INP && (p.present == nullptr || __ldg(p.present + b) != 0);
+        bool need_pred = true;
+        if (defer && present) {
+            // rows y_band .. y_end-1 of this sample's mask: any nonzero?
+            const unsigned* words = p.mask_rows + (p.mask_shared ? 0 : b) * p.mask_words;
+            const int y_end = y_band + p.RB < p.H ? y_band + p.RB : p.H;
+            unsigned any = 0u;
+            for (int w = y_band >> 5; w <= (y_end - 1) >> 5; ++w) {
+                const int lo = y_band > w * 32 ? y_band - w * 32 : 0;
+                const int hi = y_end < w * 32 + 32 ? y_end - w * 32 : 32;   // rows [lo, hi)
+                const unsigned sel = (hi == 32 ? ~0u : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+                any |= __ldg(words + w) & sel;
+            }
+            need_pred = any != 0u;
+        }
+        if constexpr (defer) {
+            if (need_pred) issue_prediction();
+            if constexpr (kSplit) {
+                // group A is complete: with deferral this thread is its only feeder
+                if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+                mbar_arrive(bar);
+            }
+        }
+        if (INP && present) {
+            mbar_add_tx(barB, p.plane_bytes + p.mask_bytes + (want_mi ? p.plane_bytes : 0u));
+            tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, barB);
+            tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, barB);
+            if (want_mi) tma_load_3d(s0 + p.off_on, &p.tm_on, 0, y_band, z, barB);
+        }
+        tp.inpaint = present ? 1 : 0;
+        if constexpr (defer) tp.need_pred = need_pred ? 1 : 0;
+        if (ptid != 0) mbar_arrive(barB);
+        const bool in_range =
+            idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
+        const int si = in_range ? idx : 0;
+        const float sv = p.lut != nullptr ? __ldg(p.lut + si) : p.cfg;
+        const float sigma = __ldg(p.sig + si);
+        const float sigma_next = __ldg(p.sig + si + 1);
+        // (the ancestral split takes sigma_next as a standard deviation: >= 0)
+        const bool sigma_ok =
+            sigma > 0.0f && sigma <= 3.402823466e38f && (!anc || sigma_next >= 0.0f);
+        const bool uncond_ok = has_u || sv == 1.0f;
+        tp.s = sv;
+        tp.one_minus_s = 1.0f - sv;
+        float ratio = __fdiv_rn(sigma_next, sigma), up = 0.0f;
+        if (anc) ancestral_split(sigma, sigma_next, up, ratio);
+        tp.ratio = ratio;
+        tp.up = up;
+        tp.sigma_next = sigma_next;
+        tp.ok = in_range && sigma_ok && uncond_ok ? 1 : 0;
+        if (!tp.ok && band == 0 && cgi == 0) {
+            unsigned bits = 0;
+            if (!in_range) bits |= GS_DEV_STEP_RANGE;
+            else if (!sigma_ok) bits |= GS_DEV_SIGMA;
+            if (in_range && !uncond_ok) bits |= GS_DEV_NEED_UNCOND;
+            flag(p.status, bits);
+        }
+    }
+
+    if constexpr (REG) {
+        // While the boxes are in flight: one warp per region reads the region's
+        // descriptor from the kernel parameters with the same addresses in every
+        // lane (a broadcast, where lanes reading different words would serialise
+        // one parameter load per lane), lane 0 keeps a copy in shared memory for
+        // the compute loop, and the warp fills the region's frame-aligned
+        // column-factor table if the region touches the band.  Warps 0 and 1 feed
+        // the barrier, so with three or more warps the others take this work.
+        const int warp = tid >> 5, lane = tid & 31, nwarps = (nthreads + 31) >> 5;
+        const int w0 = nwarps >= 3 ? 2 : 0;
+        // the sample's step index decides which regions' timestep ranges hold; a
+        // region outside its range is recorded as touching no row of the band
+        const int sidx = p.ranged && warp >= w0 && warp - w0 < p.n_regions
+                             ? (p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step)
+                             : 0;
+        for (int r = warp - w0; r >= 0 && r < p.n_regions; r += nwarps - w0) {
+            const TmaRegion R = p.reg[r];
+            const bool hits =
+                band_hits(R, y_band, p.RB) && sidx >= R.step_lo && sidx < R.step_hi;
+            if (lane == 0) {
+                regs[r] = R;
+                TileRegion t;
+                t.row_lo = hits ? (R.y0 > y_band ? R.y0 - y_band : 0) : 0;
+                t.row_hi = hits ? (R.y0 + R.h - y_band < p.RB ? R.y0 + R.h - y_band : p.RB) : 0;
+                t.x_lo = R.x0;
+                t.x_hi = R.x0 + R.w;
+                t.sh = (VEC - R.x0 % VEC) % VEC;
+                t.qoff = -R.x0 - t.sh;
+                t.nq = R.wbox / VEC;
+                t.has_mask = R.mask != nullptr ? 1 : 0;
+                t.rbase0 = R.smem_off;
+                t.rrow = static_cast<unsigned>(R.wbox) * sizeof(S);
+                t.rk = static_cast<unsigned>(p.RB) * R.wbox * sizeof(S);
+                t.tabx = static_cast<int>(R.tab_off) - 4 * R.col0;
+                tregs[r] = t;
+            }
+            if (!hits) continue;
+            // row factors of the band's rows: strength * top ramp * bottom ramp
+            float* rowtab = reinterpret_cast<float*>(st + p.rowtab_off) + r * p.RB;
+            for (int i = lane; i < p.RB; i += 32) {
+                const int ty = y_band + i - R.y0;
+                float wrow = R.strength;
+                if (R.edges & kEdgeTop) wrow = wrow * ramp(ty, R.feather, R.inv_feather);
+                if (R.edges & kEdgeBottom) wrow = wrow * ramp(R.h - 1 - ty, R.feather, R.inv_feather);
+                rowtab[i] = wrow;
+            }
+            float* tab = reinterpret_cast<float*>(st + R.tab_off);
+            for (int i = lane; i < R.ncol; i += 32) {
+                const int tx = R.col0 + i - R.x0;
+                tab[i] = (tx >= 0 && tx < R.w)
+                             ? column_factor(R.edges, R.feather, R.inv_feather, tx, R.w)
+                             : 0.0f;
+            }
+        }
+    }
+
+    if (tid == 0) {
+        tp.arrived = 1;
+        if constexpr (!kSplit) {
+            if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+        }
+        mbar_arrive(barB);
+        // ---- wait for the boxes (the rest of the CTA sleeps at the barrier) ----
+        if (!mbar_wait(bar, 0)) {
+            flag(p.status, GS_DEV_TIMEOUT);
+            tp.arrived = 0;
+            // let group B land before the CTA can exit (bounded)
+            if constexpr (kSplit) (void)mbar_wait_for(barB, 0, kDrainLimitNs);
+        }
+    }
+    __syncthreads();
+    if (tp.ok != 1 || tp.arrived != 1) {
+        // A skipped sample: group B (x, original, mask, noise) may still be landing in
+        // this CTA's shared memory, which must not be handed to another CTA before it
+        // has.  (After a timeout thread 0 has drained it already.)
+        if constexpr (kSplit) {
+            if (tid == 0 && tp.arrived == 1 && !mbar_wait(barB, 0)) flag(p.status, GS_DEV_TIMEOUT);
+        }
+        return;
+    }
+    // rows past H (a ragged last band): no arithmetic, but with regions they still
+    // take part in the second CTA barrier
+    const bool active = y < p.H;
+    if (!kSplit && !active) return;
+    const bool inpaint = INP && tp.inpaint != 0;
+    if (SKIP && tp.need_pred == 0) {
+        // A blended band whose mask is 0 on every row: den = original (up to the sign
+        // of zero), so the prediction was not loaded.  Only x and the original remain.
+        if constexpr (kSplit) {
+            if (tid == 0 && !mbar_wait(barB, 0)) {
+                flag(p.status, GS_DEV_TIMEOUT);
+                tp.arrived = 0;
+            }
+            __syncthreads();
+            if (tp.arrived != 1) return;
+        }
+        if (!active) return;
+        const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
+        const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
+        const long long plane = static_cast<long long>(p.H) * p.W;
+        const long long gbase =
+            static_cast<long long>(z) * plane + static_cast<long long>(y) * p.W + x0;
+        const f2 r2 = splat2(tp.ratio);
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+            const Raw<T, VEC> xv = ld_smem<T, VEC>(st + p.off_x, k * kstride + pix);
+            const Raw<T, VEC> ov = ld_smem<T, VEC>(st + p.off_o, k * kstride + pix);
+            Raw<T, VEC> xo;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const f2 den = widen2<T, VEC>(ov, q);
+                narrow2<T, VEC>(xo, q, fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den));
+            }
+            store_raw<T, VEC>(p.x_out, gbase + k * plane, xo);
+            if (p.den_out != nullptr) store_raw<T, VEC>(p.den_out, gbase + k * plane, ov);
+        }
+        return;
+    }
+
+    const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
+    const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
+
+    // positive branch
+    f2 pos[CG][NP];
+    const f2 s2 = splat2(tp.s);
+    const f2 oms2 = splat2(tp.one_minus_s);
+    if constexpr (REG) {
+        if (active) {
+            f2 wsum2[NP];
+#pragma unroll
+            for (int q = 0; q < NP; ++q) wsum2[q] = splat2(has_c ? 1.0f : 0.0f);
+#pragma unroll
+            for (int k = 0; k < CG; ++k) {
+                if (has_c) {
+                    const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_c, k * kstride + pix);
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(v, q);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) pos[k][q] = splat2(0.0f);
+                }
+            }
+            const float* rowtabs = reinterpret_cast<const float*>(st + p.rowtab_off);
+            for (int r = 0; r < p.n_regions; ++r) {
+                const TileRegion tr = tregs[r];
+                if (row < tr.row_lo || row >= tr.row_hi || x0 + VEC <= tr.x_lo || x0 >= tr.x_hi) continue;
+                // weights: row factor times the tabulated column factors (0 outside)
+                const float* tab = reinterpret_cast<const float*>(st + tr.tabx + 4 * x0);
+                const f2 wr2 = splat2(rowtabs[r * p.RB + row]);
+                f2 w2[NP];
+#pragma unroll
+                for (int q = 0; q < VEC / 4; ++q) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(tab + 4 * q);
+                    w2[2 * q] = mul2(wr2, mk2(c4.x, c4.y));
+                    w2[2 * q + 1] = mul2(wr2, mk2(c4.z, c4.w));
+                }
+                if (tr.has_mask) {
+                    const TmaRegion& R = regs[r];
+                    const int ty = y - R.y0;
+                    const int xs = x0 - R.x0;
+                    const float* mrow = R.mask + b * R.mask_bstride + static_cast<long long>(ty) * R.w;
+                    float wj[VEC];
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) {
+                        wj[2 * q] = lo_of(w2[q]);
+                        wj[2 * q + 1] = hi_of(w2[q]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        if (xs + j >= 0 && xs + j < R.w) wj[j] = wj[j] * __ldg(mrow + xs + j);
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
+                }
+#pragma unroll
+                for (int q = 0; q < NP; ++q) wsum2[q] = add2(wsum2[q], w2[q]);
+                // Box row `row` of this region's tile is frame row y.  Columns outside
+                // [0, w) are zeros (TMA fills the box past the slab's width, and
+                // vectors outside the box are not read), so no pixel outside the
+                // region can bring a non-finite value.
+                const int q0 = (x0 + tr.qoff) / VEC;      // exact: x0 + qoff is a multiple of VEC
+                const int sh = tr.sh;
+                const bool lo_ok = q0 >= 0 && q0 < tr.nq;
+                const bool hi_ok = q0 + 1 >= 0 && q0 + 1 < tr.nq;
+                const unsigned rbase = tr.rbase0 + static_cast<unsigned>(row) * tr.rrow;
+                const unsigned rk = tr.rk;
+                switch (sh) {
+                    case 0: region_channels<T, VEC, CG, 0>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                    case 1: region_channels<T, VEC, CG, 1>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                    case 2: region_channels<T, VEC, CG, 2>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                    case 3: region_channels<T, VEC, CG, 3>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                    default:
+                        if constexpr (VEC == 8) {
+                            switch (sh) {
+                                case 4: region_channels<T, VEC, CG, 4>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                                case 5: region_channels<T, VEC, CG, 5>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                                case 6: region_channels<T, VEC, CG, 6>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                                default: region_channels<T, VEC, CG, 7>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
+                            }
+                        }
+                        break;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const f2 inv = recip_or_zero2(wsum2[q]);
+#pragma unroll
+                for (int k = 0; k < CG; ++k) pos[k][q] = mul2(pos[k][q], inv);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+            const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_c, k * kstride + pix);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(v, q);
+        }
+    }
+
+    if constexpr (kSplit) {
+        // combine while group B lands, then wait for it
+        if (active && has_u) {
+#pragma unroll
+            for (int k = 0; k < CG; ++k) {
+                const Raw<T, VEC> uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    pos[k][q] = fma2(s2, pos[k][q], mul2(oms2, widen2<T, VEC>(uv, q)));
+            }
+        }
+        if (tid == 0 && !mbar_wait(barB, 0)) {
+            flag(p.status, GS_DEV_TIMEOUT);
+            tp.arrived = 0;
+        }
+        __syncthreads();
+        if (tp.arrived != 1 || !active) return;
+    }
+
+    // combine (without regions), inpaint blend, Euler, round and store
+    const f2 r2 = splat2(tp.ratio);
+    f2 m2[NP], omm2[NP];
+    if (INP && inpaint) {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(
+                st + p.off_m + (static_cast<unsigned>(row) * p.W + x0 + 4 * q) * 4u);
+            m2[2 * q] = mk2(v.x, v.y);
+            m2[2 * q + 1] = mk2(v.z, v.w);
+        }
+#pragma unroll
+        for (int q = 0; q < NP; ++q) omm2[q] = sub2(splat2(1.0f), m2[q]);
+    }
+    const long long plane = static_cast<long long>(p.H) * p.W;
+    const long long gbase = static_cast<long long>(z) * plane + static_cast<long long>(y) * p.W + x0;
+    const f2 up2 = splat2(NZ ? tp.up : 0.0f);
+    const f2 sn2 = splat2(NZ ? tp.sigma_next : 0.0f);
+#pragma unroll
+    for (int k = 0; k < CG; ++k) {
+        const Raw<T, VEC> xv = ld_smem<T, VEC>(st + p.off_x, k * kstride + pix);
+        Raw<T, VEC> uv, ov, nv, onv, xo, dn, mi;
+        if (!kSplit && has_u) uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+        if (INP && inpaint) ov = ld_smem<T, VEC>(st + p.off_o, k * kstride + pix);
+        if (NZ && anc) nv = ld_smem<T, VEC>(st + p.off_n, k * kstride + pix);
+        if (NZ && INP && want_mi && inpaint) onv = ld_smem<T, VEC>(st + p.off_on, k * kstride + pix);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            f2 pred = pos[k][q];
+            if (!kSplit && has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(uv, q)));
+            f2 den = pred;
+            if (INP && inpaint) den = fma2(m2[q], pred, mul2(omm2[q], widen2<T, VEC>(ov, q)));
+            f2 xn = fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den);
+            if (NZ && anc) xn = fma2(up2, widen2<T, VEC>(nv, q), xn);
+            narrow2<T, VEC>(xo, q, xn);
+            if (p.den_out != nullptr) narrow2<T, VEC>(dn, q, den);
+            if (NZ && want_mi) {
+                f2 v = xn;
+                if (INP && inpaint) {
+                    const f2 noised = fma2(sn2, widen2<T, VEC>(onv, q), widen2<T, VEC>(ov, q));
+                    v = fma2(m2[q], xn, mul2(omm2[q], noised));
+                }
+                narrow2<T, VEC>(mi, q, v);
+            }
+        }
+        store_raw<T, VEC>(p.x_out, gbase + k * plane, xo);
+        if (p.den_out != nullptr) store_raw<T, VEC>(p.den_out, gbase + k * plane, dn);
+        if (NZ && want_mi) store_raw<T, VEC>(p.model_in, gbase + k * plane, mi);
+    }
+}
+
+template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ>
+gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stream, unsigned flags) {
+    auto kern = guided_step_tma_kernel<T, CG, REG, INP, SKIP, NZ>;
+    static std::mutex mu;
+    static unsigned smem_set[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GS_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (smem_set[dev] < smem) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return GS_ERR_CUDA;
+            }
+            smem_set[dev] = smem;
+        }
+    }
+    if (p.B > 65535 || p.ncg > 65535) return GS_ERR_UNSUPPORTED;
+    const int gpr = threads / p.RB;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.nbands), static_cast<unsigned>(p.ncg),
+                       static_cast<unsigned>(p.B));
+    cfg.blockDim = dim3(static_cast<unsigned>(gpr), static_cast<unsigned>(p.RB));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (flags & GS_LAUNCH_PDL) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GS_ERR_CUDA;
+    }
+    return GS_OK;
+}
+
+template <typename T, bool REG, bool INP, bool SKIP, bool NZ>
+gs_status launch_cg(TmaParams& p, int cg, int threads, unsigned smem, gs_stream stream,
+                    unsigned flags) {
+    if (cg == 4) return launch_kernel<T, 4, REG, INP, SKIP, NZ>(p, threads, smem, stream, flags);
+    if (cg == 2) return launch_kernel<T, 2, REG, INP, SKIP, NZ>(p, threads, smem, stream, flags);
+    return launch_kernel<T, 1, REG, INP, SKIP, NZ>(p, threads, smem, stream, flags);
+}
+
+// NZ = false: the deterministic Euler step; read skipping (a row summary of the
+// inpaint mask) has instances of its own.  NZ = true: the sampler options, without
+// read skipping (the host clears mask_rows for them).
+template <typename T, bool NZ>
+gs_status launch_features(TmaParams& p, int cg, int threads, unsigned smem, bool reg, bool inp,
+                          gs_stream stream, unsigned flags) {
+    if constexpr (NZ) {
+        if (reg && inp) return launch_cg<T, true, true, false, true>(p, cg, threads, smem, stream, flags);
+        if (reg) return launch_cg<T, true, false, false, true>(p, cg, threads, smem, stream, flags);
+        if (inp) return launch_cg<T, false, true, false, true>(p, cg, threads, smem, stream, flags);
+        return launch_cg<T, false, false, false, true>(p, cg, threads, smem, stream, flags);
+    } else {
+        const bool skip = inp && p.mask_rows != nullptr;
+        if (reg && skip) return launch_cg<T, true, true, true, false>(p, cg, threads, smem, stream, flags);
+        if (reg && inp) return launch_cg<T, true, true, false, false>(p, cg, threads, smem, stream, flags);
+        if (reg) return launch_cg<T, true, false, false, false>(p, cg, threads, smem, stream, flags);
+        if (skip) return launch_cg<T, false, true, true, false>(p, cg, threads, smem, stream, flags);
+        if (inp) return launch_cg<T, false, true, false, false>(p, cg, threads, smem, stream, flags);
+        return launch_cg<T, false, false, false, false>(p, cg, threads, smem, stream, flags);
+    }
+}
+
+}  // namespace
+}  // namespace gs_detail

@@ -371,3 +371,32 @@ def test_model_input_follows_the_mask(dtype, shape, sampler):
     assert same_bits(mi[k:], out[k:])
     want = o[:k].to(torch.float64) + 2.0 * on[:k].to(torch.float64)
     assert close_to(mi[:k], want, dtype)
+
+
+@pytest.mark.parametrize("sampler", ["euler", "euler_ancestral"])
+def test_skipped_samples_with_regions_in_large_tiles(sampler):
+    """Samples skipped for an out-of-range step index, in a step large enough for the
+    TMA kernel's two-barrier tiles (regions, 4 channels): they stay unwritten and every
+    other sample equals the step in which all samples are valid, bit for bit."""
+    B, C, H, W = 32, 8, 64, 128
+    x, u, c, n, o, on = (rnd((B, C, H, W), s, torch.bfloat16) for s in (60, 61, 62, 63, 64, 65))
+    regs = [gs.Region(4, 8, 40, 96, 1.0, 6, rnd((B, C, 40, 96), 66, torch.bfloat16)),
+            gs.Region(20, 0, 44, 64, 0.7, 3, rnd((B, C, 44, 64), 67, torch.bfloat16))]
+    mask = (torch.rand((B, 1, H, W), generator=torch.Generator().manual_seed(68)) > 0.5)
+    kw = dict(sigmas=sig(6.0, 3.0, 1.0, 0.0), uncond=u, cond=c, regions=regs, cfg=2.5,
+              inpaint_mask=mask.float().to(DEV), original=o)
+    if sampler != "euler":
+        kw.update(sampler=sampler, noise=n)
+    good = torch.tensor([i % 3 for i in range(B)], dtype=torch.int32, device=DEV)
+    bad = good.clone()
+    bad[1::4] = -1
+    ref = torch.empty_like(x)
+    gs.guided_step(x, x_out=ref, step_idx=good, **kw)
+    out = torch.full_like(x, 5.0)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gs.guided_step(x, x_out=out, step_idx=bad, status=st, **kw)
+    torch.cuda.synchronize()
+    assert int(st.item()) == gs.GS_DEV_STEP_RANGE
+    skipped = (bad < 0).cpu()
+    assert bool((out[skipped.to(DEV)] == 5.0).all())
+    assert same_bits(out[~skipped.to(DEV)], ref[~skipped.to(DEV)])

@@ -337,20 +337,22 @@ def test_region_timestep_ranges(wl, tma):
     assert rep.n == wl.elements
 
 
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
 @pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
-def test_ancestral_full_size(wl):
+def test_ancestral_full_size(wl, tma):
     """The Euler-ancestral step (eta = 1) at each workload's full size, with the next
     model input under the inpaint wrapper where the workload inpaints."""
     rep, got, *_ = run_case(wl, sampler="euler_ancestral", model_in=wl.inpaint,
-                            want_den=True, expect_kernel="vector")
+                            want_den=True, tma=tma, expect_kernel="tma" if tma else "vector")
     assert rep.n == wl.elements and np.isfinite(got).all()
 
 
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
 @pytest.mark.parametrize("sampler", ["euler", "euler_ancestral"])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("shape,offset", [((3, 3, 13, 11), 0), ((2, 6, 7, 24), 0),
                                           ((5, 2, 16, 16), 1), ((2, 4, 37, 64), 0)])
-def test_sampler_options_ragged(dtype, shape, offset, sampler):
+def test_sampler_options_ragged(dtype, shape, offset, sampler, tma):
     """Both samplers with the model-input output on ragged shapes, on the vector and
     the scalar path (an unaligned base), with regions and a partial inpaint batch."""
     B, C, H, W = shape
@@ -359,7 +361,21 @@ def test_sampler_options_ragged(dtype, shape, offset, sampler):
                   full_frame_cond=True, n_regions=2, region_side=(1, max(1, min(H, W))),
                   feather=2, inpaint=True, inpaint_samples=max(1, B // 2), seed=18)
     run_case(wl, region_masks=True, want_den=True, sampler=sampler, model_in=True,
-             offset=offset, expect_kernel="scalar" if offset else None)
+             offset=offset, tma=tma, expect_kernel="scalar" if offset else None)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("regions", [0, 3])
+def test_sampler_options_large_tiles(dtype, regions):
+    """Both sampler options in the TMA kernel's multi-channel tiles (two barrier groups
+    with regions), with a ragged last band and half the batch blended."""
+    base = WORKLOADS[4]
+    wl = Workload("large_samplers", 48, 8, 45, 128, dtype, base.schedule, base.guidance,
+                  full_frame_cond=regions == 0, n_regions=regions, region_side=(6, 45),
+                  inpaint=True, inpaint_samples=24, seed=20)
+    rep, *_ = run_case(wl, region_masks=regions > 0, want_den=True, sampler="euler_ancestral",
+                       model_in=True, expect_kernel="tma")
+    assert rep.n == wl.elements
 
 
 def test_ancestral_close_sigmas():
