@@ -67,6 +67,9 @@ TRAFFIC = {
     # with --mask-rows (profiles/guided_step_tma__read_skipping.md)
     "inpaint_bcg_bf16_b32+mask_rows": (51107328 + 93952, "f32ead9260a322a5"),
     "sweep_bf16_b64+mask_rows": (88780800 + 3727360, "f32ead9260a322a5"),
+    # with --sampler euler_ancestral --model-in (profiles/guided_step_tma__sampler_options.md)
+    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102788864 + 8381440, "6f65b944bb542906"),
+    "sweep_bf16_b64@euler_ancestral@model_in": (151022336 + 28633344, "6f65b944bb542906"),
 }
 
 
@@ -483,6 +486,7 @@ def run_ours(args, world, rank, local):
                    "tuning": {k: os.environ[k] for k in ("GS_TMA_ROWS", "GS_TMA_CHANNELS", "GS_STEP_CHANNELS")
                               if k in os.environ},
                    "parallelism": f"replicas x{world} (independent batches)"},
+        "kernel_sources": kernel_source_hash(),
         "hbm_gbs": round(world * achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,

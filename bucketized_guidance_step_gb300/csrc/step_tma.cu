@@ -96,7 +96,10 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     //   large steps without regions: 2 channels x ~64 threads per tile (short
     //     CTA lifetimes keep the tail of the step short);
     //   large steps with regions: 4 channels x ~128 threads per tile (the
-    //     per-tile region set-up is amortised over more work).
+    //     per-tile region set-up is amortised over more work); with the next
+    //     model input (the fixed-noise box, and with the ancestral step its noise
+    //     box too) 2 channels, since the 4-channel tile's shared memory leaves
+    //     only 3 CTAs per SM.
     // GS_TMA_CHANNELS=1|2|4 and GS_TMA_ROWS override (tuning knobs; results do
     // not depend on them).
     const int gpr = W / vec;
@@ -106,7 +109,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     const bool large = units >= (1ll << 18);
     int cg = 1, target_threads = 128;
     if (large && sp.n_regions > 0) {
-        cg = 4;
+        cg = mi ? 2 : 4;
     } else if (large) {
         cg = 2;
         target_threads = 64;
