@@ -13,7 +13,7 @@ Sources.  Two web pages define what is computed:
 * [SAMPLING] "12 · 采样器、调度器与 CFG" (ComfyUI sampler, scheduler and CFG notes).
   Sections used: "sigma 序列", "denoise 小于 1", "force_full_denoise",
   "CFG 的核心", "cfg = 1 的优化", "calc_cond_batch()：最密集的条件逻辑",
-  "inpaint 与 mask", "一步采样的数据形状".
+  "为什么要自己拼 batch", "inpaint 与 mask", "一步采样的数据形状".
 * [BCG] the write-up on implementing Bucketized Continuous Guidance in SGLang
   (zwxr.cn news 258547).  Sections used: "2. BCG的核心机制拆解",
   "3. 张量并行下的bucket构造", "4. Debug完整链路" (stages 2 and 4).
@@ -28,9 +28,10 @@ Modules:
 * ``buckets``    -- bucket id of a step, curve -> bucket table, per-step scale LUT
 * ``step``       -- regional accumulation, guidance combine, inpaint blend, Euler update
 * ``mask``       -- bilinear (align_corners=False) pixel-mask -> latent-mask resize
+* ``conds``      -- areas to latent slices, packing cond entries into model calls
 
 Every function is pinned by ``tests/test_oracle_*.py`` to closed forms, the
 invariants the pages state, library routines or brute force on tiny inputs.
 """
 
-from . import buckets, mask, schedules, step  # noqa: F401
+from . import buckets, conds, mask, schedules, step  # noqa: F401
