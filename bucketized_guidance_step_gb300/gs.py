@@ -16,7 +16,7 @@ import ctypes
 import os
 import threading
 from dataclasses import dataclass
-from typing import Optional, Sequence, Tuple
+from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -36,9 +36,10 @@ GS_MAX_REGIONS = 16
 GS_LAUNCH_PDL = 1
 GS_LAUNCH_NO_TMA = 2
 GS_LAUNCH_TEST_WAIT_TIMEOUT = 4
-GS_ABI_VERSION = 3
+GS_ABI_VERSION = 4
 
 EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_guided_step",
+           "gs_areas_to_latent", "gs_pack_conds",
            "gs_step_kernel_kind", "gs_status_from_word", "gs_status_string", "gs_abi_version")
 GS_KERNEL_SCALAR, GS_KERNEL_VECTOR, GS_KERNEL_TMA = 0, 1, 2
 KERNEL_NAMES = {0: "scalar", 1: "vector", 2: "tma"}
@@ -78,6 +79,26 @@ class RegionDesc(ctypes.Structure):
                 ("mask", ctypes.c_void_p), ("mask_bstride", ctypes.c_int64),
                 ("out", ctypes.c_void_p), ("pitch", ctypes.c_int64),
                 ("t_start", ctypes.c_double), ("t_end", ctypes.c_double)]
+
+
+class Area(ctypes.Structure):
+    _fields_ = [("units", ctypes.c_int32), ("y0", ctypes.c_double), ("x0", ctypes.c_double),
+                ("h", ctypes.c_double), ("w", ctypes.c_double)]
+
+
+class Rect(ctypes.Structure):
+    _fields_ = [("y0", ctypes.c_int32), ("x0", ctypes.c_int32), ("h", ctypes.c_int32),
+                ("w", ctypes.c_int32)]
+
+
+class CondEntry(ctypes.Structure):
+    _fields_ = [("h", ctypes.c_int32), ("w", ctypes.c_int32), ("rows", ctypes.c_int32),
+                ("options", ctypes.c_int64)]
+
+
+class CondChunk(ctypes.Structure):
+    _fields_ = [("call", ctypes.c_int32), ("entry", ctypes.c_int32), ("row0", ctypes.c_int32),
+                ("rows", ctypes.c_int32)]
 
 
 class StepArgs(ctypes.Structure):
@@ -129,8 +150,13 @@ def load() -> ctypes.CDLL:
         lib.gs_status_string.argtypes = [i32]
         lib.gs_status_string.restype = ctypes.c_char_p
         lib.gs_abi_version.argtypes = []
+        lib.gs_areas_to_latent.argtypes = [ctypes.POINTER(Area), i32, i32, i32, i32,
+                                           ctypes.POINTER(Rect)]
+        lib.gs_pack_conds.argtypes = [ctypes.POINTER(CondEntry), i32, ctypes.c_int64,
+                                      ctypes.POINTER(CondChunk), i32, p, p]
         for f in ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_guided_step",
-                  "gs_step_kernel_kind", "gs_status_from_word", "gs_abi_version"):
+                  "gs_step_kernel_kind", "gs_status_from_word", "gs_abi_version",
+                  "gs_areas_to_latent", "gs_pack_conds"):
             getattr(lib, f).restype = i32
         if lib.gs_abi_version() != GS_ABI_VERSION:
             raise GSLibraryError("libgs.so ABI version does not match the binding")
@@ -176,6 +202,48 @@ def sigmas(kind: str, steps: int, *, sigma_min: float = 0.0292, sigma_max: float
     _check("gs_sigmas", lib.gs_sigmas(ctypes.byref(d), _ptr(out), out.size, ctypes.byref(n),
                                       ctypes.byref(off)))
     return out[: n.value].copy(), off.value
+
+
+AREA_UNITS = {"latent": 0, "pixels": 1, "fraction": 2}
+
+
+def areas_to_latent(areas: Sequence[Tuple[str, float, float, float, float]], H: int, W: int,
+                    scale: int = 8) -> List[Tuple[int, int, int, int]]:
+    """gs_areas_to_latent: (units, y0, x0, h, w) areas -> (y0, x0, h, w) latent slices
+    covering them, clipped to H x W ((0, 0, 0, 0) for an area that covers no pixel).
+    units: "latent", "pixels" (divided by the VAE scale) or "fraction" (of H and W)."""
+    n = len(areas)
+    arr = (Area * max(n, 1))()
+    for i, (u, y0, x0, h, w) in enumerate(areas):
+        if u not in AREA_UNITS:
+            raise ValueError(f"unknown area units {u!r}")
+        arr[i] = Area(AREA_UNITS[u], float(y0), float(x0), float(h), float(w))
+    out = (Rect * max(n, 1))()
+    _check("gs_areas_to_latent", load().gs_areas_to_latent(arr, n, int(H), int(W), int(scale),
+                                                           out))
+    return [(r.y0, r.x0, r.h, r.w) for r in out[:n]]
+
+
+def pack_conds(entries: Sequence[Tuple[int, int, int, int]], budget: int
+               ) -> Tuple[int, List[Tuple[int, int, int, int]]]:
+    """gs_pack_conds: cond entries (h, w, rows, options) -> (number of model calls,
+    chunks (call, entry, row0, rows)); budget = latent pixels per call."""
+    lib = load()
+    n = len(entries)
+    arr = (CondEntry * max(n, 1))()
+    for i, (h, w, rows, opt) in enumerate(entries):
+        arr[i] = CondEntry(int(h), int(w), int(rows), int(opt))
+    nch, ncall = ctypes.c_int32(0), ctypes.c_int32(0)
+    cap = max(n, 1)
+    while True:
+        chunks = (CondChunk * cap)()
+        st = lib.gs_pack_conds(arr, n, int(budget), chunks, cap, ctypes.byref(nch),
+                               ctypes.byref(ncall))
+        if st == GS_ERR_CAPACITY:
+            cap = nch.value
+            continue
+        _check("gs_pack_conds", st)
+        return ncall.value, [(c.call, c.entry, c.row0, c.rows) for c in chunks[:nch.value]]
 
 
 def bucket_plan(steps: int, num_buckets: int, *, curve: str = "linear", v0: float = 0.0,

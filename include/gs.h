@@ -385,6 +385,70 @@ enum { GS_KERNEL_SCALAR = 0, GS_KERNEL_VECTOR = 1, GS_KERNEL_TMA = 2 };
  */
 gs_status gs_step_kernel_kind(const gs_step_args* args, int32_t* kind);
 
+/* ---- Host helpers of the conditioning pass ------------------------------------
+ * [SAMPLING] "calc_cond_batch()": for each conditioning entry the pass turns its
+ * area (a percentage or coordinates) into a latent slice, and decides which entries
+ * can share one model call and how many to merge given the free memory; "为什么要
+ * 自己拼 batch": cond, uncond and regions batch together when shape and control
+ * options agree, and are split when memory runs short.  Both helpers are plain host
+ * code (no device memory, no stream).
+ */
+enum { GS_AREA_LATENT = 0, GS_AREA_PIXELS = 1, GS_AREA_FRACTION = 2 };
+
+typedef struct gs_area {
+    int32_t units;          /* GS_AREA_*: latent pixels, image pixels or fractions of H, W */
+    double  y0, x0, h, w;   /* top-left corner and size in those units                     */
+} gs_area;
+
+typedef struct gs_rect {
+    int32_t y0, x0, h, w;   /* a latent slice: rows y0 .. y0+h-1, columns x0 .. x0+w-1     */
+} gs_rect;
+
+/*
+ * gs_areas_to_latent -- for each of n areas, the smallest whole-pixel slice of an
+ * H x W latent that covers it, clipped to the frame.  In latent units (image pixels
+ * divided by `scale`, the VAE's downscale factor; fractions multiplied by H or W) the
+ * area covers [y0, y0+h) x [x0, x0+w); its slice is rows floor(y0) .. ceil(y0+h)-1 and
+ * columns floor(x0) .. ceil(x0+w)-1, in binary64.  An area that covers no latent
+ * pixel (outside the frame, or of zero height or width) gives h = w = 0 and
+ * y0 = x0 = 0; drop it before building gs_region entries.
+ * areas: host [n]; out: host [n] (caller-owned).  scale: used for GS_AREA_PIXELS.
+ * Errors: n < 0, a NULL array with n > 0, H or W < 1, scale < 1 with a pixel area,
+ *         a non-finite corner or size, a negative size, unknown units ->
+ *         GS_ERR_INVALID_ARG (out untouched).
+ */
+gs_status gs_areas_to_latent(const gs_area* areas, int32_t n, int32_t H, int32_t W,
+                             int32_t scale, gs_rect* out);
+
+typedef struct gs_cond_entry {
+    int32_t h, w;           /* the entry's latent shape (its model input's spatial size)   */
+    int32_t rows;           /* batch rows it needs (samples)                               */
+    int64_t options;        /* compatibility key of its control options                    */
+} gs_cond_entry;
+
+typedef struct gs_cond_chunk {
+    int32_t call;           /* model call index, in the order calls open                   */
+    int32_t entry;          /* entry index                                                 */
+    int32_t row0, rows;     /* that entry's rows row0 .. row0+rows-1                       */
+} gs_cond_chunk;
+
+/*
+ * gs_pack_conds -- pack n cond entries into model calls.  Entries share a call only
+ * when (h, w, options) are equal; a call of shape h x w holds at most
+ * max(1, floor(budget / (h*w))) rows, budget being the latent pixels per call the free
+ * memory allows.  Entries are taken in order: an entry's rows fill the last call opened
+ * for its key while it has room, then new calls of that key, each filled to capacity
+ * (so each key uses ceil(its rows / capacity) calls).  Chunks are written entry by
+ * entry in row order.
+ * entries: host [n]; chunks: host [cap]; *n_chunks, *n_calls: host, receive the counts.
+ * Errors: n < 0, NULL arrays, budget < 1, an entry with h, w or rows < 1 ->
+ *         GS_ERR_INVALID_ARG; GS_ERR_CAPACITY if more than cap chunks are needed
+ *         (*n_chunks then receives the number needed, chunks is partly written).
+ */
+gs_status gs_pack_conds(const gs_cond_entry* entries, int32_t n, int64_t budget,
+                        gs_cond_chunk* chunks, int32_t cap, int32_t* n_chunks,
+                        int32_t* n_calls);
+
 /* Decode a device status word into the first gs_status it carries (GS_OK if 0). */
 gs_status gs_status_from_word(uint32_t word);
 
@@ -392,7 +456,7 @@ gs_status gs_status_from_word(uint32_t word);
 const char* gs_status_string(gs_status status);
 
 /* ABI version of this header (bumped on any layout change). */
-#define GS_ABI_VERSION 3
+#define GS_ABI_VERSION 4
 int32_t gs_abi_version(void);
 
 #ifdef __cplusplus

@@ -147,6 +147,10 @@ int main(void) {
     printf("gs_region sizeof %zu\n", sizeof(gs_region));
     printf("gs_curve_desc sizeof %zu\n", sizeof(gs_curve_desc));
     printf("gs_schedule_desc sizeof %zu\n", sizeof(gs_schedule_desc));
+    printf("gs_area sizeof %zu\n", sizeof(gs_area));
+    printf("gs_rect sizeof %zu\n", sizeof(gs_rect));
+    printf("gs_cond_entry sizeof %zu\n", sizeof(gs_cond_entry));
+    printf("gs_cond_chunk sizeof %zu\n", sizeof(gs_cond_chunk));
     %FIELDS%
     return 0;
 }
@@ -161,7 +165,9 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     pairs = {"gs_step_args": gs.StepArgs, "gs_region": gs.RegionDesc,
-             "gs_curve_desc": gs.CurveDesc, "gs_schedule_desc": gs.ScheduleDesc}
+             "gs_curve_desc": gs.CurveDesc, "gs_schedule_desc": gs.ScheduleDesc,
+             "gs_area": gs.Area, "gs_rect": gs.Rect, "gs_cond_entry": gs.CondEntry,
+             "gs_cond_chunk": gs.CondChunk}
     fields = "\n    ".join(f"F({c}, {f})" for c, py in pairs.items() for f, _ in py._fields_)
     src = tmp_path / "layout.c"
     src.write_text(_LAYOUT_PROBE.replace("%FIELDS%", fields))
