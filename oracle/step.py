@@ -9,7 +9,10 @@ sigma_next = sig[i + 1] and guidance scale s_b:
    and mask (with feathering), and overlaps are normalised by the summed weight.
 2. Guidance combine, [SAMPLING] "CFG 的核心" and [BCG] section 3:
    pred = uncond + s * (cond - uncond).  With s = 1 the result is cond and the
-   uncond branch is not needed ([SAMPLING] "cfg = 1 的优化").
+   uncond branch is not needed ([SAMPLING] "cfg = 1 的优化").  The uncond branch is
+   built like the positive one: negative conditioning carries the same area, mask
+   and strength metadata ([SAMPLING] "negative 不是简单“反向 prompt”"), so regions
+   marked negative accumulate, with the full-frame uncond output, into it.
 3. Inpaint blend, [SAMPLING] "inpaint 与 mask": the unmasked part of the
    prediction is replaced by the original latent; the mask is broadcast over
    channels.
@@ -65,6 +68,7 @@ class Region:
     mask: Optional[np.ndarray] = None
     t_start: float = 0.0
     t_end: float = 0.0
+    negative: bool = False       # part of the uncond branch instead of the positive one
 
 
 def region_active(r: Region, i: int, steps: int) -> bool:
@@ -108,6 +112,8 @@ def positive_branch(B: int, C: int, H: int, W: int, cond=None,
                     regions: Sequence[Region] = (), active=None) -> np.ndarray:
     """Full-frame cond, or the weight-normalised sum of the regional outputs.
 
+    The uncond branch with negative regions is the same accumulation with the
+    full-frame uncond output in the place of cond.
     active: None (every region takes part) or bool [B, len(regions)]: region r
     contributes to sample b only where active[b, r]."""
     if cond is not None and not regions:
@@ -223,14 +229,21 @@ def guided_step(x, sigmas, step_idx, *, uncond=None, cond=None, cfg: float = 1.0
     sigma = sig[safe]
     sigma_next = sig[np.where(ok, safe + 1, 0)]
     ok &= sigma > 0.0
-    if uncond is None:
+    pos_idx = [k for k, r in enumerate(regions) if not r.negative]
+    neg_idx = [k for k, r in enumerate(regions) if r.negative]
+    if uncond is None and not neg_idx:
         ok &= s == 1.0
 
     steps = len(sig) - 1
     active = np.array([[region_active(r, int(safe[b]), steps) for r in regions]
                        for b in range(B)], dtype=bool).reshape(B, len(regions))
-    pos = positive_branch(B, C, H, W, cond=cond, regions=regions, active=active)
-    pred = pos if uncond is None else combine(uncond, pos, s)
+    pos = positive_branch(B, C, H, W, cond=cond, regions=[regions[k] for k in pos_idx],
+                          active=active[:, pos_idx])
+    unc = uncond
+    if neg_idx:
+        unc = positive_branch(B, C, H, W, cond=uncond, regions=[regions[k] for k in neg_idx],
+                              active=active[:, neg_idx])
+    pred = pos if unc is None else combine(unc, pos, s)
 
     den = pred
     if inpaint_mask is not None:

@@ -302,3 +302,58 @@ def test_ancestral_negative_sigma_next_is_skipped():
     assert ok.tolist() == [True, False] and np.array_equal(xa[1], x[1])
     _, _, ok = O.guided_step(x, sig, [0, 1], cond=c)
     assert ok.tolist() == [True, True]
+
+
+def _reg(y0, x0, h, w, out, strength=1.0, negative=False, **kw):
+    return O.Region(y0, x0, h, w, strength, 0, np.asarray(out, dtype=np.float64),
+                    negative=negative, **kw)
+
+
+def test_negative_regions_hand_worked():
+    """uncond [2, 2] full frame plus a negative region of 4 on the right pixel: the uncond
+    branch is [2, (2 + 4) / 2] = [2, 3]; with cond 10 and s = 2, pred = u + 2 (10 - u)."""
+    x = np.zeros((1, 1, 1, 2))
+    u = np.full((1, 1, 1, 2), 2.0)
+    c = np.full((1, 1, 1, 2), 10.0)
+    neg = _reg(0, 1, 1, 1, np.full((1, 1, 1, 1), 4.0), negative=True)
+    _, den, ok = O.guided_step(x, [1.0, 0.0], [0], uncond=u, cond=c, cfg=2.0, regions=[neg])
+    assert ok.all() and den.ravel().tolist() == [18.0, 17.0]
+    # without the full-frame uncond the left pixel's uncond is 0 (no entry covers it)
+    _, den, ok = O.guided_step(x, [1.0, 0.0], [0], cond=c, cfg=2.0, regions=[neg])
+    assert ok.all() and den.ravel().tolist() == [20.0, 16.0]
+
+
+def test_negative_full_frame_region_equals_plain_uncond():
+    B, C, H, W = 2, 3, 5, 6
+    x, u, c = rnd((B, C, H, W), 7), rnd((B, C, H, W), 8), rnd((B, C, H, W), 9)
+    pos = _reg(1, 2, 3, 3, rnd((B, C, 3, 3), 10), strength=0.7)
+    full = _reg(0, 0, H, W, u, negative=True)
+    a = O.guided_step(x, [3.0, 1.0], [0, 0], cond=c, cfg=4.0, regions=[pos, full])
+    b = O.guided_step(x, [3.0, 1.0], [0, 0], uncond=u, cond=c, cfg=4.0, regions=[pos])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_identical_branches_give_the_positive_branch_for_any_scale():
+    """When the uncond branch is built from the same entries as the positive branch,
+    pred = u + s (pos - u) = pos exactly, whatever s."""
+    B, C, H, W = 1, 2, 6, 7
+    x, c = rnd((B, C, H, W), 11), rnd((B, C, H, W), 12)
+    outs = [rnd((B, C, 4, 5), 13), rnd((B, C, 3, 6), 14)]
+    regs = [_reg(0, 0, 4, 5, outs[0], strength=0.8), _reg(3, 1, 3, 6, outs[1], strength=1.3)]
+    negs = [_reg(r.y0, r.x0, r.h, r.w, r.out, strength=r.strength, negative=True) for r in regs]
+    _, den, ok = O.guided_step(x, [2.0, 1.0], [0], uncond=c, cond=c, cfg=6.5, regions=regs + negs)
+    plain = O.positive_branch(B, C, H, W, cond=c, regions=regs)
+    assert ok.all() and np.array_equal(den, plain)
+
+
+def test_negative_regions_make_uncond_present_and_follow_ranges():
+    B, C, H, W = 2, 1, 2, 2
+    x, c = rnd((B, C, H, W), 15), rnd((B, C, H, W), 16)
+    neg = _reg(0, 0, 2, 2, rnd((B, C, 2, 2), 17), negative=True, t_start=0.0, t_end=0.5)
+    sig = np.array([4.0, 3.0, 2.0, 1.0, 0.0])
+    # step 0 (progress 0): the negative region is the uncond branch; step 2 (0.5): it is
+    # out of range and the uncond branch is 0 everywhere
+    _, den, ok = O.guided_step(x, sig, [0, 2], cond=c, cfg=3.0, regions=[neg])
+    assert ok.all()
+    np.testing.assert_array_equal(den[0], O.combine(neg.out[0:1], c[0:1], [3.0])[0])
+    np.testing.assert_array_equal(den[1], 3.0 * c[1].astype(np.float64))
