@@ -104,6 +104,8 @@ def parse_args():
     ap.add_argument("--model-in", action="store_true",
                     help="also write the next model input under the inpaint wrapper (inpaint "
                          "workloads; reads the run's fixed noise for the blended samples)")
+    ap.add_argument("--negative-regions", type=int, default=0,
+                    help="the first K regions belong to the uncond branch (regional uncond)")
     ap.add_argument("--cpu-procs", type=int, default=1,
                     help="oracle processes timed at once for cpu_baseline / --impl reference")
     return ap.parse_args()
@@ -131,6 +133,13 @@ def workload_for(args):
     if args.sampler != "euler":
         wl = dataclasses.replace(wl, sampler=args.sampler)
         name += f"@{args.sampler}"
+    if args.negative_regions > 0:
+        if args.negative_regions >= wl.n_regions and not wl.full_frame_cond:
+            raise SystemExit("--negative-regions must leave a positive region (no full-frame cond)")
+        if args.negative_regions > wl.n_regions:
+            raise SystemExit("--negative-regions exceeds the workload's regions")
+        wl = dataclasses.replace(wl, negative_regions=args.negative_regions)
+        name += f"@neg{args.negative_regions}"
     if args.model_in:
         if not wl.inpaint:
             raise SystemExit("--model-in needs an inpaint workload")
@@ -297,8 +306,9 @@ def build_sets(wl, R, dev, sig_np, lut_np, seed=0, mask_rows=False):
             st["stacked"] = branch[k]
         else:
             st["uncond"] = branch[k]
-        st["regions"] = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, slab[k])
-                         for r, slab in zip(proto.regions, slabs)]
+        st["regions"] = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, slab[k],
+                                   negative=i < wl.negative_regions)
+                         for i, (r, slab) in enumerate(zip(proto.regions, slabs))]
         if wl.inpaint:
             st["mask"] = masks[k]
             st["orig"] = origs[k]
@@ -610,7 +620,9 @@ def describe(wl) -> str:
     if wl.full_frame_cond:
         parts.append("stacked [uncond_0..B-1, cond_0..B-1]")
     if wl.n_regions:
-        parts.append(f"{wl.n_regions} regions feather {wl.feather}")
+        parts.append(f"{wl.n_regions} regions feather {wl.feather}" +
+                     (f" ({wl.negative_regions} in the uncond branch)" if wl.negative_regions
+                      else ""))
     if wl.inpaint:
         parts.append("inpaint mask+original" +
                      (f" on {wl.inpaint_samples} samples" if wl.inpaint_samples else ""))
@@ -655,7 +667,8 @@ def oracle_sample(wl, n_samples: int, seed: int = 0):
     idx = (inp.step_idx.numpy() if inp.step_idx is not None
            else np.zeros(n_samples, dtype=np.int64))
     x = sig[idx].astype(np.float64).reshape(-1, 1, 1, 1) * f64(inp.noise)
-    regs = [O.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, f64(r.out)) for r in inp.regions]
+    regs = [O.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, f64(r.out),
+                     negative=i < wl.negative_regions) for i, r in enumerate(inp.regions)]
     lat = None if inp.pixel_mask is None else OM.bilinear_resize(inp.pixel_mask.numpy(),
                                                                  wl.H, wl.W)
     kw = dict(uncond=f64(inp.uncond), cond=f64(inp.cond), scale_lut=lut,

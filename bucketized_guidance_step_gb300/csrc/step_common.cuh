@@ -26,7 +26,7 @@ struct DevRegion {
     int edges;               // kEdge* bits: edges that ramp (not on the latent border)
     int vec_ok;              // out is 16-byte aligned and pitch is a multiple of VEC
     int feather;             // F
-    int pad_;
+    int negative;            // 1: the region belongs to the uncond branch (regional uncond)
     int step_lo, step_hi;    // the region takes part at step indices step_lo <= i < step_hi
     const void* out;         // [B][C][h][pitch]
     long long pitch;
@@ -42,6 +42,7 @@ struct StepParams {
     long long groups;        // pixel groups per plane, P / VEC
     int chunks;              // C / CH
     int n_regions;
+    int has_neg;             // some region is negative (the uncond branch has regions)
     long long n_items;       // B * chunks * groups
     const void* x;
     void* x_out;

@@ -77,6 +77,9 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     const bool anc = sp.sampler == GS_SAMPLER_EULER_ANCESTRAL;
     const bool mi = sp.model_in != nullptr;
     const bool nz = anc || mi;
+    // negative regions with the sampler options run on the register kernel
+    const bool neg = sp.has_neg != 0;
+    if (neg && nz) return GS_OK;
     if (anc && !aligned16(sp.noise)) return GS_OK;
     if (mi && (!aligned16(sp.model_in) || !aligned16(sp.orig_noise))) return GS_OK;
     if (inp && (!aligned16(sp.orig) || !aligned16(sp.imask) ||
@@ -99,7 +102,9 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     //     per-tile region set-up is amortised over more work); with the next
     //     model input (the fixed-noise box, and with the ancestral step its noise
     //     box too) 2 channels, since the 4-channel tile's shared memory leaves
-    //     only 3 CTAs per SM.
+    //     only 3 CTAs per SM.  Negative regions keep 4 channels although the
+    //     second accumulator takes that tile to 128 registers a thread (4 CTAs
+    //     per SM): 2 channels measured 30 % slower on the sweep shape.
     // GS_TMA_CHANNELS=1|2|4 and GS_TMA_ROWS override (tuning knobs; results do
     // not depend on them).
     const int gpr = W / vec;
@@ -155,8 +160,8 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     p.has_c = sp.c != nullptr;
     p.mask_shared = inp && sp.imask_bstride == 0;
     p.test_wait_timeout = (flags & GS_LAUNCH_TEST_WAIT_TIMEOUT) ? 1 : 0;
-    // (the sampler-option instances do not skip reads)
-    p.mask_rows = inp && !nz ? sp.mask_rows : nullptr;
+    // (the sampler-option and negative-region instances do not skip reads)
+    p.mask_rows = inp && !nz && !neg ? sp.mask_rows : nullptr;
     p.sampler = sp.sampler;
     p.model_in = sp.model_in;
     for (int r = 0; r < sp.n_regions; ++r)
@@ -191,7 +196,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
         d.w = R.w;
         d.strength = R.strength;
         d.inv_feather = R.inv_feather;
-        d.edges = R.edges;
+        d.edges = R.edges | (R.negative ? kRegionNegative : 0);
         d.feather = R.feather;
         d.wbox = (R.w + vec - 1) / vec * vec;
         d.mask = R.mask;
@@ -248,7 +253,9 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
 
     gs_status st;
     const bool reg = sp.n_regions > 0;
-    if (nz) {
+    if (neg) {
+        st = tma_launch_neg(p, dtype, cg, threads, smem, inp, stream, flags);
+    } else if (nz) {
         st = tma_launch_sampler(p, dtype, cg, threads, smem, reg, inp, stream, flags);
     } else {
         switch (dtype) {

@@ -64,6 +64,10 @@ struct TmaRegion {
 
 static_assert(sizeof(TmaRegion) == 80, "region descriptors: 80 bytes (shared memory per CTA is tight)");
 
+// TmaRegion::edges carries, above the kEdge* bits, whether the region belongs to the
+// uncond branch (regional uncond).
+constexpr int kRegionNegative = 16;
+
 struct TmaParams {
     CUtensorMap tm_x, tm_u, tm_c, tm_o, tm_m;
     CUtensorMap tm_n, tm_on;     // the ancestral step's noise, the run's fixed noise
@@ -98,6 +102,11 @@ struct TmaParams {
 // model input); defined in step_tma_sampler.cu.
 gs_status tma_launch_sampler(TmaParams& p, int dtype, int cg, int threads, unsigned smem,
                              bool reg, bool inp, gs_stream stream, unsigned flags);
+
+// Launch the instances with negative regions (the regional uncond branch); defined
+// in step_tma_neg.cu.
+gs_status tma_launch_neg(TmaParams& p, int dtype, int cg, int threads, unsigned smem, bool inp,
+                         gs_stream stream, unsigned flags);
 
 namespace {
 
@@ -232,6 +241,30 @@ __device__ __forceinline__ void region_channels(const unsigned char* st, unsigne
     }
 }
 
+// region_channels with the tile's window shift picked at run time (once per region).
+template <typename T, int VEC, int CG>
+__device__ __forceinline__ void region_channels_sh(int sh, const unsigned char* st, unsigned rbase,
+                                                   unsigned rk, int q0, bool lo_ok, bool hi_ok,
+                                                   const f2 (&w2)[VEC / 2],
+                                                   f2 (&acc)[CG][VEC / 2]) {
+    switch (sh) {
+        case 0: region_channels<T, VEC, CG, 0>(st, rbase, rk, q0, lo_ok, hi_ok, w2, acc); break;
+        case 1: region_channels<T, VEC, CG, 1>(st, rbase, rk, q0, lo_ok, hi_ok, w2, acc); break;
+        case 2: region_channels<T, VEC, CG, 2>(st, rbase, rk, q0, lo_ok, hi_ok, w2, acc); break;
+        case 3: region_channels<T, VEC, CG, 3>(st, rbase, rk, q0, lo_ok, hi_ok, w2, acc); break;
+        default:
+            if constexpr (VEC == 8) {
+                switch (sh) {
+                    case 4: region_channels<T, VEC, CG, 4>(st, rbase, rk, q0, lo_ok, hi_ok, w2, acc); break;
+                    case 5: region_channels<T, VEC, CG, 5>(st, rbase, rk, q0, lo_ok, hi_ok, w2, acc); break;
+                    case 6: region_channels<T, VEC, CG, 6>(st, rbase, rk, q0, lo_ok, hi_ok, w2, acc); break;
+                    default: region_channels<T, VEC, CG, 7>(st, rbase, rk, q0, lo_ok, hi_ok, w2, acc); break;
+                }
+            }
+            break;
+    }
+}
+
 // ---- the kernel ---------------------------------------------------------------
 // One CTA per tile; grid (band, channel group, sample), block (pixel group, row).
 // Before the grid-dependency wait the CTA only prefetches its tensor maps and
@@ -263,19 +296,23 @@ struct TileParams {
 // x0 finds its first box vector at q0 = (x0 + qoff) / VEC (an exact division)
 // and its window sh elements into it; box row i starts at byte rbase0 + i*rrow of
 // the tile, channel k at k*rk further; column-factor entry of frame column x is
-// at byte tabx + 4x of the tile.
+// at byte tabx + 4x of the tile.  flags: bit 0 = the region has a mask, bit 1 = it
+// belongs to the uncond branch.
 struct __align__(16) TileRegion {
     int row_lo, row_hi, x_lo, x_hi;
-    int qoff, sh, nq, has_mask;
+    int qoff, sh, nq, flags;
     unsigned rbase0, rrow, rk;
     int tabx;
 };
 
-template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ>
+template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ, bool NEG>
 __global__ void __launch_bounds__(kMaxThreads)
     guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
     static_assert(INP || !SKIP, "read skipping needs the inpaint inputs");
     static_assert(!(NZ && SKIP), "the sampler options are not combined with read skipping");
+    // NEG: some regions belong to the uncond branch, which is then their weighted sum
+    // with the full-frame uncond output (weight 1, if given), like the positive branch
+    static_assert(!NEG || (REG && !SKIP && !NZ), "negative regions: region instances only");
     using S = typename T::scalar;
     constexpr int VEC = 16 / static_cast<int>(sizeof(S));
     constexpr int NP = VEC / 2;
@@ -449,7 +486,7 @@ __global__ void __launch_bounds__(kMaxThreads)
         // (the ancestral split takes sigma_next as a standard deviation: >= 0)
         const bool sigma_ok =
             sigma > 0.0f && sigma <= 3.402823466e38f && (!anc || sigma_next >= 0.0f);
-        const bool uncond_ok = has_u || sv == 1.0f;
+        const bool uncond_ok = has_u || NEG || sv == 1.0f;
         tp.s = sv;
         tp.one_minus_s = 1.0f - sv;
         float ratio = __fdiv_rn(sigma_next, sigma), up = 0.0f;
@@ -496,7 +533,7 @@ __global__ void __launch_bounds__(kMaxThreads)
                 t.sh = (VEC - R.x0 % VEC) % VEC;
                 t.qoff = -R.x0 - t.sh;
                 t.nq = R.wbox / VEC;
-                t.has_mask = R.mask != nullptr ? 1 : 0;
+                t.flags = (R.mask != nullptr ? 1 : 0) | ((R.edges & kRegionNegative) ? 2 : 0);
                 t.rbase0 = R.smem_off;
                 t.rrow = static_cast<unsigned>(R.wbox) * sizeof(S);
                 t.rk = static_cast<unsigned>(p.RB) * R.wbox * sizeof(S);
@@ -598,6 +635,23 @@ __global__ void __launch_bounds__(kMaxThreads)
             f2 wsum2[NP];
 #pragma unroll
             for (int q = 0; q < NP; ++q) wsum2[q] = splat2(has_c ? 1.0f : 0.0f);
+            // the uncond branch's sum (NEG): the full-frame uncond joins with weight 1
+            f2 negacc[CG][NP], wsn2[NP];                  // (unused without NEG)
+            if constexpr (NEG) {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) wsn2[q] = splat2(has_u ? 1.0f : 0.0f);
+#pragma unroll
+                for (int k = 0; k < CG; ++k) {
+                    if (has_u) {
+                        const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+#pragma unroll
+                        for (int q = 0; q < NP; ++q) negacc[k][q] = widen2<T, VEC>(v, q);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < NP; ++q) negacc[k][q] = splat2(0.0f);
+                    }
+                }
+            }
 #pragma unroll
             for (int k = 0; k < CG; ++k) {
                 if (has_c) {
@@ -623,7 +677,7 @@ __global__ void __launch_bounds__(kMaxThreads)
                     w2[2 * q] = mul2(wr2, mk2(c4.x, c4.y));
                     w2[2 * q + 1] = mul2(wr2, mk2(c4.z, c4.w));
                 }
-                if (tr.has_mask) {
+                if (tr.flags & 1) {
                     const TmaRegion& R = regs[r];
                     const int ty = y - R.y0;
                     const int xs = x0 - R.x0;
@@ -640,8 +694,6 @@ __global__ void __launch_bounds__(kMaxThreads)
 #pragma unroll
                     for (int q = 0; q < NP; ++q) w2[q] = mk2(wj[2 * q], wj[2 * q + 1]);
                 }
-#pragma unroll
-                for (int q = 0; q < NP; ++q) wsum2[q] = add2(wsum2[q], w2[q]);
                 // Box row `row` of this region's tile is frame row y.  Columns outside
                 // [0, w) are zeros (TMA fills the box past the slab's width, and
                 // vectors outside the box are not read), so no pixel outside the
@@ -652,21 +704,14 @@ __global__ void __launch_bounds__(kMaxThreads)
                 const bool hi_ok = q0 + 1 >= 0 && q0 + 1 < tr.nq;
                 const unsigned rbase = tr.rbase0 + static_cast<unsigned>(row) * tr.rrow;
                 const unsigned rk = tr.rk;
-                switch (sh) {
-                    case 0: region_channels<T, VEC, CG, 0>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                    case 1: region_channels<T, VEC, CG, 1>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                    case 2: region_channels<T, VEC, CG, 2>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                    case 3: region_channels<T, VEC, CG, 3>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                    default:
-                        if constexpr (VEC == 8) {
-                            switch (sh) {
-                                case 4: region_channels<T, VEC, CG, 4>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                                case 5: region_channels<T, VEC, CG, 5>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                                case 6: region_channels<T, VEC, CG, 6>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                                default: region_channels<T, VEC, CG, 7>(st, rbase, rk, q0, lo_ok, hi_ok, w2, pos); break;
-                            }
-                        }
-                        break;
+                if (NEG && (tr.flags & 2)) {
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) wsn2[q] = add2(wsn2[q], w2[q]);
+                    region_channels_sh<T, VEC, CG>(sh, st, rbase, rk, q0, lo_ok, hi_ok, w2, negacc);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) wsum2[q] = add2(wsum2[q], w2[q]);
+                    region_channels_sh<T, VEC, CG>(sh, st, rbase, rk, q0, lo_ok, hi_ok, w2, pos);
                 }
             }
 #pragma unroll
@@ -674,6 +719,16 @@ __global__ void __launch_bounds__(kMaxThreads)
                 const f2 inv = recip_or_zero2(wsum2[q]);
 #pragma unroll
                 for (int k = 0; k < CG; ++k) pos[k][q] = mul2(pos[k][q], inv);
+            }
+            if constexpr (NEG) {
+                // normalise the uncond branch and combine: pred = s pos + (1 - s) uncond
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const f2 inv = recip_or_zero2(wsn2[q]);
+#pragma unroll
+                    for (int k = 0; k < CG; ++k)
+                        pos[k][q] = fma2(s2, pos[k][q], mul2(oms2, mul2(negacc[k][q], inv)));
+                }
             }
         }
     } else {
@@ -686,8 +741,8 @@ __global__ void __launch_bounds__(kMaxThreads)
     }
 
     if constexpr (kSplit) {
-        // combine while group B lands, then wait for it
-        if (active && has_u) {
+        // combine while group B lands, then wait for it (NEG: combined above)
+        if (!NEG && active && has_u) {
 #pragma unroll
             for (int k = 0; k < CG; ++k) {
                 const Raw<T, VEC> uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
@@ -726,14 +781,14 @@ __global__ void __launch_bounds__(kMaxThreads)
     for (int k = 0; k < CG; ++k) {
         const Raw<T, VEC> xv = ld_smem<T, VEC>(st + p.off_x, k * kstride + pix);
         Raw<T, VEC> uv, ov, nv, onv, xo, dn, mi;
-        if (!kSplit && has_u) uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+        if (!NEG && !kSplit && has_u) uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
         if (INP && inpaint) ov = ld_smem<T, VEC>(st + p.off_o, k * kstride + pix);
         if (NZ && anc) nv = ld_smem<T, VEC>(st + p.off_n, k * kstride + pix);
         if (NZ && INP && want_mi && inpaint) onv = ld_smem<T, VEC>(st + p.off_on, k * kstride + pix);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             f2 pred = pos[k][q];
-            if (!kSplit && has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(uv, q)));
+            if (!NEG && !kSplit && has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(uv, q)));
             f2 den = pred;
             if (INP && inpaint) den = fma2(m2[q], pred, mul2(omm2[q], widen2<T, VEC>(ov, q)));
             f2 xn = fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den);
@@ -755,9 +810,9 @@ __global__ void __launch_bounds__(kMaxThreads)
     }
 }
 
-template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ>
+template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ, bool NEG = false>
 gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stream, unsigned flags) {
-    auto kern = guided_step_tma_kernel<T, CG, REG, INP, SKIP, NZ>;
+    auto kern = guided_step_tma_kernel<T, CG, REG, INP, SKIP, NZ, NEG>;
     static std::mutex mu;
     static unsigned smem_set[64] = {0};
     int dev = 0;
@@ -795,12 +850,21 @@ gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stre
     return GS_OK;
 }
 
-template <typename T, bool REG, bool INP, bool SKIP, bool NZ>
+template <typename T, bool REG, bool INP, bool SKIP, bool NZ, bool NEG = false>
 gs_status launch_cg(TmaParams& p, int cg, int threads, unsigned smem, gs_stream stream,
                     unsigned flags) {
-    if (cg == 4) return launch_kernel<T, 4, REG, INP, SKIP, NZ>(p, threads, smem, stream, flags);
-    if (cg == 2) return launch_kernel<T, 2, REG, INP, SKIP, NZ>(p, threads, smem, stream, flags);
-    return launch_kernel<T, 1, REG, INP, SKIP, NZ>(p, threads, smem, stream, flags);
+    if (cg == 4) return launch_kernel<T, 4, REG, INP, SKIP, NZ, NEG>(p, threads, smem, stream, flags);
+    if (cg == 2) return launch_kernel<T, 2, REG, INP, SKIP, NZ, NEG>(p, threads, smem, stream, flags);
+    return launch_kernel<T, 1, REG, INP, SKIP, NZ, NEG>(p, threads, smem, stream, flags);
+}
+
+// Negative regions (the regional uncond branch): region instances without read
+// skipping or sampler options (the host sends those requests to the register kernel).
+template <typename T>
+gs_status launch_features_neg(TmaParams& p, int cg, int threads, unsigned smem, bool inp,
+                              gs_stream stream, unsigned flags) {
+    if (inp) return launch_cg<T, true, true, false, false, true>(p, cg, threads, smem, stream, flags);
+    return launch_cg<T, true, false, false, false, true>(p, cg, threads, smem, stream, flags);
 }
 
 // NZ = false: the deterministic Euler step; read skipping (a row summary of the

@@ -36,7 +36,7 @@ GS_MAX_REGIONS = 16
 GS_LAUNCH_PDL = 1
 GS_LAUNCH_NO_TMA = 2
 GS_LAUNCH_TEST_WAIT_TIMEOUT = 4
-GS_ABI_VERSION = 4
+GS_ABI_VERSION = 5
 
 EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_guided_step",
            "gs_areas_to_latent", "gs_pack_conds",
@@ -78,7 +78,8 @@ class RegionDesc(ctypes.Structure):
                 ("w", ctypes.c_int32), ("strength", ctypes.c_float), ("feather", ctypes.c_int32),
                 ("mask", ctypes.c_void_p), ("mask_bstride", ctypes.c_int64),
                 ("out", ctypes.c_void_p), ("pitch", ctypes.c_int64),
-                ("t_start", ctypes.c_double), ("t_end", ctypes.c_double)]
+                ("t_start", ctypes.c_double), ("t_end", ctypes.c_double),
+                ("negative", ctypes.c_int32)]
 
 
 class Area(ctypes.Structure):
@@ -338,6 +339,7 @@ class Region:
     pitch: Optional[int] = None       # defaults to out.shape[-1]
     t_start: float = 0.0              # timestep range [t_start, t_end) in progress i/S;
     t_end: float = 0.0                # t_end <= t_start: every step
+    negative: bool = False            # part of the uncond branch (regional uncond)
 
 
 _DT = {}
@@ -400,7 +402,7 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
         reg_arr[i] = RegionDesc(int(r.y0), int(r.x0), int(r.h), int(r.w), float(r.strength),
                                 int(r.feather), _dptr(r.mask, "region mask", torch.float32),
                                 mstride, _dptr(r.out, "region out", dt), pitch,
-                                float(r.t_start), float(r.t_end))
+                                float(r.t_start), float(r.t_end), int(bool(r.negative)))
     mstride = 0
     if inpaint_mask is not None:
         mstride = 0 if inpaint_mask.shape[0] == 1 else H * W

@@ -86,6 +86,7 @@ class Workload:
     seed: int = 0
     sampler: str = "euler"                   # "euler" | "euler_ancestral" (fresh noise per step)
     model_input: bool = False                # also the next model input (inpaint wrapper)
+    negative_regions: int = 0                # the first k regions belong to the uncond branch
 
     @property
     def elements(self) -> int:

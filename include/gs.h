@@ -219,6 +219,14 @@ gs_status gs_mask_rows(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
  *            i = the sample's step index, S = n_sigmas - 1, evaluated in binary64
  *            (the progress the guidance buckets use).  t_end <= t_start (a zeroed
  *            struct) means no range: every step.
+ *   negative: 0 = the region is part of the positive (cond) branch; 1 = of the
+ *            uncond branch (regional uncond: negative conditioning carries the same
+ *            area, mask and strength metadata, [SAMPLING] "negative 不是简单“反向
+ *            prompt”").  Each branch is the weight-normalised sum of its entries:
+ *            the full-frame output (cond or uncond, weight 1, if given) and its
+ *            regions; a pixel no entry of a branch covers gets 0 in that branch.
+ *            The positive branch needs cond or a positive region.  Other values are
+ *            GS_ERR_INVALID_ARG.
  */
 typedef struct gs_region {
     int32_t     y0, x0, h, w;
@@ -229,6 +237,7 @@ typedef struct gs_region {
     const void* out;
     int64_t     pitch;
     double      t_start, t_end;
+    int32_t     negative;
 } gs_region;
 
 /* samplers (gs_step_args.sampler) */
@@ -456,7 +465,7 @@ gs_status gs_status_from_word(uint32_t word);
 const char* gs_status_string(gs_status status);
 
 /* ABI version of this header (bumped on any layout change). */
-#define GS_ABI_VERSION 4
+#define GS_ABI_VERSION 5
 int32_t gs_abi_version(void);
 
 #ifdef __cplusplus

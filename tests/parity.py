@@ -10,7 +10,9 @@ the quantity it rounds, and one hardware reciprocal of the summed region weight
 bounded by the error scale
 
     M = |r| (|x| + Mden) + Mden,   Mden = m Mpred + (1 - m) |orig|,
-    Mpred = |1 - s| |u| + |s| Mpos,   Mpos = (|c| + sum_r w_r |out_r|) / W,
+    Mpred = |1 - s| Mu + |s| Mpos,   Mpos = (|c| + sum_r w_r |out_r|) / W,
+
+Mu is |u|, or with negative regions (|u| + sum_neg w_r |out_r|) / W_neg,
 
 with r = sigma_next / sigma.  Hence |g32 - ref| <= k 2^-24 M with
 k = n_regions + 16.  An element passes when
@@ -77,27 +79,35 @@ def oracle_latent_mask(pixel_mask, H: int, W: int) -> np.ndarray:
     return OM.bilinear_resize(pixel_mask.numpy(), H, W).astype(np.float32)
 
 
+def _branch_scale(full, regions, B, H, W, like) -> np.ndarray:
+    """(|full| + sum_r w_r |out_r|) / (1 + sum_r w_r): the magnitude scale of one branch."""
+    acc = np.zeros_like(like)
+    wsum = np.zeros((B, 1, H, W))
+    if full is not None:
+        acc += np.abs(full)
+        wsum += 1.0
+    for reg in regions:
+        w = O.region_weight(reg, B, H, W)
+        sl = (slice(None), slice(None), slice(reg.y0, reg.y0 + reg.h),
+              slice(reg.x0, reg.x0 + reg.w))
+        acc[sl] += w * np.abs(np.asarray(reg.out, dtype=np.float64)[:, :, :, :reg.w])
+        wsum[sl] += w
+    return np.where(wsum > 0, acc / np.where(wsum > 0, wsum, 1.0), 0.0)
+
+
 def error_scale(x, u, c, regions, s, r, m, present, orig, H, W) -> np.ndarray:
-    """Elementwise M of the module docstring (float64 numpy inputs)."""
+    """Elementwise M of the module docstring (float64 numpy inputs).  Regions marked
+    negative build the uncond branch's scale the way the others build Mpos."""
     B = x.shape[0]
-    C = x.shape[1]
-    if regions:
-        acc = np.zeros_like(x)
-        wsum = np.zeros((B, 1, H, W))
-        if c is not None:
-            acc += np.abs(c)
-            wsum += 1.0
-        for reg in regions:
-            w = O.region_weight(reg, B, H, W)
-            sl = (slice(None), slice(None), slice(reg.y0, reg.y0 + reg.h),
-                  slice(reg.x0, reg.x0 + reg.w))
-            acc[sl] += w * np.abs(np.asarray(reg.out, dtype=np.float64)[:, :, :, :reg.w])
-            wsum[sl] += w
-        mpos = np.where(wsum > 0, acc / np.where(wsum > 0, wsum, 1.0), 0.0)
+    pos_regs = [g for g in regions if not getattr(g, "negative", False)]
+    neg_regs = [g for g in regions if getattr(g, "negative", False)]
+    mpos = _branch_scale(c, pos_regs, B, H, W, x) if pos_regs else np.abs(c)
+    if neg_regs:
+        mu = _branch_scale(u, neg_regs, B, H, W, x)
     else:
-        mpos = np.abs(c)
+        mu = None if u is None else np.abs(u)
     s4 = np.asarray(s, dtype=np.float64).reshape(B, 1, 1, 1)
-    mpred = np.abs(s4) * mpos if u is None else np.abs(1 - s4) * np.abs(u) + np.abs(s4) * mpos
+    mpred = np.abs(s4) * mpos if mu is None else np.abs(1 - s4) * mu + np.abs(s4) * mpos
     mden = mpred
     if m is not None:
         mm = np.broadcast_to(m, (B, 1, H, W))

@@ -183,3 +183,19 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
         assert got[(c, "sizeof")] == ctypes.sizeof(py), c
         for f, _ in py._fields_:
             assert got[(c, f)] == getattr(py, f).offset, (c, f)
+
+
+def test_step_rejects_bad_negative_regions(lib):
+    # a negative flag other than 0 / 1
+    a = _valid_args()
+    arr = (gs.RegionDesc * 1)(gs.RegionDesc(0, 0, 2, 4, 1.0, 0, None, 0, 0x4000, 4, 0.0, 0.0, 2))
+    a.n_regions = 1
+    a.regions = ctypes.cast(arr, ctypes.POINTER(gs.RegionDesc))
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+    # only negative regions and no full-frame cond: the positive branch is empty
+    a = _valid_args()
+    a.cond = 0
+    arr = (gs.RegionDesc * 1)(gs.RegionDesc(0, 0, 2, 4, 1.0, 0, None, 0, 0x4000, 4, 0.0, 0.0, 1))
+    a.n_regions = 1
+    a.regions = ctypes.cast(arr, ctypes.POINTER(gs.RegionDesc))
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG

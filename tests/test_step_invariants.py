@@ -90,6 +90,21 @@ def test_full_frame_region_equals_plain_cond(dtype, shape):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", SHAPES)
+def test_full_frame_negative_region_equals_plain_uncond(dtype, shape):
+    """Regional uncond: one full-frame negative region of strength 1 (no full-frame
+    uncond output) is the plain uncond branch, bit for bit."""
+    B, C, H, W = shape
+    x, u, c = (rnd(shape, s, dtype) for s in (70, 71, 72))
+    a, b = torch.empty_like(x), torch.empty_like(x)
+    gs.guided_step(x, sigmas=sig(5.0, 2.0), uncond=u, cond=c, cfg=6.0, x_out=a)
+    reg = gs.Region(0, 0, H, W, 1.0, 8, u, negative=True)
+    gs.guided_step(x, sigmas=sig(5.0, 2.0), cond=c, regions=[reg], cfg=6.0, x_out=b)
+    torch.cuda.synchronize()
+    assert same_bits(a, b)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", SHAPES)
 def test_inpaint_all_ones_and_all_zeros(dtype, shape):
     B, C, H, W = shape
     x, u, c, o = (rnd(shape, s, dtype) for s in (10, 11, 12, 13))

@@ -35,7 +35,7 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
              uncond_none: bool = False, want_den: bool = False, pitch_align: int = 8,
              tma: bool = True, expect_kernel: str = None, mask_rows: bool = False,
              poison: bool = False, region_ranges=None, sampler: str = "euler",
-             model_in: bool = False, sigmas=None):
+             model_in: bool = False, sigmas=None, negative=()):
     """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok).
 
     mask_rows: pass the row summary of the latent mask (gs_mask_rows), so that bands
@@ -47,7 +47,8 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     to both sides.  sampler: "euler" or "euler_ancestral" (fresh seeded noise, the
     same on both sides).  model_in: also produce the next model input under the
     inpaint wrapper (needs an inpaint workload) and gate it against the oracle's.
-    sigmas: a schedule (float32) in place of the workload's.
+    sigmas: a schedule (float32) in place of the workload's.  negative: indices of
+    regions that belong to the uncond branch (on both sides).
     """
     if sampler != wl.sampler or model_in != wl.model_input:
         wl = dataclasses.replace(wl, sampler=sampler, model_input=model_in)
@@ -112,8 +113,8 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     dend = dev_latent(torch.full_like(x, float("nan"))) if want_den else None
     ranges = region_ranges or [(0.0, 0.0)] * len(inp.regions)
     regs = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, _cuda(o), _cuda(r.mask),
-                      t_start=t0, t_end=t1)
-            for r, o, (t0, t1) in zip(inp.regions, reg_outs, ranges)]
+                      t_start=t0, t_end=t1, negative=i in negative)
+            for i, (r, o, (t0, t1)) in enumerate(zip(inp.regions, reg_outs, ranges))]
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     kw = dict(uncond=dev_latent(u_gpu), cond=dev_latent(c_gpu), regions=regs,
               sigmas=torch.from_numpy(sig).to(DEV), x_out=outd, denoised_out=dend,
@@ -151,8 +152,8 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     # --- oracle ---
     oregs = [O.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, to64(r.out),
                       None if r.mask is None else r.mask.numpy().astype(np.float64),
-                      t_start=t0, t_end=t1)
-             for r, (t0, t1) in zip(inp.regions, ranges)]
+                      t_start=t0, t_end=t1, negative=i in negative)
+             for i, (r, (t0, t1)) in enumerate(zip(inp.regions, ranges))]
     present = (np.ones(Bn, bool) if inp.mask_present is None
                else inp.mask_present.numpy().astype(bool))
     ref, den, ok = O.guided_step(to64(x), sig, idx, uncond=to64(u), cond=to64(inp.cond), cfg=cfg,
@@ -389,3 +390,47 @@ def test_ancestral_close_sigmas():
     assert set(step_inputs(wl).step_idx.tolist()) == set(range(5))
     rep, *_ = run_case(wl, sampler="euler_ancestral", sigmas=sig)
     assert rep.normwise <= 1e-5
+
+
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
+@pytest.mark.parametrize("uncond", [True, False], ids=["with_uncond", "regions_only"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_negative_regions_full_sweep_shape(dtype, uncond, tma):
+    """Regional uncond on the sweep shape (B = 64, 16 x 128 x 128): two of four regions
+    belong to the uncond branch, with or without the full-frame uncond output, half the
+    batch blended, region masks."""
+    base = WORKLOADS[4]
+    wl = Workload("negative", 64, 16, 128, 128, dtype, base.schedule, base.guidance,
+                  full_frame_cond=False, n_regions=4, inpaint=True, inpaint_samples=32,
+                  seed=21)
+    rep, *_ = run_case(wl, region_masks=True, negative=(0, 2), uncond_none=not uncond,
+                       want_den=True, tma=tma, expect_kernel="tma" if tma else "vector")
+    assert rep.n == wl.elements
+
+
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+@pytest.mark.parametrize("shape,offset", [((3, 3, 13, 11), 0), ((2, 6, 7, 24), 0),
+                                          ((5, 2, 16, 16), 1), ((2, 4, 37, 64), 0),
+                                          ((24, 8, 70, 64), 0)])
+def test_negative_regions_ragged(dtype, shape, offset, tma):
+    """Negative regions on ragged shapes, the scalar path and small-step tiles, with a
+    full-frame cond and uncond, feathers and masks."""
+    B, C, H, W = shape
+    base = WORKLOADS[4]
+    wl = Workload("neg_ragged", B, C, H, W, dtype, base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=4, region_side=(1, max(1, min(H, W))),
+                  feather=2, inpaint=True, inpaint_samples=max(1, B // 2), seed=22)
+    run_case(wl, region_masks=True, want_den=True, negative=(1, 3), offset=offset, tma=tma,
+             expect_kernel="scalar" if offset else None)
+
+
+def test_negative_regions_with_sampler_options():
+    """Negative regions together with the ancestral step and the model input (the
+    register kernel serves this combination)."""
+    base = WORKLOADS[4]
+    wl = Workload("neg_anc", 16, 8, 64, 64, "bf16", base.schedule, base.guidance,
+                  full_frame_cond=False, n_regions=3, inpaint=True, inpaint_samples=8, seed=23)
+    rep, *_ = run_case(wl, negative=(1,), sampler="euler_ancestral", model_in=True,
+                       expect_kernel="vector")
+    assert rep.n == wl.elements
