@@ -434,3 +434,46 @@ def test_negative_regions_with_sampler_options():
     rep, *_ = run_case(wl, negative=(1,), sampler="euler_ancestral", model_in=True,
                        expect_kernel="vector")
     assert rep.n == wl.elements
+
+
+def _combo(seed):
+    """A random feature combination on a small shape (deterministic in seed)."""
+    import random
+    rng = random.Random(1000 + seed)
+    dtype = rng.choice(["fp32", "bf16", "fp16"])
+    B, C = rng.randint(1, 6), rng.randint(1, 6)
+    H = rng.randint(1, 40)
+    W = rng.choice([8, 16, 24, 40, 64, 128, rng.randint(1, 70)])
+    n_regions = rng.randint(0, 4)
+    full_cond = n_regions == 0 or rng.random() < 0.5
+    negative = tuple(i for i in range(n_regions) if rng.random() < 0.4)
+    if not full_cond and len(negative) == n_regions:
+        negative = negative[1:]                  # keep a positive entry
+    inpaint = rng.random() < 0.6
+    base = WORKLOADS[4]
+    wl = Workload(f"combo{seed}", B, C, H, W, dtype, base.schedule, base.guidance,
+                  full_frame_cond=full_cond, n_regions=n_regions,
+                  region_side=(1, max(1, min(H, W))), feather=rng.choice([0, 2, 5]),
+                  inpaint=inpaint, inpaint_samples=rng.randint(1, B) if inpaint else None,
+                  seed=100 + seed)
+    ranges = None
+    if n_regions and rng.random() < 0.4:
+        ranges = [rng.choice([(0.0, 0.0), (0.0, 0.5), (0.3, 1.0)]) for _ in range(n_regions)]
+    kw = dict(region_masks=n_regions > 0 and rng.random() < 0.5, want_den=rng.random() < 0.5,
+              negative=negative, region_ranges=ranges,
+              sampler=rng.choice(["euler", "euler_ancestral"]),
+              model_in=inpaint and rng.random() < 0.5,
+              mask_rows=inpaint and rng.random() < 0.5,
+              uncond_none=bool(negative) and rng.random() < 0.3,
+              offset=1 if rng.random() < 0.15 else 0, step=rng.randint(0, 49))
+    return wl, kw
+
+
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
+@pytest.mark.parametrize("seed", range(40))
+def test_feature_combinations(seed, tma):
+    """Random combinations of every option (dtype, ragged shape, regions with masks,
+    feathers, timestep ranges and negative regions, inpaint with partial presence and the
+    row summary, both samplers, the model input, unaligned bases) against the oracle."""
+    wl, kw = _combo(seed)
+    run_case(wl, tma=tma, **kw)
