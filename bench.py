@@ -58,18 +58,20 @@ FALLBACK_HBM_GBS = 6800.0
 # capture, with the SHA-256 prefix of the kernel source it was taken on.  A
 # different source hash means the counters are stale: traffic is reported null.
 TRAFFIC = {
-    # profiles/guided_step_tma__bcg_bf16_b16.md: dram read 6,302,720 B + write 0 B
-    "bcg_bf16_b16": (6302720, "f32ead9260a322a5"),
+    # profiles/guided_step_tma__bcg_bf16_b16.md
+    "bcg_bf16_b16": (6303488, "a241fc25be2c1c81"),
     # profiles/guided_step_tma__large_steps.md
-    "area_fp16_b8": (2958336, "f32ead9260a322a5"),
-    "inpaint_bcg_bf16_b32": (69223680 + 834560, "f32ead9260a322a5"),
-    "sweep_bf16_b64": (100662272 + 4908032, "f32ead9260a322a5"),
+    "area_fp16_b8": (2959616, "a241fc25be2c1c81"),
+    "inpaint_bcg_bf16_b32": (69225472 + 568320, "a241fc25be2c1c81"),
+    "sweep_bf16_b64": (100663808 + 4732160, "a241fc25be2c1c81"),
     # with --mask-rows (profiles/guided_step_tma__read_skipping.md)
-    "inpaint_bcg_bf16_b32+mask_rows": (51107328 + 93952, "f32ead9260a322a5"),
-    "sweep_bf16_b64+mask_rows": (88780800 + 3727360, "f32ead9260a322a5"),
-    # with --sampler euler_ancestral --model-in (profiles/guided_step_tma__sampler_options.md)
-    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102788864 + 8381440, "6f65b944bb542906"),
-    "sweep_bf16_b64@euler_ancestral@model_in": (151022336 + 28633344, "6f65b944bb542906"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51108608 + 44288, "a241fc25be2c1c81"),
+    "sweep_bf16_b64+mask_rows": (88782080 + 3069440, "a241fc25be2c1c81"),
+    # sampler options and negative regions (profiles/guided_step_tma__sampler_options.md)
+    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102789888 + 7572992, "a241fc25be2c1c81"),
+    "sweep_bf16_b64@euler_ancestral@model_in": (151018752 + 27539968, "a241fc25be2c1c81"),
+    "sweep_bf16_b64@euler_ancestral": (134242816 + 10234880, "a241fc25be2c1c81"),
+    "sweep_bf16_b64@neg1": (100677632 + 5143808, "a241fc25be2c1c81"),
 }
 
 
