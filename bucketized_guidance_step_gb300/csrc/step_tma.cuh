@@ -325,6 +325,11 @@ __global__ void __launch_bounds__(kMaxThreads)
     // whole step is one wave of CTAs and latency-bound) keep a single barrier: there
     // the second wait costs more than the overlap gains.
     constexpr bool kSplit = REG && CG > 1;
+    // Without regions no warp builds tables the others need, so every thread waits
+    // on the tile's mbarrier itself (its phase completion also publishes the step
+    // parameters, which the parameter thread writes before it arrives) instead of
+    // thread 0 waiting and releasing the CTA through a hardware barrier.
+    constexpr bool kAllWait = !REG;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
         tp.inpaint = present ? 1 : 0;
         if constexpr (defer) tp.need_pred = need_pred ? 1 : 0;
-        if (ptid != 0) mbar_arrive(barB);
+        if (!kAllWait && ptid != 0) mbar_arrive(barB);
         const bool in_range =
             idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
         const int si = in_range ? idx : 0;
@@ -502,6 +507,8 @@ __global__ void __launch_bounds__(kMaxThreads)
             if (in_range && !uncond_ok) bits |= GS_DEV_NEED_UNCOND;
             flag(p.status, bits);
         }
+        // (release: the waiters' acquire on the phase makes tp visible to them)
+        if (kAllWait && ptid != 0) mbar_arrive(barB);
     }
 
     if constexpr (REG) {
@@ -560,6 +567,18 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
     }
 
+    if constexpr (kAllWait) {
+        if (tid == 0) {
+            if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+            mbar_arrive(barB);
+        }
+        // ---- every thread waits for the boxes (suspended in hardware) ----
+        if (!mbar_wait(bar, 0)) {
+            flag(p.status, GS_DEV_TIMEOUT);
+            return;
+        }
+        if (tp.ok != 1) return;
+    } else {
     if (tid == 0) {
         tp.arrived = 1;
         if constexpr (!kSplit) {
@@ -583,6 +602,7 @@ __global__ void __launch_bounds__(kMaxThreads)
             if (tid == 0 && tp.arrived == 1 && !mbar_wait(barB, 0)) flag(p.status, GS_DEV_TIMEOUT);
         }
         return;
+    }
     }
     // rows past H (a ragged last band): no arithmetic, but with regions they still
     // take part in the second CTA barrier
