@@ -285,8 +285,8 @@ struct TileParams {
     float up, sigma_next;          // sigma_up (ancestral), sigma_next (model input)
     int ok;             // 1 = step this sample, 0 = skip it
     int inpaint;        // 1 = this sample blends with its original
-    int arrived;        // 0 = the wait for the tile gave up
     int need_pred;      // 0 = the band's mask rows are all zero: prediction not read
+    int arrived;        // 0 = thread 0's wait for the tile gave up (one-group region tiles)
 };
 
 // One region as this tile's threads use it, built once per CTA by the region's
@@ -325,11 +325,16 @@ __global__ void __launch_bounds__(kMaxThreads)
     // whole step is one wave of CTAs and latency-bound) keep a single barrier: there
     // the second wait costs more than the overlap gains.
     constexpr bool kSplit = REG && CG > 1;
-    // Without regions no warp builds tables the others need, so every thread waits
-    // on the tile's mbarrier itself (its phase completion also publishes the step
-    // parameters, which the parameter thread writes before it arrives) instead of
-    // thread 0 waiting and releasing the CTA through a hardware barrier.
+    // Tiles without regions, and two-group tiles: every thread waits on the tile's
+    // mbarriers itself (suspended in hardware) instead of thread 0 waiting and
+    // releasing the CTA through a hardware barrier.  Without regions the phase
+    // completion also publishes the step parameters, which the parameter thread then
+    // writes before it arrives; with regions one CTA barrier before the first wait
+    // publishes them together with the region tables.  One-group tiles with regions
+    // (the small-step shape) keep thread 0's wait: there the per-thread waits measured
+    // 1 % slower (area step 3.79 against 3.76 us; sweep step 24.41 against 24.83 us).
     constexpr bool kAllWait = !REG;
+    constexpr bool kThreadWaits = !REG || kSplit;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -567,60 +572,58 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
     }
 
-    if constexpr (kAllWait) {
+    if constexpr (kThreadWaits) {
         if (tid == 0) {
-            if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+            if constexpr (!kSplit) {
+                if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+            }
             mbar_arrive(barB);
         }
-        // ---- every thread waits for the boxes (suspended in hardware) ----
+        if constexpr (REG) __syncthreads();       // region tables and step parameters
+        // ---- every thread waits for the boxes ----
         if (!mbar_wait(bar, 0)) {
             flag(p.status, GS_DEV_TIMEOUT);
-            return;
-        }
-        if (tp.ok != 1) return;
-    } else {
-    if (tid == 0) {
-        tp.arrived = 1;
-        if constexpr (!kSplit) {
-            if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
-        }
-        mbar_arrive(barB);
-        // ---- wait for the boxes (the rest of the CTA sleeps at the barrier) ----
-        if (!mbar_wait(bar, 0)) {
-            flag(p.status, GS_DEV_TIMEOUT);
-            tp.arrived = 0;
             // let group B land before the CTA can exit (bounded)
             if constexpr (kSplit) (void)mbar_wait_for(barB, 0, kDrainLimitNs);
+            return;
         }
-    }
-    __syncthreads();
-    if (tp.ok != 1 || tp.arrived != 1) {
-        // A skipped sample: group B (x, original, mask, noise) may still be landing in
-        // this CTA's shared memory, which must not be handed to another CTA before it
-        // has.  (After a timeout thread 0 has drained it already.)
-        if constexpr (kSplit) {
-            if (tid == 0 && tp.arrived == 1 && !mbar_wait(barB, 0)) flag(p.status, GS_DEV_TIMEOUT);
+        if (tp.ok != 1) {
+            // A skipped sample: group B (x, original, mask, noise) may still be landing
+            // in this CTA's shared memory, which must not be handed to another CTA
+            // before it has.
+            if constexpr (kSplit) {
+                if (tid == 0 && !mbar_wait(barB, 0)) flag(p.status, GS_DEV_TIMEOUT);
+            }
+            return;
         }
-        return;
+    } else {
+        if (tid == 0) {
+            tp.arrived = 1;
+            if (p.test_wait_timeout) mbar_add_tx(bar, 16u);       // bytes nothing will deliver
+            mbar_arrive(barB);
+            // ---- wait for the boxes (the rest of the CTA sleeps at the barrier) ----
+            if (!mbar_wait(bar, 0)) {
+                flag(p.status, GS_DEV_TIMEOUT);
+                tp.arrived = 0;
+            }
+        }
+        __syncthreads();
+        if (tp.ok != 1 || tp.arrived != 1) return;
     }
-    }
-    // rows past H (a ragged last band): no arithmetic, but with regions they still
-    // take part in the second CTA barrier
+    // rows past H (a ragged last band): no arithmetic (the CTA stays resident while
+    // its other threads wait for group B)
     const bool active = y < p.H;
-    if (!kSplit && !active) return;
+    if (!active) return;
     const bool inpaint = INP && tp.inpaint != 0;
     if (SKIP && tp.need_pred == 0) {
         // A blended band whose mask is 0 on every row: den = original (up to the sign
         // of zero), so the prediction was not loaded.  Only x and the original remain.
         if constexpr (kSplit) {
-            if (tid == 0 && !mbar_wait(barB, 0)) {
+            if (!mbar_wait(barB, 0)) {
                 flag(p.status, GS_DEV_TIMEOUT);
-                tp.arrived = 0;
+                return;
             }
-            __syncthreads();
-            if (tp.arrived != 1) return;
         }
-        if (!active) return;
         const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
         const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
         const long long plane = static_cast<long long>(p.H) * p.W;
@@ -762,7 +765,7 @@ __global__ void __launch_bounds__(kMaxThreads)
 
     if constexpr (kSplit) {
         // combine while group B lands, then wait for it (NEG: combined above)
-        if (!NEG && active && has_u) {
+        if (!NEG && has_u) {
 #pragma unroll
             for (int k = 0; k < CG; ++k) {
                 const Raw<T, VEC> uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
@@ -771,12 +774,10 @@ __global__ void __launch_bounds__(kMaxThreads)
                     pos[k][q] = fma2(s2, pos[k][q], mul2(oms2, widen2<T, VEC>(uv, q)));
             }
         }
-        if (tid == 0 && !mbar_wait(barB, 0)) {
+        if (!mbar_wait(barB, 0)) {
             flag(p.status, GS_DEV_TIMEOUT);
-            tp.arrived = 0;
+            return;
         }
-        __syncthreads();
-        if (tp.arrived != 1 || !active) return;
     }
 
     // combine (without regions), inpaint blend, Euler, round and store
