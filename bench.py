@@ -58,20 +58,17 @@ FALLBACK_HBM_GBS = 6800.0
 # capture, with the SHA-256 prefix of the kernel source it was taken on.  A
 # different source hash means the counters are stale: traffic is reported null.
 TRAFFIC = {
-    # profiles/guided_step_tma__bcg_bf16_b16.md
-    "bcg_bf16_b16": (6303488, "a241fc25be2c1c81"),
-    # profiles/guided_step_tma__large_steps.md
-    "area_fp16_b8": (2959616, "a241fc25be2c1c81"),
-    "inpaint_bcg_bf16_b32": (69225472 + 568320, "a241fc25be2c1c81"),
-    "sweep_bf16_b64": (100663808 + 4732160, "a241fc25be2c1c81"),
-    # with --mask-rows (profiles/guided_step_tma__read_skipping.md)
-    "inpaint_bcg_bf16_b32+mask_rows": (51108608 + 44288, "a241fc25be2c1c81"),
-    "sweep_bf16_b64+mask_rows": (88782080 + 3069440, "a241fc25be2c1c81"),
-    # sampler options and negative regions (profiles/guided_step_tma__sampler_options.md)
-    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102789888 + 7572992, "a241fc25be2c1c81"),
-    "sweep_bf16_b64@euler_ancestral@model_in": (151018752 + 27539968, "a241fc25be2c1c81"),
-    "sweep_bf16_b64@euler_ancestral": (134242816 + 10234880, "a241fc25be2c1c81"),
-    "sweep_bf16_b64@neg1": (100677632 + 5143808, "a241fc25be2c1c81"),
+    # profiles/guided_step_tma__dram_traffic.md (all entries)
+    "bcg_bf16_b16": (6303232, "8f6872ee80c22a10"),
+    "area_fp16_b8": (2960640, "8f6872ee80c22a10"),
+    "inpaint_bcg_bf16_b32": (69224192 + 599808, "8f6872ee80c22a10"),
+    "sweep_bf16_b64": (100662784 + 4819200, "8f6872ee80c22a10"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51108352 + 37888, "8f6872ee80c22a10"),
+    "sweep_bf16_b64+mask_rows": (88783104 + 3019776, "8f6872ee80c22a10"),
+    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102793472 + 7919360, "8f6872ee80c22a10"),
+    "sweep_bf16_b64@euler_ancestral@model_in": (151025920 + 27804160, "8f6872ee80c22a10"),
+    "sweep_bf16_b64@euler_ancestral": (134232832 + 10006784, "8f6872ee80c22a10"),
+    "sweep_bf16_b64@neg1": (100678912 + 5096960, "8f6872ee80c22a10"),
 }
 
 
