@@ -53,6 +53,8 @@ sys.path.insert(0, ROOT)
 METRIC = "guided-step latent Gelem/s and HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "Gelem/s"
 FALLBACK_HBM_GBS = 6800.0
+# NVIDIA's published HBM3e bandwidth of one GB300 GPU (context beside the measured peak)
+NOMINAL_HBM_GBS = 7900.0
 
 # Per-launch DRAM traffic (read + write bytes) of the step kernel from one ncu
 # capture, with the SHA-256 prefix of the kernel source it was taken on.  A
@@ -499,7 +501,9 @@ def run_ours(args, world, rank, local):
         "hbm_gbs": round(world * achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": abytes, "peak_source": peak_src},
+                     "algorithmic_bytes": abytes, "peak_source": peak_src,
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
         "e2e": e2e,
         "gpu_launches": K,
         "clocks": clk,
