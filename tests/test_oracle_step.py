@@ -357,3 +357,13 @@ def test_negative_regions_make_uncond_present_and_follow_ranges():
     assert ok.all()
     np.testing.assert_array_equal(den[0], O.combine(neg.out[0:1], c[0:1], [3.0])[0])
     np.testing.assert_array_equal(den[1], 3.0 * c[1].astype(np.float64))
+
+
+def test_ancestral_last_step_is_taken_and_lands_on_den():
+    """sigma_next = 0 is a valid standard deviation: the ancestral step takes the sample
+    and lands on den whatever the noise."""
+    B, C, H, W = 2, 2, 3, 3
+    x, c, u, n = (rnd((B, C, H, W), s) for s in (30, 31, 32, 33))
+    x_next, den, ok = O.guided_step(x, [2.0, 0.0], [0, 0], uncond=u, cond=c, cfg=3.0,
+                                    sampler="euler_ancestral", noise=n)
+    assert ok.all() and np.array_equal(x_next, den)
