@@ -486,7 +486,8 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": wl.dtype,
+        "data": "synthetic",
         "config": {"workload": describe(wl), "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W,
                    "l2": f"{R} rotating input sets of {per_set} B (>= 4x L2 of {l2} B)",
                    "launch": "CUDA graph replay" + (", PDL" if (not args.no_pdl) else ""),
