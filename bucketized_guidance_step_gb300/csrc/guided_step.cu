@@ -65,6 +65,9 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
     if (a->sampler == GS_SAMPLER_EULER_ANCESTRAL && a->noise == nullptr) return GS_ERR_INVALID_ARG;
     if (a->model_in_out != nullptr && (a->inpaint_mask == nullptr || a->orig_noise == nullptr))
         return GS_ERR_INVALID_ARG;
+    if (a->model_in_out != nullptr &&
+        (a->model_in_out == a->x_out || a->model_in_out == a->denoised_out))
+        return GS_ERR_INVALID_ARG;
 
     StepParams p = {};
     p.B = a->B;

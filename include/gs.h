@@ -325,8 +325,8 @@ typedef struct gs_step_args {
        each step the unmasked region is replaced by the original, the noise kept to the
        mask): the next model call's input m * x' + (1 - m) * (original + sigma_next *
        orig_noise), x' for samples without a mask.  Needs inpaint_mask, original and
-       orig_noise.  The sampler options and this output run on the register-streaming
-       kernel. */
+       orig_noise.  It may alias x (each element is read before it is written) but must
+       not overlap x_out or denoised_out (the same start address is GS_ERR_INVALID_ARG). */
     void*       model_in_out;   /* device [B][C][H][W] or NULL                           */
     const void* orig_noise;     /* device [B][C][H][W]: the run's fixed noise            */
 } gs_step_args;
@@ -364,7 +364,8 @@ typedef struct gs_step_args {
  *   - TMA-pipelined: used when every latent-shaped pointer is 16-byte aligned,
  *     W * element size is a multiple of 16 bytes, W <= 256, every region output
  *     is 16-byte aligned with a 16-byte-multiple row pitch and rounds up to at
- *     most 256 columns, and the inpaint mask is per-sample dense or shared.
+ *     most 256 columns, the inpaint mask is per-sample dense or shared, and
+ *     negative regions are not combined with the sampler options.
  *     Tensor maps are encoded per call (host cost of a few microseconds).
  *     One CTA per tile of (sample, up to 4 channels, a band of rows); the band
  *     height is chosen for about 128 threads per tile, or set with the
@@ -379,8 +380,11 @@ typedef struct gs_step_args {
  *
  * Errors: GS_ERR_INVALID_ARG (NULL required pointer, size < 1, region outside
  * the frame or pitch < w, n_regions out of range, step out of range with
- * step_idx NULL, neither cond nor regions, inpaint without original, unknown
- * dtype), GS_ERR_CUDA (launch failure).  Device-found errors: see dev_status.
+ * step_idx NULL, neither cond nor a positive region, a negative flag other than
+ * 0 / 1, inpaint without original, unknown dtype or sampler, the ancestral
+ * sampler without noise, the model input without inpaint_mask or orig_noise or
+ * on x_out / denoised_out), GS_ERR_CUDA (launch failure).  Device-found errors:
+ * see dev_status.
  */
 gs_status gs_guided_step(const gs_step_args* args, gs_stream stream);
 

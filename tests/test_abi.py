@@ -135,6 +135,10 @@ def test_step_rejects_invalid_sampler_arguments(lib):
     a = _valid_args()
     a.inpaint_mask, a.original, a.model_in_out = 0x3000, 0x4000, 0x5000  # ... no orig_noise
     assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+    a = _valid_args()                                                    # model input on x_out
+    a.inpaint_mask, a.original, a.orig_noise = 0x3000, 0x4000, 0x6000
+    a.model_in_out = a.x_out
+    assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
 
 
 _LAYOUT_PROBE = r"""
