@@ -13,21 +13,23 @@
 //     region arrives row-aligned with the frame whatever its origin, and only
 //     regions that touch the band are fetched at all.
 //
-// Thread 0 arms the CTA's mbarrier with the tile's byte count and issues the
-// boxes; no register holds a load in flight.  Every thread then computes VEC
+// Thread 0 (and the parameter thread) arm the CTA's mbarrier with the tile's byte
+// count and issue the boxes; no register holds a load in flight.  Every thread
+// waits on the mbarrier (suspended in hardware) and then computes VEC
 // pixels x CG channels of one row from shared memory (region weights and the
 // mask once per pixel, reused over the channels; packed fp32-pair math) and
 // writes x_out with 16-byte stores.  Several tile-CTAs are resident per SM, so
 // the loads of some overlap the arithmetic of others, and the CTA scheduler
 // hands out tiles as SMs drain.
 //
-// The mbarrier wait is bounded (200 ms of %globaltimer); on expiry the thread
+// Every mbarrier wait is bounded (200 ms of %globaltimer); on expiry the thread
 // sets GS_DEV_TIMEOUT in the status word and returns.
 //
 // This header holds the launch parameters, the kernel template and its launch
 // templates; step_tma.cu builds the parameters and launches the deterministic
 // Euler instances, step_tma_sampler.cu compiles the instances with the sampler
-// options (ancestral noise, the next model input), so the two compile in parallel.
+// options (ancestral noise, the next model input) and step_tma_neg.cu those with
+// negative regions, so the three compile in parallel.
 #pragma once
 
 #include <cuda.h>
@@ -276,10 +278,11 @@ __device__ __forceinline__ void region_channels_sh(int sh, const unsigned char* 
 // global load that another box does not need.  While the boxes are in flight the
 // remaining warps build, for every region touching the band, a frame-aligned
 // table of its column factors (feather ramps, 0 outside the region), so that a
-// thread's VEC weights are two 16-byte loads.  After a CTA barrier every thread
-// computes CG channels of its VEC pixels from shared memory.  With regions in
-// multi-channel tiles the boxes come in two groups on two barriers (see kSplit), so
-// that the regional accumulation overlaps the arrival of x, original and mask.
+// thread's VEC weights are two 16-byte loads.  Once the boxes have landed every
+// thread computes CG channels of its VEC pixels from shared memory (see
+// kThreadWaits for who waits how).  With regions in multi-channel tiles the boxes
+// come in two groups on two barriers (see kSplit), so that the regional
+// accumulation overlaps the arrival of x, original and mask.
 struct TileParams {
     float s, one_minus_s, ratio;   // ratio: sigma_next / sigma, or sigma_down / sigma
     float up, sigma_next;          // sigma_up (ancestral), sigma_next (model input)
