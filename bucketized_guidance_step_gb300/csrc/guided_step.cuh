@@ -19,9 +19,9 @@
 // CH channels, a group of VEC pixels in one row); per-pixel quantities (region
 // weights, mask) are computed once per item and reused over its CH channels.
 // Consecutive threads take consecutive pixel groups, so each warp reads
-// 512 contiguous bytes per plane.  The grid is a whole number of waves of
-// SM-count CTAs, and CTAs own equal contiguous item ranges, so that every SM
-// moves the same number of bytes.
+// 512 contiguous bytes per plane.  One item per thread, 128-thread CTAs; the CTA
+// scheduler hands CTAs to SMs as they drain, which balances SMs whose memory
+// traffic finishes at different rates.
 //
 // Built with -fmad=false: every multiply-add that is fused is an explicit fmaf,
 // which fixes the rounding the tests reason about (s = 0 / s = 1 / m = 0 / m = 1

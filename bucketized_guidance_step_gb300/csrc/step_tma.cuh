@@ -1,6 +1,6 @@
 // TMA-fed variant of the fused guided step (sm_103a).
 //
-// Same arithmetic as the register-streaming kernel in guided_step.cu (see the
+// Same arithmetic as the register-streaming kernel in guided_step.cuh (see the
 // formulas in include/gs.h); a different way to move the bytes.  Each CTA owns
 // one tile = (sample b, a group of CG channels, a band of RB full rows), and
 // every input of the tile arrives as one 3-D TMA box into shared memory:
