@@ -61,16 +61,16 @@ NOMINAL_HBM_GBS = 7900.0
 # different source hash means the counters are stale: traffic is reported null.
 TRAFFIC = {
     # profiles/guided_step_tma__dram_traffic.md (all entries)
-    "bcg_bf16_b16": (6303232, "8f6872ee80c22a10"),
-    "area_fp16_b8": (2960640, "8f6872ee80c22a10"),
-    "inpaint_bcg_bf16_b32": (69224192 + 599808, "8f6872ee80c22a10"),
-    "sweep_bf16_b64": (100662784 + 4819200, "8f6872ee80c22a10"),
-    "inpaint_bcg_bf16_b32+mask_rows": (51108352 + 37888, "8f6872ee80c22a10"),
-    "sweep_bf16_b64+mask_rows": (88783104 + 3019776, "8f6872ee80c22a10"),
-    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102793472 + 7919360, "8f6872ee80c22a10"),
-    "sweep_bf16_b64@euler_ancestral@model_in": (151025920 + 27804160, "8f6872ee80c22a10"),
-    "sweep_bf16_b64@euler_ancestral": (134232832 + 10006784, "8f6872ee80c22a10"),
-    "sweep_bf16_b64@neg1": (100678912 + 5096960, "8f6872ee80c22a10"),
+    "bcg_bf16_b16": (6303488, "e043c1b5beb67078"),
+    "area_fp16_b8": (2959616, "e043c1b5beb67078"),
+    "inpaint_bcg_bf16_b32": (69224448 + 664576, "e043c1b5beb67078"),
+    "sweep_bf16_b64": (100665088 + 5023744, "e043c1b5beb67078"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51108608 + 40448, "e043c1b5beb67078"),
+    "sweep_bf16_b64+mask_rows": (88782592 + 3274496, "e043c1b5beb67078"),
+    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102789888 + 7498496, "e043c1b5beb67078"),
+    "sweep_bf16_b64@euler_ancestral@model_in": (151042560 + 28199424, "e043c1b5beb67078"),
+    "sweep_bf16_b64@euler_ancestral": (134237184 + 9946368, "e043c1b5beb67078"),
+    "sweep_bf16_b64@neg1": (100680960 + 5161472, "e043c1b5beb67078"),
 }
 
 
