@@ -415,3 +415,35 @@ def test_skipped_samples_with_regions_in_large_tiles(sampler):
     skipped = (bad < 0).cpu()
     assert bool((out[skipped.to(DEV)] == 5.0).all())
     assert same_bits(out[~skipped.to(DEV)], ref[~skipped.to(DEV)])
+
+
+def _golden_layout():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "bcg_stacked_layout.txt")
+    rows = []
+    for line in open(path):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, branch, b = line.split()
+            rows.append((int(k), branch, int(b)))
+    return rows
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_stacked_layout_follows_the_pages(dtype, kernel_choice):
+    """The stacked [2B] model output is read in the order the BCG write-up prints: with
+    scale 0 sample b's step lands on stacked row (uncond, b), with scale 1 on (cond, b)."""
+    rows = _golden_layout()
+    B = max(b for _, _, b in rows) + 1
+    C, H, W = 2, 8, 16
+    stacked = torch.empty((2 * B, C, H, W), dtype=dtype, device=DEV)
+    for k, branch, b in rows:
+        stacked[k] = float(10 * (1 if branch == "cond" else 0) + b + 1)
+    x = rnd((B, C, H, W), 80, dtype)
+    out = torch.empty_like(x)
+    for cfg, want_branch in ((0.0, "uncond"), (1.0, "cond")):
+        gs.guided_step(x, sigmas=sig(4.0, 0.0), stacked=stacked, cfg=cfg, x_out=out)
+        torch.cuda.synchronize()
+        for k, branch, b in rows:
+            if branch == want_branch:
+                assert torch.equal(out[b], stacked[k]), (cfg, k, branch, b)
