@@ -77,9 +77,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     const bool anc = sp.sampler == GS_SAMPLER_EULER_ANCESTRAL;
     const bool mi = sp.model_in != nullptr;
     const bool nz = anc || mi;
-    // negative regions with the sampler options run on the register kernel
     const bool neg = sp.has_neg != 0;
-    if (neg && nz) return GS_OK;
     if (anc && !aligned16(sp.noise)) return GS_OK;
     if (mi && (!aligned16(sp.model_in) || !aligned16(sp.orig_noise))) return GS_OK;
     if (inp && (!aligned16(sp.orig) || !aligned16(sp.imask) ||
@@ -160,8 +158,8 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     p.has_c = sp.c != nullptr;
     p.mask_shared = inp && sp.imask_bstride == 0;
     p.test_wait_timeout = (flags & GS_LAUNCH_TEST_WAIT_TIMEOUT) ? 1 : 0;
-    // (the sampler-option and negative-region instances do not skip reads)
-    p.mask_rows = inp && !nz && !neg ? sp.mask_rows : nullptr;
+    // (the negative-region instances do not skip reads)
+    p.mask_rows = inp && !neg ? sp.mask_rows : nullptr;
     p.sampler = sp.sampler;
     p.model_in = sp.model_in;
     for (int r = 0; r < sp.n_regions; ++r)
@@ -254,7 +252,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     gs_status st;
     const bool reg = sp.n_regions > 0;
     if (neg) {
-        st = tma_launch_neg(p, dtype, cg, threads, smem, inp, stream, flags);
+        st = tma_launch_neg(p, dtype, nz, cg, threads, smem, inp, stream, flags);
     } else if (nz) {
         st = tma_launch_sampler(p, dtype, cg, threads, smem, reg, inp, stream, flags);
     } else {

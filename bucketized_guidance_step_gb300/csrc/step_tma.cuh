@@ -105,10 +105,10 @@ struct TmaParams {
 gs_status tma_launch_sampler(TmaParams& p, int dtype, int cg, int threads, unsigned smem,
                              bool reg, bool inp, gs_stream stream, unsigned flags);
 
-// Launch the instances with negative regions (the regional uncond branch); defined
-// in step_tma_neg.cu.
-gs_status tma_launch_neg(TmaParams& p, int dtype, int cg, int threads, unsigned smem, bool inp,
-                         gs_stream stream, unsigned flags);
+// Launch the instances with negative regions (the regional uncond branch), with or
+// without the sampler options; defined in step_tma_neg.cu.
+gs_status tma_launch_neg(TmaParams& p, int dtype, bool nz, int cg, int threads, unsigned smem,
+                         bool inp, gs_stream stream, unsigned flags);
 
 namespace {
 
@@ -312,10 +312,9 @@ template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ, bool NEG>
 __global__ void __launch_bounds__(kMaxThreads)
     guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
     static_assert(INP || !SKIP, "read skipping needs the inpaint inputs");
-    static_assert(!(NZ && SKIP), "the sampler options are not combined with read skipping");
     // NEG: some regions belong to the uncond branch, which is then their weighted sum
     // with the full-frame uncond output (weight 1, if given), like the positive branch
-    static_assert(!NEG || (REG && !SKIP && !NZ), "negative regions: region instances only");
+    static_assert(!NEG || (REG && !SKIP), "negative regions: region instances only");
     using S = typename T::scalar;
     constexpr int VEC = 16 / static_cast<int>(sizeof(S));
     constexpr int NP = VEC / 2;
@@ -633,18 +632,27 @@ __global__ void __launch_bounds__(kMaxThreads)
         const long long gbase =
             static_cast<long long>(z) * plane + static_cast<long long>(y) * p.W + x0;
         const f2 r2 = splat2(tp.ratio);
+        const f2 up2 = splat2(NZ ? tp.up : 0.0f);
+        const f2 sn2 = splat2(NZ ? tp.sigma_next : 0.0f);
 #pragma unroll
         for (int k = 0; k < CG; ++k) {
             const Raw<T, VEC> xv = ld_smem<T, VEC>(st + p.off_x, k * kstride + pix);
             const Raw<T, VEC> ov = ld_smem<T, VEC>(st + p.off_o, k * kstride + pix);
-            Raw<T, VEC> xo;
+            Raw<T, VEC> xo, nv, onv, mi;
+            if (NZ && anc) nv = ld_smem<T, VEC>(st + p.off_n, k * kstride + pix);
+            if (NZ && want_mi) onv = ld_smem<T, VEC>(st + p.off_on, k * kstride + pix);
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
                 const f2 den = widen2<T, VEC>(ov, q);
-                narrow2<T, VEC>(xo, q, fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den));
+                f2 xn = fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den);
+                if (NZ && anc) xn = fma2(up2, widen2<T, VEC>(nv, q), xn);
+                narrow2<T, VEC>(xo, q, xn);
+                // the model input where the mask is 0: the original noised to sigma_next
+                if (NZ && want_mi) narrow2<T, VEC>(mi, q, fma2(sn2, widen2<T, VEC>(onv, q), den));
             }
             store_raw<T, VEC>(p.x_out, gbase + k * plane, xo);
             if (p.den_out != nullptr) store_raw<T, VEC>(p.den_out, gbase + k * plane, ov);
+            if (NZ && want_mi) store_raw<T, VEC>(p.model_in, gbase + k * plane, mi);
         }
         return;
     }
@@ -883,34 +891,27 @@ gs_status launch_cg(TmaParams& p, int cg, int threads, unsigned smem, gs_stream 
 }
 
 // Negative regions (the regional uncond branch): region instances without read
-// skipping or sampler options (the host sends those requests to the register kernel).
-template <typename T>
+// skipping (the host drops the row summary for them), with or without the sampler
+// options.
+template <typename T, bool NZ>
 gs_status launch_features_neg(TmaParams& p, int cg, int threads, unsigned smem, bool inp,
                               gs_stream stream, unsigned flags) {
-    if (inp) return launch_cg<T, true, true, false, false, true>(p, cg, threads, smem, stream, flags);
-    return launch_cg<T, true, false, false, false, true>(p, cg, threads, smem, stream, flags);
+    if (inp) return launch_cg<T, true, true, false, NZ, true>(p, cg, threads, smem, stream, flags);
+    return launch_cg<T, true, false, false, NZ, true>(p, cg, threads, smem, stream, flags);
 }
 
-// NZ = false: the deterministic Euler step; read skipping (a row summary of the
-// inpaint mask) has instances of its own.  NZ = true: the sampler options, without
-// read skipping (the host clears mask_rows for them).
+// NZ = false: the deterministic Euler step; NZ = true: the sampler options.  Read
+// skipping (a row summary of the inpaint mask) has instances of its own in both.
 template <typename T, bool NZ>
 gs_status launch_features(TmaParams& p, int cg, int threads, unsigned smem, bool reg, bool inp,
                           gs_stream stream, unsigned flags) {
-    if constexpr (NZ) {
-        if (reg && inp) return launch_cg<T, true, true, false, true>(p, cg, threads, smem, stream, flags);
-        if (reg) return launch_cg<T, true, false, false, true>(p, cg, threads, smem, stream, flags);
-        if (inp) return launch_cg<T, false, true, false, true>(p, cg, threads, smem, stream, flags);
-        return launch_cg<T, false, false, false, true>(p, cg, threads, smem, stream, flags);
-    } else {
-        const bool skip = inp && p.mask_rows != nullptr;
-        if (reg && skip) return launch_cg<T, true, true, true, false>(p, cg, threads, smem, stream, flags);
-        if (reg && inp) return launch_cg<T, true, true, false, false>(p, cg, threads, smem, stream, flags);
-        if (reg) return launch_cg<T, true, false, false, false>(p, cg, threads, smem, stream, flags);
-        if (skip) return launch_cg<T, false, true, true, false>(p, cg, threads, smem, stream, flags);
-        if (inp) return launch_cg<T, false, true, false, false>(p, cg, threads, smem, stream, flags);
-        return launch_cg<T, false, false, false, false>(p, cg, threads, smem, stream, flags);
-    }
+    const bool skip = inp && p.mask_rows != nullptr;
+    if (reg && skip) return launch_cg<T, true, true, true, NZ>(p, cg, threads, smem, stream, flags);
+    if (reg && inp) return launch_cg<T, true, true, false, NZ>(p, cg, threads, smem, stream, flags);
+    if (reg) return launch_cg<T, true, false, false, NZ>(p, cg, threads, smem, stream, flags);
+    if (skip) return launch_cg<T, false, true, true, NZ>(p, cg, threads, smem, stream, flags);
+    if (inp) return launch_cg<T, false, true, false, NZ>(p, cg, threads, smem, stream, flags);
+    return launch_cg<T, false, false, false, NZ>(p, cg, threads, smem, stream, flags);
 }
 
 }  // namespace

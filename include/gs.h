@@ -364,8 +364,7 @@ typedef struct gs_step_args {
  *   - TMA-pipelined: used when every latent-shaped pointer is 16-byte aligned,
  *     W * element size is a multiple of 16 bytes, W <= 256, every region output
  *     is 16-byte aligned with a 16-byte-multiple row pitch and rounds up to at
- *     most 256 columns, the inpaint mask is per-sample dense or shared, and
- *     negative regions are not combined with the sampler options.
+ *     most 256 columns, and the inpaint mask is per-sample dense or shared.
  *     Tensor maps are encoded per call (host cost of a few microseconds).
  *     One CTA per tile of (sample, up to 4 channels, a band of rows); the band
  *     height is chosen for about 128 threads per tile, or set with the

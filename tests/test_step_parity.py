@@ -194,6 +194,7 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
         Mmi = np.where(present.reshape(Bn, 1, 1, 1), Mmi, M)
         gate(to64(mid)[okb], ref_mi[okb], Mmi[okb], wl.dtype, len(oregs),
              what=wl.name + " model input", extra=extra + 4)
+    run_case.last_model_in = to64(mid) if model_in else None
     return rep, got, ref, ok
 
 
@@ -425,14 +426,16 @@ def test_negative_regions_ragged(dtype, shape, offset, tma):
              expect_kernel="scalar" if offset else None)
 
 
-def test_negative_regions_with_sampler_options():
-    """Negative regions together with the ancestral step and the model input (the
-    register kernel serves this combination)."""
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
+@pytest.mark.parametrize("model_in", [False, True], ids=["ancestral", "ancestral_model_in"])
+def test_negative_regions_with_sampler_options(model_in, tma):
+    """Negative regions together with the ancestral step (and the model input), on the
+    sweep shape: the combination runs on both kernels."""
     base = WORKLOADS[4]
-    wl = Workload("neg_anc", 16, 8, 64, 64, "bf16", base.schedule, base.guidance,
-                  full_frame_cond=False, n_regions=3, inpaint=True, inpaint_samples=8, seed=23)
-    rep, *_ = run_case(wl, negative=(1,), sampler="euler_ancestral", model_in=True,
-                       expect_kernel="vector")
+    wl = Workload("neg_anc", 64, 16, 128, 128, "bf16", base.schedule, base.guidance,
+                  full_frame_cond=False, n_regions=3, inpaint=True, inpaint_samples=32, seed=23)
+    rep, *_ = run_case(wl, negative=(1,), sampler="euler_ancestral", model_in=model_in,
+                       tma=tma, expect_kernel="tma" if tma else "vector")
     assert rep.n == wl.elements
 
 
@@ -477,3 +480,18 @@ def test_feature_combinations(seed, tma):
     row summary, both samplers, the model input, unaligned bases) against the oracle."""
     wl, kw = _combo(seed)
     run_case(wl, tma=tma, **kw)
+
+
+@pytest.mark.parametrize("poison", [False, True], ids=["clean", "poisoned"])
+@pytest.mark.parametrize("wl", [WORKLOADS[3], WORKLOADS[4]], ids=["inpaint", "sweep"])
+def test_mask_rows_skip_reads_with_sampler_options(wl, poison):
+    """Read skipping together with the ancestral step and the model input: both outputs
+    match the oracle (also with the skipped bands' prediction poisoned) and equal the
+    step without the row summary bit for bit."""
+    rep, got, _, _ = run_case(wl, mask_rows=True, poison=poison, sampler="euler_ancestral",
+                              model_in=True, expect_kernel="tma")
+    mi = run_case.last_model_in
+    assert rep.n == wl.elements and np.isfinite(got).all() and np.isfinite(mi).all()
+    _, plain, _, _ = run_case(wl, sampler="euler_ancestral", model_in=True, expect_kernel="tma")
+    assert np.array_equal(got.view(np.uint64), plain.view(np.uint64))
+    assert np.array_equal(mi.view(np.uint64), run_case.last_model_in.view(np.uint64))
