@@ -61,16 +61,18 @@ NOMINAL_HBM_GBS = 7900.0
 # different source hash means the counters are stale: traffic is reported null.
 TRAFFIC = {
     # profiles/guided_step_tma__dram_traffic.md (all entries)
-    "bcg_bf16_b16": (6303488, "e043c1b5beb67078"),
-    "area_fp16_b8": (2959616, "e043c1b5beb67078"),
-    "inpaint_bcg_bf16_b32": (69224448 + 664576, "e043c1b5beb67078"),
-    "sweep_bf16_b64": (100665088 + 5023744, "e043c1b5beb67078"),
-    "inpaint_bcg_bf16_b32+mask_rows": (51108608 + 40448, "e043c1b5beb67078"),
-    "sweep_bf16_b64+mask_rows": (88782592 + 3274496, "e043c1b5beb67078"),
-    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102789888 + 7498496, "e043c1b5beb67078"),
-    "sweep_bf16_b64@euler_ancestral@model_in": (151042560 + 28199424, "e043c1b5beb67078"),
-    "sweep_bf16_b64@euler_ancestral": (134237184 + 9946368, "e043c1b5beb67078"),
-    "sweep_bf16_b64@neg1": (100680960 + 5161472, "e043c1b5beb67078"),
+    "bcg_bf16_b16": (6303488, "09603797658d4206"),
+    "area_fp16_b8": (2959872, "09603797658d4206"),
+    "inpaint_bcg_bf16_b32": (69224704 + 573184, "09603797658d4206"),
+    "sweep_bf16_b64": (100664320 + 4617984, "09603797658d4206"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51108864 + 37120, "09603797658d4206"),
+    "sweep_bf16_b64+mask_rows": (88782080 + 3080448, "09603797658d4206"),
+    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102790144 + 7858176, "09603797658d4206"),
+    "sweep_bf16_b64@euler_ancestral@model_in": (151034880 + 27881728, "09603797658d4206"),
+    "sweep_bf16_b64@euler_ancestral": (134235136 + 10008576, "09603797658d4206"),
+    "sweep_bf16_b64@neg1": (100679936 + 5136896, "09603797658d4206"),
+    "inpaint_bcg_bf16_b32@euler_ancestral@model_in+mask_rows": (84679168 + 5858560, "09603797658d4206"),
+    "sweep_bf16_b64@euler_ancestral@model_in+mask_rows": (139146240 + 27759872, "09603797658d4206"),
 }
 
 
