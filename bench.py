@@ -3,7 +3,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference] [--no-pdl] [--no-tma]
-                    [--buckets N] [--batch B] [--cpu-procs P]
+                    [--buckets N] [--batch B] [--mask-rows]
+                    [--sampler euler|euler_ancestral] [--model-in]
+                    [--negative-regions K] [--cpu-procs P]
 
 A step is one call of gs_guided_step: the whole per-step path (per-sample
 parameters, regional accumulation, guidance combine, inpaint blend, Euler
@@ -17,7 +19,9 @@ Other keys of the JSON line:
 * e2e: the same metric when every step copies its inputs from pinned host
   memory and reads x_out back (copies inside the timed region).
 * roofline: algorithmic bytes per launch (``accounting.step_bytes``) over the
-  measured launch time, against the measured HBM copy peak.
+  measured launch time, against the measured HBM copy peak (and NVIDIA's published
+  figure); traffic = the DRAM bytes of one ncu capture of this configuration, reported
+  while the kernel sources still hash to the captured revision.
 * cpu_baseline: the float64 oracle on a bounded sample of the workload, timed
   on the host (rank 0 at N = 1 only).
 * clocks: nvidia-smi samples taken while the GPU runs the step.
@@ -26,8 +30,11 @@ Other keys of the JSON line:
 against) on the same workload, metric and unit.
 
 --buckets and --batch change the named workload's bucket count or batch size
-(the sweeps of the measurement plan); --cpu-procs P times the oracle in P
-processes at once (one sample each) instead of one.
+(the sweeps of the measurement plan); --mask-rows passes the inpaint mask's row
+summary (bands whose mask is 0 skip the prediction reads; the roofline counts the
+bytes still required); --sampler, --model-in and --negative-regions select the
+Euler-ancestral step, the next-model-input output and regional uncond; --cpu-procs
+P times the oracle in P processes at once (one sample each) instead of one.
 
 With N > 1 every rank runs its own batch of the workload on its own GPU (the
 step is independent per sample and needs no exchange), so the job's throughput
