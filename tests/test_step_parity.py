@@ -472,8 +472,12 @@ def _combo(seed):
     return wl, kw
 
 
+# GS_TEST_COMBOS raises the number of random combinations (default 40) for a longer run.
+N_COMBOS = int(__import__("os").environ.get("GS_TEST_COMBOS", "40"))
+
+
 @pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(N_COMBOS))
 def test_feature_combinations(seed, tma):
     """Random combinations of every option (dtype, ragged shape, regions with masks,
     feathers, timestep ranges and negative regions, inpaint with partial presence and the
