@@ -12,7 +12,9 @@ bounded by the error scale
     M = |r| (|x| + Mden) + Mden,   Mden = m Mpred + (1 - m) |orig|,
     Mpred = |1 - s| Mu + |s| Mpos,   Mpos = (|c| + sum_r w_r |out_r|) / W,
 
-Mu is |u|, or with negative regions (|u| + sum_neg w_r |out_r|) / W_neg,
+Mu is |u|, or with negative regions (|u| + sum_neg w_r |out_r|) / W_neg, and M carries
+2^-26 |x| more for the oracle's own float64 rounding of the Euler form, which is not
+proportional to r (it stays when sigma_next = 0),
 
 with r = sigma_next / sigma.  Hence |g32 - ref| <= k 2^-24 M with
 k = n_regions + 16.  An element passes when
@@ -114,7 +116,10 @@ def error_scale(x, u, c, regions, s, r, m, present, orig, H, W) -> np.ndarray:
         pres = np.asarray(present, dtype=bool).reshape(B, 1, 1, 1)
         mden = np.where(pres, mm * mpred + np.abs(1 - mm) * np.abs(orig), mpred)
     r4 = np.abs(np.asarray(r, dtype=np.float64)).reshape(B, 1, 1, 1)
-    return r4 * (np.abs(x) + mden) + mden
+    # + 2^-26 |x|: the oracle's own float64 rounding of x + (sigma' - sigma)(x - den)/sigma,
+    # which does not vanish at sigma' = 0 where r does (an exact 0 from the kernel then
+    # meets a reference of order 2^-53 |x|)
+    return r4 * (np.abs(x) + mden) + mden + np.abs(x) * 2.0 ** -26
 
 
 def _ulp(v: np.ndarray, dtype: str) -> np.ndarray:
