@@ -2,11 +2,14 @@
  * gs.h -- C ABI of the fused guided denoise step for GB300 (sm_103a).
  *
  * One sampler step of a diffusion model, after the model has produced its
- * outputs for the step: regional conditioning accumulation, classifier-free
- * guidance with a scalar or bucketized per-sample scale, inpaint blend with the
- * original latent and the Euler update to the next sigma -- all in one kernel
- * launch.  Host helpers build the sigma schedule and the bucket plan once per
- * run, and a small kernel prepares the latent inpaint mask once per run.
+ * outputs for the step: regional conditioning accumulation (positive and, with
+ * negative regions, uncond branch), classifier-free guidance with a scalar or
+ * bucketized per-sample scale, inpaint blend with the original latent and the
+ * Euler or Euler-ancestral update to the next sigma, optionally with the next
+ * model input under the inpaint wrapper -- all in one kernel launch.  Host
+ * helpers build the sigma schedule and the bucket plan once per run, convert
+ * areas to latent slices and pack cond entries into model calls; small kernels
+ * prepare the latent inpaint mask and its row summary once per run.
  *
  * Sources (page title, section):
  *   [SAMPLING] "12 · 采样器、调度器与 CFG" -- ComfyUI's sampler / scheduler / CFG notes.
