@@ -6,7 +6,10 @@ gives uncond and scale 1 gives cond; sampling page "cfg = 1 的优化": with sca
 the plain cond; an all-ones inpaint mask changes nothing; sigma_next = 0 lands
 on the denoised prediction), plus determinism, aliasing, the device status
 word, buffer guard bands and the shared-mask stride.  They hold exactly by the
-kernel's fp32 formulation and need no oracle.
+kernel's fp32 formulation and need no oracle.  Later additions: the ancestral
+split's closed forms and its last step, the next model input following the mask,
+a full-frame negative region equal to the plain uncond, and the stacked layout
+printed in the BCG write-up (tests/golden/bcg_stacked_layout.txt).
 """
 
 from __future__ import annotations
