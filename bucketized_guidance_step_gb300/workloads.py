@@ -28,6 +28,10 @@ The five workloads (the sizes the step is measured and checked on):
    uncond, inpaint mask and original on samples 0..31, 16 buckets of the curve
    of (3), step indices uniform over a 50-step Karras schedule with
    force_full_denoise.
+
+Variants of any workload (``sampler``, ``model_input``, ``negative_regions``) draw
+the ancestral step's fresh noise and the run's fixed noise from seeds of their own,
+so that the other inputs keep their bits.
 """
 
 from __future__ import annotations
