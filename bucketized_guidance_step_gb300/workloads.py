@@ -29,9 +29,10 @@ The five workloads (the sizes the step is measured and checked on):
    of (3), step indices uniform over a 50-step Karras schedule with
    force_full_denoise.
 
-Variants of any workload (``sampler``, ``model_input``, ``negative_regions``) draw
-the ancestral step's fresh noise and the run's fixed noise from seeds of their own,
-so that the other inputs keep their bits.
+The sampler variants of any workload (``sampler``, ``model_input``) draw the
+ancestral step's fresh noise and the run's fixed noise from seeds of their own, so
+that the other inputs keep their bits; ``negative_regions`` only marks the first
+regions as part of the uncond branch.
 """
 
 from __future__ import annotations
