@@ -161,7 +161,7 @@ int main(void) {
 """
 
 
-def test_ctypes_structs_match_the_header_layout(tmp_path):
+def test_ctypes_structs_match_the_header_layout(repo_tmp):
     """Every ctypes mirror in the binding has the C compiler's offsets and size."""
     import shutil
     import subprocess
@@ -173,9 +173,9 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
              "gs_area": gs.Area, "gs_rect": gs.Rect, "gs_cond_entry": gs.CondEntry,
              "gs_cond_chunk": gs.CondChunk}
     fields = "\n    ".join(f"F({c}, {f})" for c, py in pairs.items() for f, _ in py._fields_)
-    src = tmp_path / "layout.c"
+    src = repo_tmp / "layout.c"
     src.write_text(_LAYOUT_PROBE.replace("%FIELDS%", fields))
-    exe = tmp_path / "layout"
+    exe = repo_tmp / "layout"
     subprocess.run([cc, "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
                    check=True)
     got = {}

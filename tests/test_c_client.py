@@ -61,15 +61,15 @@ int main(void) {
 """
 
 
-def test_c_client_matches_oracle(tmp_path):
+def test_c_client_matches_oracle(repo_tmp):
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
     build.build()
     lib = gs.library_path()
-    src = tmp_path / "client.c"
+    src = repo_tmp / "client.c"
     src.write_text(CLIENT)
-    exe = tmp_path / "client"
+    exe = repo_tmp / "client"
     subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), lib,
                     "-Wl,-rpath," + os.path.dirname(lib), "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
