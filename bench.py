@@ -5,25 +5,36 @@
                     [--impl ours|reference] [--no-pdl] [--no-tma]
                     [--buckets N] [--batch B] [--mask-rows]
                     [--sampler euler|euler_ancestral] [--model-in]
-                    [--negative-regions K] [--cpu-procs P]
+                    [--negative-regions K] [--cpu-procs P] [--api-steps N]
+                    [--no-per-config]
 
 A step is one call of gs_guided_step: the whole per-step path (per-sample
 parameters, regional accumulation, guidance combine, inpaint blend, Euler
-update) over one batch.  Inputs are seeded synthetic tensors resident in HBM
-before timing starts; R input sets whose total exceeds 4x the L2 cache rotate
-from step to step, so every step reads from DRAM.  The K timed steps are
-replayed from CUDA graphs and timed with CUDA events on the launching stream,
-bracketed by a barrier and device synchronisation, max over ranks.
+update) over one batch.  The headline workload is the throughput sweep (B=64,
+16x128x128 bf16, three regions, inpaint on half the batch), the largest
+configuration that fits one GPU.  Inputs are seeded synthetic tensors resident
+in HBM before timing starts; R input sets whose total exceeds 4x the L2 cache
+rotate from step to step, so every step reads from DRAM.  Exactly K timed steps
+are replayed from CUDA graphs and timed with CUDA events on the launching
+stream, bracketed by a barrier and device synchronisation, max over ranks; a
+short device-side spin, enqueued before the start event, holds the stream while
+the host enqueues the timed graphs, so the timed region does not wait on host
+submission.
 
 Other keys of the JSON line:
+* per_config: every target workload (bcg, area, inpaint, sweep) timed the same way
+  in the same process, with at least 2000 steps each.
 * e2e: the same metric when every step copies its inputs from pinned host
   memory and reads x_out back (copies inside the timed region).
+* api: the per-call cost of gs_guided_step without CUDA graphs (host microseconds
+  per call and the device time per step that mode reaches).
 * roofline: algorithmic bytes per launch (``accounting.step_bytes``) over the
   measured launch time, against the measured HBM copy peak (and NVIDIA's published
-  figure); traffic = the DRAM bytes of one ncu capture of this configuration, reported
-  while the kernel sources still hash to the captured revision.
+  figure); traffic = the DRAM bytes (read and write) of one ncu capture of this
+  configuration, reported while the kernel sources still hash to the captured
+  revision.
 * cpu_baseline: the float64 oracle on a bounded sample of the workload, timed
-  on the host (rank 0 at N = 1 only).
+  on the host cores (rank 0 at N = 1 only).
 * clocks: nvidia-smi samples taken while the GPU runs the step.
 
 --impl reference times the oracle (the CPU restatement the kernel is checked
@@ -34,7 +45,8 @@ against) on the same workload, metric and unit.
 summary (bands whose mask is 0 skip the prediction reads; the roofline counts the
 bytes still required); --sampler, --model-in and --negative-regions select the
 Euler-ancestral step, the next-model-input output and regional uncond; --cpu-procs
-P times the oracle in P processes at once (one sample each) instead of one.
+P times the oracle in P processes at once (one sample each; default one per host
+core).
 
 With N > 1 every rank runs its own batch of the workload on its own GPU (the
 step is independent per sample and needs no exchange), so the job's throughput
@@ -63,23 +75,12 @@ FALLBACK_HBM_GBS = 6800.0
 # NVIDIA's published HBM3e bandwidth of one GB300 GPU (context beside the measured peak)
 NOMINAL_HBM_GBS = 7900.0
 
-# Per-launch DRAM traffic (read + write bytes) of the step kernel from one ncu
-# capture, with the SHA-256 prefix of the kernel source it was taken on.  A
-# different source hash means the counters are stale: traffic is reported null.
+# Per-launch DRAM traffic of the step kernel from one ncu capture of one launch:
+# (dram__bytes_read.sum, dram__bytes_write.sum, SHA-256 prefix of the kernel sources
+# it was taken on).  A different source hash means the counters are stale and the
+# line reports traffic null.  Keys: workload name, then "+mask_rows" or "+mask_spans"
+# with a mask summary.
 TRAFFIC = {
-    # profiles/guided_step_tma__dram_traffic.md (all entries)
-    "bcg_bf16_b16": (6303232, "8f840309b80560a6"),
-    "area_fp16_b8": (2959872, "8f840309b80560a6"),
-    "inpaint_bcg_bf16_b32": (69225728 + 593920, "8f840309b80560a6"),
-    "sweep_bf16_b64": (100665856 + 4693504, "8f840309b80560a6"),
-    "inpaint_bcg_bf16_b32+mask_rows": (51108352 + 46080, "8f840309b80560a6"),
-    "sweep_bf16_b64+mask_rows": (88780800 + 3304448, "8f840309b80560a6"),
-    "inpaint_bcg_bf16_b32@euler_ancestral@model_in": (102789888 + 7828480, "8f840309b80560a6"),
-    "sweep_bf16_b64@euler_ancestral@model_in": (151024384 + 27753472, "8f840309b80560a6"),
-    "sweep_bf16_b64@euler_ancestral": (134248448 + 10248704, "8f840309b80560a6"),
-    "sweep_bf16_b64@neg1": (100678656 + 5125376, "8f840309b80560a6"),
-    "inpaint_bcg_bf16_b32@euler_ancestral@model_in+mask_rows": (84678912 + 6104576, "8f840309b80560a6"),
-    "sweep_bf16_b64@euler_ancestral@model_in+mask_rows": (139172096 + 28194560, "8f840309b80560a6"),
 }
 
 
@@ -89,7 +90,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="bcg_bf16_b16")
+    ap.add_argument("--workload", default="sweep_bf16_b64",
+                    help="the headline workload (default: the throughput sweep, B=64 "
+                         "16x128x128 bf16, the largest one-GPU configuration)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch (on by default: each "
                          "step's CTAs are scheduled while the previous kernel drains, and wait "
@@ -108,6 +111,14 @@ def parse_args():
                     help="give the step the row summary of the inpaint mask (gs_mask_rows), so "
                          "bands whose mask is 0 on every row skip reading the prediction; "
                          "the roofline then counts only the bytes still required")
+    ap.add_argument("--mask-spans", action="store_true",
+                    help="give the step the span summary of the inpaint mask (gs_mask_spans): "
+                         "as --mask-rows, and the bands still read load uncond and cond only "
+                         "over their nonzero mask columns")
+    ap.add_argument("--unit-tail", action="store_true",
+                    help="bucketized workloads: a step curve 3.0 -> 1.0 at 20 %% progress, so "
+                         "most samples have scale exactly 1, and the step skips their uncond "
+                         "reads (unit_scale_skip)")
     ap.add_argument("--sampler", choices=["euler", "euler_ancestral"], default="euler",
                     help="the sampler of the step: the deterministic Euler update (default) or "
                          "Euler-ancestral (eta 1, a fresh noise tensor read per step)")
@@ -116,9 +127,26 @@ def parse_args():
                          "workloads; reads the run's fixed noise for the blended samples)")
     ap.add_argument("--negative-regions", type=int, default=0,
                     help="the first K regions belong to the uncond branch (regional uncond)")
-    ap.add_argument("--cpu-procs", type=int, default=1,
-                    help="oracle processes timed at once for cpu_baseline / --impl reference")
-    return ap.parse_args()
+    ap.add_argument("--cpu-procs", type=int, default=0,
+                    help="oracle processes timed at once for cpu_baseline / --impl reference "
+                         "(default: one per host core this process may run on)")
+    ap.add_argument("--api-steps", type=int, default=2000,
+                    help="steps of the per-call API leg (host calls without a CUDA graph); "
+                         "0 skips it")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing every target workload after the headline")
+    args = ap.parse_args()
+    if args.cpu_procs <= 0:
+        args.cpu_procs = host_cores()
+    return args
+
+
+def host_cores() -> int:
+    """Host cores this process may run on (the affinity mask, else the CPU count)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
 
 
 def workload_for(args):
@@ -155,6 +183,14 @@ def workload_for(args):
             raise SystemExit("--model-in needs an inpaint workload")
         wl = dataclasses.replace(wl, model_input=True)
         name += "@model_in"
+    if getattr(args, "unit_tail", False):
+        if wl.guidance.cfg is not None:
+            raise SystemExit("--unit-tail needs a bucketized-guidance workload")
+        wl = dataclasses.replace(wl, guidance=dataclasses.replace(
+            wl.guidance, curve="step", v0=3.0, v1=1.0, edge=0.2))
+        name += "@unit_tail"
+    if getattr(args, "mask_spans", False) and getattr(args, "mask_rows", False):
+        raise SystemExit("--mask-spans and --mask-rows are alternatives")
     return dataclasses.replace(wl, name=name)
 
 
@@ -262,7 +298,7 @@ def plan(wl, world, dev):
     return sig_np, lut_np
 
 
-def build_sets(wl, R, dev, sig_np, lut_np, seed=0, mask_rows=False):
+def build_sets(wl, R, dev, sig_np, lut_np, seed=0, mask_rows=False, mask_spans=False):
     """R rotating input sets on the device, plus the shared per-run state."""
     import torch
 
@@ -324,6 +360,8 @@ def build_sets(wl, R, dev, sig_np, lut_np, seed=0, mask_rows=False):
             st["orig"] = origs[k]
             if mask_rows:
                 st["mask_rows"] = gs.mask_rows(masks[k])      # once per set, outside timing
+            if mask_spans:
+                st["mask_spans"] = gs.mask_spans(masks[k])    # once per set, outside timing
             if nm < wl.B:
                 pres = torch.zeros(wl.B, dtype=torch.uint8, device=dev)
                 pres[:nm] = 1
@@ -340,14 +378,16 @@ def build_sets(wl, R, dev, sig_np, lut_np, seed=0, mask_rows=False):
     return sets, sig, lut, steps
 
 
-def step_kwargs(wl, st, sig, lut, pdl, tma=True):
-    kw = dict(sigmas=sig, regions=st["regions"], pdl=pdl, tma=tma)
+def step_kwargs(wl, st, sig, lut, pdl, tma=True, unit_skip=False):
+    kw = dict(sigmas=sig, regions=st["regions"], pdl=pdl, tma=tma, unit_scale_skip=unit_skip)
     if "stacked" in st:
         kw["stacked"] = st["stacked"]
     else:
         kw["uncond"] = st["uncond"]
     if "mask_rows" in st:
         kw["mask_rows"] = st["mask_rows"]
+    if "mask_spans" in st:
+        kw["mask_spans"] = st["mask_spans"]
     if "idx" in st:
         kw["step_idx"] = st["idx"]
     else:
@@ -390,11 +430,221 @@ def capture(launches, stream):
     return g
 
 
+# configs[1..4] of the measurement plan, timed in the same process as the headline
+TARGET_WORKLOADS = ("bcg_bf16_b16", "area_fp16_b8", "inpaint_bcg_bf16_b32", "sweep_bf16_b64")
+# floor on the steps of each per-workload timing: a short timed region would be
+# dominated by the graph launch around it
+PER_WORKLOAD_MIN_STEPS = 2000
+
+
+def block_stream(stream, us: float = 300.0) -> None:
+    """Hold the stream with a short device-side spin before the start event, so the
+    host enqueues the timed launches while the GPU is still busy and the timed region
+    holds no host submission gap (outside the timed region: before its start event)."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2000))        # ~2 GHz SM clock: cycles for `us`
+
+
+class Timed:
+    """One workload's rotating input sets, launch arguments and CUDA graphs."""
+
+    def __init__(self, wl, args, world, rank, dev, l2, mask_rows=False, mask_spans=False,
+                 unit_skip=False):
+        from bucketized_guidance_step_gb300 import gs
+        self.wl = wl
+        sig_np, lut_np = plan(wl, world, dev)
+        one, _, _, _ = build_sets(wl, 1, dev, sig_np, lut_np, seed=1234 + rank)
+        self.per_set = set_bytes(wl, one[0])
+        del one
+        self.R = max(2, math.ceil(4 * l2 / self.per_set))
+        self.use_rows = mask_rows and wl.inpaint
+        self.use_spans = mask_spans and wl.inpaint
+        self.unit_skip = unit_skip
+        self.sets, self.sig, self.lut, self.steps = build_sets(
+            wl, self.R, dev, sig_np, lut_np, seed=1234 + rank, mask_rows=self.use_rows,
+            mask_spans=self.use_spans)
+        self.prepared = [gs.make_step_args(st["x"], **step_kwargs(wl, st, self.sig, self.lut,
+                                                                  not args.no_pdl,
+                                                                  not args.no_tma, unit_skip))
+                         for st in self.sets]
+        self.kernel = gs.kernel_kind(self.prepared[0][0])
+        self.graphs = {}
+
+    def graph(self, n, stream):
+        """A CUDA graph of n back-to-back launches over the rotating sets (cached)."""
+        from bucketized_guidance_step_gb300 import gs
+        if n not in self.graphs:
+            args = [self.prepared[k % self.R][0] for k in range(n)]
+            self.graphs[n] = capture([(lambda a=a: gs.launch_step(a)) for a in args], stream)
+        return self.graphs[n]
+
+    def time(self, K, W, stream, dev, pg, soak_s=0.0, clocks=None):
+        """Milliseconds for exactly K steps (graph replays of R launches, then a graph of
+        the remainder), after W untimed warm-up launches and an optional soak."""
+        import torch
+
+        from bucketized_guidance_step_gb300 import gs
+        with torch.cuda.stream(stream):
+            for k in range(W):
+                gs.launch_step(self.prepared[k % self.R][0])
+            torch.cuda.synchronize(dev)
+            g_full = self.graph(self.R, stream)
+            rem = K % self.R
+            g_rem = self.graph(rem, stream) if rem else None
+            g_full.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            torch.cuda.synchronize(dev)
+            if clocks is not None:
+                clocks.start()
+            t_end = time.time() + soak_s                    # load the GPU while clocks settle
+            while time.time() < t_end:
+                g_full.replay()
+                torch.cuda.synchronize(dev)
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            if pg is not None:
+                pg.barrier()
+            torch.cuda.synchronize(dev)
+            block_stream(stream)
+            start.record(stream)
+            for _ in range(K // self.R):
+                g_full.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            end.record(stream)
+            torch.cuda.synchronize(dev)
+            if pg is not None:
+                pg.barrier()
+        clk = clocks.stop() if clocks is not None else None
+        return start.elapsed_time(end), clk
+
+    @property
+    def key(self):
+        """The workload's name with its mask summary (the traffic table's key)."""
+        return self.wl.name + ("+mask_rows" if self.use_rows else
+                               "+mask_spans" if self.use_spans else "")
+
+    def algorithmic_bytes(self):
+        """Bytes the step must move (``accounting.step_bytes``); with a mask summary or the
+        uncond skip at scale 1, the bytes still required given the data, per 32-byte
+        sector (``accounting.required_bytes``), averaged over the rotating sets."""
+        from bucketized_guidance_step_gb300.workloads import step_inputs
+        wl = self.wl
+        proto = step_inputs(wl, 0, B=1)
+        if not (self.use_rows or self.use_spans or self.unit_skip):
+            return algorithmic_bytes(wl, proto.regions)
+        return sum(self.required_bytes(st, proto) for st in self.sets) // len(self.sets)
+
+    def required_bytes(self, st, proto):
+        import numpy as np
+
+        from bucketized_guidance_step_gb300.accounting import required_bytes
+        wl = self.wl
+        mask_nz = present = unit = None
+        if wl.inpaint and (self.use_rows or self.use_spans):
+            mask_nz = (st["mask"][:, 0] != 0).cpu().numpy()
+            nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
+            present = np.arange(wl.B) < nm
+        if self.unit_skip:
+            lut = self.lut.cpu().numpy() if self.lut is not None else None
+            idx = st["idx"].cpu().numpy() if "idx" in st else np.zeros(wl.B, np.int64)
+            s = lut[idx] if lut is not None else np.full(wl.B, np.float32(wl.guidance.cfg))
+            unit = s == 1.0
+        return required_bytes(wl.B, wl.C, wl.H, wl.W, wl.dtype, uncond=True,
+                              cond=wl.full_frame_cond,
+                              regions=[(r.y0, r.x0, r.h, r.w, r.pitch) for r in proto.regions],
+                              mask_nz=mask_nz, present=present, unit_scale=unit,
+                              noise=wl.sampler == "euler_ancestral",
+                              model_input=wl.model_input)
+
+
+def run_api(timed, stream, dev, n: int):
+    """Per-call cost of the public API without CUDA graphs: host calls of
+    gs_guided_step, one per step, rotating the input sets.
+
+    host_us_per_call: host time of one call (Python binding, argument checks,
+    tensor-map encoding and the launch), the best of 10 bursts of 100 calls (a burst
+    this short never fills the launch queue, which would make calls wait for the
+    GPU); device_us_per_step: the step time this mode reaches over n calls in a row
+    (the larger of the kernel time and the host cost); ctypes_call_us and
+    checks_and_encode_us: a trivial call into the library and gs_step_kernel_kind
+    (the same checks and encoding, no launch), the parts of the host cost before the
+    launch itself."""
+    import torch
+
+    from bucketized_guidance_step_gb300 import gs
+    lib = gs.load()
+    R = timed.R
+    args = [a for a, _ in timed.prepared]
+    burst = 100
+    with torch.cuda.stream(stream):
+        for k in range(min(n, 50)):
+            gs.launch_step(args[k % R], stream)
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(10):
+            t0 = time.perf_counter()
+            for k in range(burst):
+                gs.launch_step(args[k % R], stream)
+            best = min(best, time.perf_counter() - t0)
+            torch.cuda.synchronize(dev)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(n):
+            gs.launch_step(args[k % R], stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    dev_ms = start.elapsed_time(end)
+    t2 = time.perf_counter()
+    for _ in range(n):
+        lib.gs_abi_version()
+    t3 = time.perf_counter()
+    for k in range(n):
+        gs.kernel_kind(args[k % R])
+    t4 = time.perf_counter()
+    return {"steps": n,
+            "host_us_per_call": round(best / burst * 1e6, 3),
+            "device_us_per_step": round(dev_ms * 1e3 / n, 3),
+            "ctypes_call_us": round((t3 - t2) / n * 1e6, 3),
+            "checks_and_encode_us": round((t4 - t3) / n * 1e6, 3),
+            "mode": "one gs_guided_step call per step from Python (ctypes), no CUDA graph, "
+                    "rotating input sets"}
+
+
+def traffic_entry(name: str):
+    """(read, write) DRAM bytes per launch of the captured revision, else None."""
+    tr = TRAFFIC.get(name)
+    if tr is None or tr[2] != kernel_source_hash():
+        return None
+    return tr[0], tr[1]
+
+
+def roofline(abytes, ms, K, peak, peak_src, traffic_key):
+    achieved = abytes / (ms / 1e3 / K) / 1e9
+    rw = traffic_entry(traffic_key)
+    out = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+           "frac": round(achieved / peak, 4),
+           "traffic": None if rw is None else rw[0] + rw[1],
+           "dram_read": None if rw is None else rw[0],
+           "dram_write": None if rw is None else rw[1],
+           "algorithmic_bytes": abytes, "peak_source": peak_src,
+           "nominal_peak": NOMINAL_HBM_GBS,
+           "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)}
+    if rw is not None:
+        out["traffic_note"] = (
+            "one ncu capture of one launch (dram__bytes_read.sum + dram__bytes_write.sum); "
+            "x_out is written into the 129 MB L2 and reaches DRAM after the launch ends, "
+            "so dram_write sees only the lines evicted during the launch")
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
 
     from bucketized_guidance_step_gb300 import gs
-    from bucketized_guidance_step_gb300.workloads import workload
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -407,117 +657,100 @@ def run_ours(args, world, rank, local):
     wl = workload_for(args)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-
-    sig_np, lut_np = plan(wl, world, dev)
-    one, sig, lut, steps = build_sets(wl, 1, dev, sig_np, lut_np, seed=1234 + rank)
-    per_set = set_bytes(wl, one[0])
-    R = max(2, math.ceil(4 * l2 / per_set))
-    del one
-    use_rows = args.mask_rows and wl.inpaint
-    sets, sig, lut, steps = build_sets(wl, R, dev, sig_np, lut_np, seed=1234 + rank,
-                                       mask_rows=use_rows)
-    prepared = []
-    for st in sets:
-        a, keep = gs.make_step_args(st["x"], **step_kwargs(wl, st, sig, lut, (not args.no_pdl),
-                                                            not args.no_tma))
-        prepared.append((a, keep))
-    kernel = gs.kernel_kind(prepared[0][0])
-
-    def launcher(a):
-        return lambda: gs.launch_step(a)
-
     stream = torch.cuda.Stream(dev)
     K, W = args.steps, args.warmup
-    with torch.cuda.stream(stream):
-        for k in range(W):                                  # untimed warm-up steps
-            gs.launch_step(prepared[k % R][0])
-        torch.cuda.synchronize(dev)
-        g_full = capture([launcher(a) for a, _ in prepared], stream)
-        rem = K % R
-        g_rem = capture([launcher(prepared[k][0]) for k in range(rem)], stream) if rem else None
-        g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        torch.cuda.synchronize(dev)
+    peak, peak_src = hbm_peak()
 
-        clocks = ClockSampler(local)
-        clocks.start()
-        t_end = time.time() + args.soak_seconds             # load the GPU while clocks settle
-        while time.time() < t_end:
-            g_full.replay()
-            torch.cuda.synchronize(dev)
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if pg is not None:
-            pg.barrier()
-        torch.cuda.synchronize(dev)
-        start.record(stream)
-        for _ in range(K // R):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        end.record(stream)
-        torch.cuda.synchronize(dev)
-        if pg is not None:
-            pg.barrier()
-        clk = clocks.stop()
-    ms = start.elapsed_time(end)
+    timed = Timed(wl, args, world, rank, dev, l2, mask_rows=args.mask_rows,
+                  mask_spans=args.mask_spans, unit_skip=args.unit_tail)
+    ms, clk = timed.time(K, W, stream, dev, pg, soak_s=args.soak_seconds,
+                         clocks=ClockSampler(local))
     ms_max = ms
     if pg is not None:
         from bucketized_guidance_step_gb300 import dist as D
         ms_max = D.max_over_ranks(ms, device=dev)
 
     # --- end to end: pinned host buffers in, result out, every step ---------
-    e2e = run_e2e(args, wl, sets, sig, lut, stream, dev, pg)
+    e2e = run_e2e(args, wl, timed.sets, timed.sig, timed.lut, stream, dev, pg)
+    api = run_api(timed, stream, dev, args.api_steps) if args.api_steps > 0 else None
 
-    from bucketized_guidance_step_gb300.workloads import step_inputs
-    proto = step_inputs(wl, 0, B=1)
-    abytes = algorithmic_bytes(wl, proto.regions)
-    if use_rows:
-        # required bytes: minus the prediction rows a blended sample's zero mask rows make
-        # unnecessary, averaged over the rotating sets' masks
-        from bucketized_guidance_step_gb300.accounting import skipped_prediction_bytes
-        nm = wl.B if wl.inpaint_samples is None else wl.inpaint_samples
-        skipped = 0
-        for st in sets:
-            zero = (st["mask"][:nm, 0] == 0).all(dim=-1).cpu().numpy()
-            skipped += skipped_prediction_bytes(zero, wl.C, wl.W, wl.dtype,
-                                                cond=wl.full_frame_cond,
-                                                regions=[(r.y0, r.h, r.w) for r in proto.regions])
-        abytes -= skipped // len(sets)
-    elems = wl.elements
+    abytes = timed.algorithmic_bytes()
     sec_step = ms_max / 1e3 / K
-    value = world * elems / sec_step / 1e9
-    achieved = abytes / (ms / 1e3 / K) / 1e9
-    peak, peak_src = hbm_peak()
-    tr = TRAFFIC.get(wl.name + ("+mask_rows" if use_rows else ""))
-    traffic = tr[0] if tr and tr[1] == kernel_source_hash() else None
-
+    value = world * wl.elements / sec_step / 1e9
+    rl = roofline(abytes, ms, K, peak, peak_src, timed.key)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": wl.dtype,
         "data": "synthetic",
         "config": {"workload": describe(wl), "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W,
-                   "l2": f"{R} rotating input sets of {per_set} B (>= 4x L2 of {l2} B)",
-                   "launch": "CUDA graph replay" + (", PDL" if (not args.no_pdl) else ""),
-                   "kernel": kernel,
-                   "mask_rows": ("row summary given: bands whose mask is 0 on every row skip "
-                                 "the prediction reads; bytes counted as still required")
-                   if use_rows else None,
-                   "tuning": {k: os.environ[k] for k in ("GS_TMA_ROWS", "GS_TMA_CHANNELS", "GS_STEP_CHANNELS")
+                   "l2": f"{timed.R} rotating input sets of {timed.per_set} B "
+                         f"(>= 4x L2 of {l2} B)",
+                   "launch": "CUDA graph replay" + (", PDL" if (not args.no_pdl) else "") +
+                             "; a device-side spin holds the stream while the timed "
+                             "launches are enqueued (before the start event)",
+                   "kernel": timed.kernel,
+                   "mask_summary": ("row summary given: bands whose mask is 0 on every row "
+                                    "skip the prediction reads" if timed.use_rows else
+                                    "span summary given: bands whose mask is 0 skip the "
+                                    "prediction reads, the others read uncond and cond only "
+                                    "over their nonzero mask columns" if timed.use_spans
+                                    else None),
+                   "unit_scale_skip": ("samples of scale exactly 1 skip their uncond reads"
+                                       if timed.unit_skip else None),
+                   "bytes": ("required bytes given the data, per 32-byte sector"
+                             if (timed.use_rows or timed.use_spans or timed.unit_skip)
+                             else "algorithmic bytes"),
+                   "tuning": {k: os.environ[k] for k in ("GS_TMA_ROWS", "GS_TMA_CHANNELS",
+                                                          "GS_STEP_CHANNELS")
                               if k in os.environ},
                    "parallelism": f"replicas x{world} (independent batches)"},
         "kernel_sources": kernel_source_hash(),
-        "hbm_gbs": round(world * achieved, 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": abytes, "peak_source": peak_src,
-                     "nominal_peak": NOMINAL_HBM_GBS,
-                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
+        "hbm_gbs": round(world * rl["achieved"], 1),
+        "roofline": rl,
         "e2e": e2e,
         "gpu_launches": K,
         "clocks": clk,
     }
+    if api is not None:
+        line["api"] = api
+    del timed
+    torch.cuda.empty_cache()
+
+    # --- every target workload, same process, same clocks --------------------
+    if not args.no_per_config:
+        per, launches = {}, 0
+        Kc = max(K, PER_WORKLOAD_MIN_STEPS)
+        clocks = ClockSampler(local)
+        clocks.start()
+        for name in TARGET_WORKLOADS:
+            from bucketized_guidance_step_gb300.workloads import workload
+            w2 = workload(name)
+            t2 = Timed(w2, args, world, rank, dev, l2)
+            ms2, _ = t2.time(Kc, W, stream, dev, pg, soak_s=0.3)
+            if pg is not None:
+                from bucketized_guidance_step_gb300 import dist as D
+                ms2 = D.max_over_ranks(ms2, device=dev)
+            r2 = roofline(t2.algorithmic_bytes(), ms2, Kc, peak, peak_src, name)
+            api2 = run_api(t2, stream, dev, args.api_steps) if args.api_steps > 0 else None
+            per[name] = {"value": round(world * w2.elements / (ms2 / 1e3 / Kc) / 1e9, 3),
+                         "ms_per_step": ms2 / Kc, "steps": Kc, "achieved_gbs": r2["achieved"],
+                         "frac": r2["frac"], "algorithmic_bytes": r2["algorithmic_bytes"],
+                         "traffic": r2["traffic"], "dram_read": r2["dram_read"],
+                         "dram_write": r2["dram_write"], "kernel": t2.kernel,
+                         "input_sets": t2.R}
+            if api2 is not None:
+                per[name]["api"] = {k: api2[k] for k in ("host_us_per_call",
+                                                         "device_us_per_step")}
+            launches += Kc
+            del t2
+            torch.cuda.empty_cache()
+        line["per_config"] = per
+        line["per_config_clocks"] = clocks.stop()
+        line["per_config_note"] = (f"each workload timed as the headline is (rotating L2-cold "
+                                   f"sets, graph replay, PDL), {Kc} steps (at least "
+                                   f"{PER_WORKLOAD_MIN_STEPS}), after the headline")
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, args.cpu_procs)
     if pg is not None:

@@ -12,11 +12,17 @@ Every latent-shaped input is read once and every output written once:
 
 with P = H W; the 2 is the read of x and the write of x_out.  Sigmas, the scale
 table and the step indices (under 1 KiB) are left out.
+
+``required_bytes`` refines this with the data: per 32-byte sector, the prediction a
+blended sample's zero mask makes unnecessary and the uncond of samples of scale 1
+are not required.
 """
 
 from __future__ import annotations
 
 from typing import Iterable, Tuple
+
+import numpy as np
 
 ESIZE = {"fp32": 4, "bf16": 2, "fp16": 2}
 
@@ -58,4 +64,73 @@ def skipped_prediction_bytes(zero_rows, C: int, W: int, dtype: str, *, cond: boo
         for y, zero in enumerate(rows):
             if zero:
                 total += frame_row + sum(C * w * e for y0, h, w in regions if y0 <= y < y0 + h)
+    return total
+
+
+SECTOR = 32          # bytes: the unit in which DRAM and L2 move data
+
+
+def _needed_bytes(nz, addr, e: int) -> int:
+    """Bytes of the given elements that share a 32-byte sector with a needed element.
+
+    nz: bool [n] (element needed); addr: int [n], each element's byte address from a
+    32-byte-aligned base; e: element size (a divisor of 32, so no element straddles
+    two sectors)."""
+    sec = np.asarray(addr, dtype=np.int64) // SECTOR
+    lo = int(sec.min())
+    hit = np.zeros(int(sec.max()) - lo + 1, dtype=bool)
+    hit[sec[np.asarray(nz, dtype=bool)] - lo] = True
+    return int(hit[sec - lo].sum()) * e
+
+
+def required_bytes(B: int, C: int, H: int, W: int, dtype: str, *, uncond: bool = True,
+                   cond: bool = True, regions: Iterable[Tuple[int, int, int, int, int]] = (),
+                   mask_nz=None, present=None, unit_scale=None, denoised_out: bool = False,
+                   noise: bool = False, model_input: bool = False) -> int:
+    """The bytes a step must move given its data, counted per 32-byte sector.
+
+    Start from ``step_bytes``.  A blended sample needs its prediction (uncond, cond and
+    the regional outputs) only where its mask is nonzero ([SAMPLING] "inpaint 与 mask":
+    den = m pred + (1 - m) original is the original where m = 0); memory moves whole
+    32-byte sectors, so a prediction element is required when its sector holds an
+    element at a nonzero mask pixel.  A sample whose scale is exactly 1 needs no uncond
+    at all when the step is asked to skip it ("cfg = 1 的优化", per sample).
+
+    regions: (y0, x0, h, w, pitch) per regional output.  mask_nz: bool [B, H, W]
+    (mask != 0) or None; present: bool [B], the samples that blend (None: all, with a
+    mask); unit_scale: bool [B], the samples that skip their uncond, or None.  Every
+    tensor is taken to start on a 32-byte boundary; row y of plane (b, c) starts
+    ((b C + c) H + y) W |T| bytes in, row t of a regional slab ((b C + c) h + t) pitch
+    |T| bytes in.
+    """
+    e = ESIZE[dtype]
+    regions = list(regions)
+    nm = 0
+    if mask_nz is not None:
+        present = np.ones(B, bool) if present is None else np.asarray(present, bool)
+        nm = int(present.sum())
+    total = step_bytes(B, C, H, W, dtype, uncond=uncond, cond=cond,
+                       regions=[(h, w) for _, _, h, w, _ in regions], inpaint_samples=nm,
+                       denoised_out=denoised_out, noise=noise, model_input=model_input)
+    skip_u = np.zeros(B, bool) if unit_scale is None else np.asarray(unit_scale, bool)
+    plane = C * H * W * e
+    if uncond:
+        total -= int(skip_u.sum()) * plane
+    if mask_nz is None:
+        return total
+    m = np.asarray(mask_nz, dtype=bool)
+    for b in np.flatnonzero(present):
+        planes = (1 if cond else 0) + (1 if uncond and not skip_u[b] else 0)
+        if planes:
+            # sample b's block [C][H][W] of a frame tensor; the mask row is the same
+            # for every channel
+            c, y, x = np.meshgrid(np.arange(C), np.arange(H), np.arange(W), indexing="ij")
+            addr = (((b * C + c) * H + y) * W + x) * e
+            nz = np.broadcast_to(m[b][None], (C, H, W))
+            total -= planes * (plane - _needed_bytes(nz.ravel(), addr.ravel(), e))
+        for (y0, x0, h, w, pitch) in regions:
+            c, t, x = np.meshgrid(np.arange(C), np.arange(h), np.arange(w), indexing="ij")
+            addr = (((b * C + c) * h + t) * pitch + x) * e
+            nz = np.broadcast_to(m[b, y0:y0 + h, x0:x0 + w][None], (C, h, w))
+            total -= C * h * w * e - _needed_bytes(nz.ravel(), addr.ravel(), e)
     return total

@@ -59,6 +59,11 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
     if (a->mask_rows != nullptr &&
         (a->inpaint_mask == nullptr || (reinterpret_cast<uintptr_t>(a->mask_rows) & 3u) != 0))
         return GS_ERR_INVALID_ARG;
+    if (a->mask_spans != nullptr &&
+        (a->inpaint_mask == nullptr || (reinterpret_cast<uintptr_t>(a->mask_spans) & 3u) != 0 ||
+         a->W > 65535))
+        return GS_ERR_INVALID_ARG;
+    if (a->unit_scale_skip != 0 && a->unit_scale_skip != 1) return GS_ERR_INVALID_ARG;
     if (static_cast<long long>(a->B) * a->C * a->H * a->W > (1ll << 46)) return GS_ERR_UNSUPPORTED;
     if (a->sampler != GS_SAMPLER_EULER && a->sampler != GS_SAMPLER_EULER_ANCESTRAL)
         return GS_ERR_INVALID_ARG;
@@ -92,6 +97,8 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
     p.present = a->mask_present;
     p.orig = a->inpaint_mask != nullptr ? a->original : nullptr;
     p.mask_rows = a->mask_rows;        // used by the TMA-fed kernel only
+    p.mask_spans = a->mask_spans;      // likewise
+    p.unit_skip = a->unit_scale_skip != 0 && a->uncond != nullptr ? 1 : 0;   // likewise
     p.sampler = a->sampler;
     p.noise = a->sampler == GS_SAMPLER_EULER_ANCESTRAL ? a->noise : nullptr;
     p.model_in = a->model_in_out;

@@ -13,7 +13,9 @@
 //
 // gs_mask_rows summarises a latent mask by row (which rows hold any nonzero
 // value) for the guided step's read skipping: one CTA per 32-row word, one warp
-// per row at a time, each lane reading every 32nd column.
+// per row at a time, each lane reading every 32nd column.  gs_mask_spans records
+// each row's nonzero column span instead (one warp per row, a warp-wide min / max
+// of the lanes' first and last nonzero columns).
 #include <cuda_runtime.h>
 
 #include "gs.h"
@@ -81,7 +83,40 @@ __global__ void __launch_bounds__(256) mask_rows_kernel(const float* __restrict_
     if (threadIdx.x == 0) out[b * words + wi] = bits;
 }
 
+// Row y of mask b: [lo, hi) = from its first to one past its last nonzero column,
+// packed as lo | hi << 16 (0 for a row with no nonzero value).  Grid (row blocks of
+// 8, masks), 256 threads: one warp per row.
+__global__ void __launch_bounds__(256) mask_spans_kernel(const float* __restrict__ m, int H,
+                                                         int W, unsigned* __restrict__ out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int y = blockIdx.x * 8 + warp;
+    const long long b = blockIdx.y;
+    if (y >= H) return;
+    const float* row = m + (b * H + y) * static_cast<long long>(W);
+    unsigned lo = 0xffffu, hi = 0u;
+    for (int x = lane; x < W; x += 32) {
+        if (__ldg(row + x) != 0.0f) {
+            lo = min(lo, static_cast<unsigned>(x));
+            hi = static_cast<unsigned>(x) + 1u;          // x grows: the last one wins
+        }
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) out[b * H + y] = hi > 0u ? (lo | (hi << 16)) : 0u;
+}
+
 }  // namespace
+
+extern "C" gs_status gs_mask_spans(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
+                                   uint32_t* spans_out, gs_stream stream) {
+    if (lat_mask == nullptr || spans_out == nullptr) return GS_ERR_INVALID_ARG;
+    if (Bm < 1 || H < 1 || W < 1) return GS_ERR_INVALID_ARG;
+    if (Bm > 65535 || W > 65535) return GS_ERR_UNSUPPORTED;
+    mask_spans_kernel<<<dim3(static_cast<unsigned>((H + 7) / 8), static_cast<unsigned>(Bm)), 256,
+                        0, reinterpret_cast<cudaStream_t>(stream)>>>(lat_mask, H, W, spans_out);
+    if (cudaGetLastError() != cudaSuccess) return GS_ERR_CUDA;
+    return GS_OK;
+}
 
 extern "C" gs_status gs_mask_rows(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
                                   uint32_t* rows_out, gs_stream stream) {

@@ -57,6 +57,8 @@ struct StepParams {
     const unsigned char* present;
     const void* orig;
     const unsigned* mask_rows;   // row summary of imask (gs_mask_rows) or null
+    const unsigned* mask_spans;  // per-row nonzero column spans of imask (gs_mask_spans) or null
+    int unit_skip;               // 1: samples of scale exactly 1 read no uncond (TMA kernel)
     int sampler;                 // GS_SAMPLER_*
     const void* noise;           // ancestral noise or null
     void* model_in;              // second output (next model input) or null

@@ -30,17 +30,20 @@ EncodeTiled encoder() {
     return fn;
 }
 
-// A 3-D tiled map of a dense [d2][d1][d0] tensor with a [b2][b1][b0] box.
+// A 3-D tiled map of a dense [d2][d1][d0] tensor with a [b2][b1][b0] box.  Boxes
+// whose rows are whole 256-byte lines or more let L2 fetch whole 256-byte lines;
+// narrower boxes (the column chunks of the narrowed prediction reads) fetch only the
+// sectors they touch, or the narrowing would bring in the columns it skips.
 bool encode3d(CUtensorMap* m, CUtensorMapDataType dt, unsigned esize, const void* base,
               unsigned long long d0, unsigned long long d1, unsigned long long d2,
-              unsigned long long pitch_elems, unsigned b0, unsigned b1, unsigned b2) {
+              unsigned long long pitch_elems, unsigned b0, unsigned b1, unsigned b2,
+              CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {pitch_elems * esize, pitch_elems * d1 * esize};
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
     return encoder()(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, promo,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -158,8 +161,12 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     p.has_c = sp.c != nullptr;
     p.mask_shared = inp && sp.imask_bstride == 0;
     p.test_wait_timeout = (flags & GS_LAUNCH_TEST_WAIT_TIMEOUT) ? 1 : 0;
-    // (the negative-region instances do not skip reads)
-    p.mask_rows = inp && !neg ? sp.mask_rows : nullptr;
+    // (the negative-region instances do not skip reads; the span summary takes the
+    // place of the row summary)
+    p.mask_spans = inp && !neg ? sp.mask_spans : nullptr;
+    p.mask_rows = inp && !neg && p.mask_spans == nullptr ? sp.mask_rows : nullptr;
+    p.unit_skip = !neg && sp.unit_skip != 0 && sp.u != nullptr ? 1 : 0;
+    p.chunk_bytes = static_cast<unsigned>(cg) * rb * static_cast<unsigned>(kChunkBytes);
     p.sampler = sp.sampler;
     p.model_in = sp.model_in;
     for (int r = 0; r < sp.n_regions; ++r)
@@ -228,6 +235,13 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     bool ok = encode3d(&p.tm_x, dt, es, sp.x, W, H, bc, W, W, rb, cg);
     if (p.has_u) ok = ok && encode3d(&p.tm_u, dt, es, sp.u, W, H, bc, W, W, rb, cg);
     if (p.has_c) ok = ok && encode3d(&p.tm_c, dt, es, sp.c, W, H, bc, W, W, rb, cg);
+    if (p.mask_spans != nullptr) {
+        // column chunks of 64 bytes for the prediction boxes narrowed to the mask
+        const unsigned chunk = static_cast<unsigned>(kChunkBytes) / es;
+        const CUtensorMapL2promotion np = CU_TENSOR_MAP_L2_PROMOTION_NONE;
+        if (p.has_u) ok = ok && encode3d(&p.tm_uc, dt, es, sp.u, W, H, bc, W, chunk, rb, cg, np);
+        if (p.has_c) ok = ok && encode3d(&p.tm_cc, dt, es, sp.c, W, H, bc, W, chunk, rb, cg, np);
+    }
     if (inp) {
         ok = ok && encode3d(&p.tm_o, dt, es, sp.orig, W, H, bc, W, W, rb, cg);
         ok = ok && encode3d(&p.tm_m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sp.imask, W, H,

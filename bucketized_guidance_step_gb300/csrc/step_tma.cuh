@@ -22,8 +22,9 @@
 // the loads of some overlap the arithmetic of others, and the CTA scheduler
 // hands out tiles as SMs drain.
 //
-// Every mbarrier wait is bounded (200 ms of %globaltimer); on expiry the thread
-// sets GS_DEV_TIMEOUT in the status word and returns.
+// Every mbarrier wait is bounded (200 ms of %globaltimer); on expiry the CTA sets
+// GS_DEV_TIMEOUT in the status word, one thread waits (10 ms at most) for the boxes
+// already issued to land, and the CTA returns without writing its tile.
 //
 // This header holds the launch parameters, the kernel template and its launch
 // templates; step_tma.cu builds the parameters and launches the deterministic
@@ -72,6 +73,7 @@ constexpr int kRegionNegative = 16;
 
 struct TmaParams {
     CUtensorMap tm_x, tm_u, tm_c, tm_o, tm_m;
+    CUtensorMap tm_uc, tm_cc;    // uncond and cond with column-chunk boxes (mask_spans)
     CUtensorMap tm_n, tm_on;     // the ancestral step's noise, the run's fixed noise
     CUtensorMap tm_r[GS_MAX_REGIONS];
     TmaRegion reg[GS_MAX_REGIONS];
@@ -98,7 +100,14 @@ struct TmaParams {
     int sampler;                 // GS_SAMPLER_*
     void* model_in;              // next model input under the inpaint wrapper, or null
     unsigned off_n, off_on;      // stage offsets of the noise and fixed-noise boxes
+    const unsigned* mask_spans;  // per-row nonzero column spans of the inpaint mask, or null
+    int unit_skip;               // 1: a sample whose scale is exactly 1 reads no uncond
+    unsigned chunk_bytes;        // CG * RB * kChunkCols * element size (column-chunk boxes)
 };
+
+// Column chunks of the narrowed prediction boxes: 64 bytes of a row (two DRAM
+// sectors), i.e. 32 16-bit or 16 fp32 elements.
+constexpr int kChunkBytes = 64;
 
 // Launch the instances with the sampler options (ancestral noise and/or the next
 // model input); defined in step_tma_sampler.cu.
@@ -129,6 +138,14 @@ __device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
 // Add bytes the current phase must receive before it can complete (no arrival).
 __device__ __forceinline__ void mbar_add_tx(unsigned bar, unsigned bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Retire bytes the current phase was told to expect (no data moves): used after an
+// expired wait in the error-path test, whose extra expected bytes never arrive, so
+// that the drain below can still tell when the real boxes have landed.
+__device__ __forceinline__ void mbar_complete_tx(unsigned bar, unsigned bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
 
@@ -173,6 +190,15 @@ __device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity) {
     return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
+// After a wait on `bar` expired: let the boxes already issued on it land (bounded)
+// before the CTA exits, so that no bulk copy writes into shared memory the SM has
+// handed to another CTA.  With the error-path test's phantom bytes on the barrier,
+// they are retired first (the phase then completes once the real boxes are in).
+__device__ __forceinline__ void mbar_drain(unsigned bar, bool phantom) {
+    if (phantom) mbar_complete_tx(bar, 16u);
+    (void)mbar_wait_for(bar, 0, kDrainLimitNs);
+}
+
 __device__ __forceinline__ void tma_load_3d(unsigned dst, const CUtensorMap* map, int x, int y,
                                             int z, unsigned bar) {
     asm volatile(
@@ -190,6 +216,9 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 __device__ __forceinline__ void flag(unsigned int* status, unsigned bits) {
     if (status != nullptr) atomicOr(status, bits);
 }
+
+// The parameter thread: the first lane of warp 1, or thread 0 in one-warp tiles.
+__device__ __forceinline__ int ptid_of(int nthreads) { return nthreads > 32 ? 32 : 0; }
 
 __device__ __forceinline__ bool band_hits(const TmaRegion& R, int y_band, int RB) {
     return y_band < R.y0 + R.h && y_band + RB > R.y0;
@@ -290,6 +319,14 @@ struct TileParams {
     int inpaint;        // 1 = this sample blends with its original
     int need_pred;      // 0 = the band's mask rows are all zero: prediction not read
     int arrived;        // 0 = thread 0's wait for the tile gave up (one-group region tiles)
+    int abandon;        // 1 = thread 0's wait gave up: the tile is not written (the
+                        //     threads that see the phase complete later leave too)
+    int use_u;          // deferred instances: 0 = the uncond box was not loaded (scale 1)
+    int narrow;         // deferred instances: 1 = uncond and cond came as column chunks
+                        //     starting at frame column xs, 0 = as whole rows
+    int xs, xv;         // frame columns [xs, xv) of the prediction are read (whole
+                        //     vectors over the band's nonzero mask columns); the rest
+                        //     is taken as 0
 };
 
 // One region as this tile's threads use it, built once per CTA by the region's
@@ -308,13 +345,18 @@ struct __align__(16) TileRegion {
     int tabx;
 };
 
-template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ, bool NEG>
+template <typename T, int CG, bool REG, bool INP, bool DEFER, bool NZ, bool NEG>
 __global__ void __launch_bounds__(kMaxThreads)
     guided_step_tma_kernel(const __grid_constant__ TmaParams p) {
-    static_assert(INP || !SKIP, "read skipping needs the inpaint inputs");
+    // DEFER: the parameter thread issues the prediction boxes (uncond, cond, regions)
+    // once it knows what the tile needs: nothing for a blended band whose mask is 0
+    // on every row, uncond and cond narrowed to the band's nonzero mask columns (as
+    // column chunks) with the mask's span summary, and no uncond for a sample whose
+    // scale is exactly 1 when the caller asks for that.
     // NEG: some regions belong to the uncond branch, which is then their weighted sum
     // with the full-frame uncond output (weight 1, if given), like the positive branch
-    static_assert(!NEG || (REG && !SKIP), "negative regions: region instances only");
+    static_assert(!NEG || (REG && !DEFER), "negative regions: region instances only");
+    constexpr int kChunk = kChunkBytes / static_cast<int>(sizeof(typename T::scalar));
     using S = typename T::scalar;
     constexpr int VEC = 16 / static_cast<int>(sizeof(S));
     constexpr int NP = VEC / 2;
@@ -355,6 +397,11 @@ __global__ void __launch_bounds__(kMaxThreads)
     const int y = y_band + row;
     const int z = b * p.C + cgi * CG;
     const bool has_u = p.has_u != 0, has_c = p.has_c != 0;
+    // DEFER instances with a mask summary (row or span): the parameter thread issues
+    // every prediction box once it knows the band's mask; with only the uncond skip
+    // at scale 1, thread 0 still issues cond and the regions, and the parameter thread
+    // the uncond box alone
+    const bool summary = DEFER && INP && (p.mask_rows != nullptr || p.mask_spans != nullptr);
     // sampler options (NZ instances only): ancestral noise (a box in x's group) and
     // the next model input (the fixed noise a box in the original's group)
     const bool anc = NZ && p.sampler == GS_SAMPLER_EULER_ANCESTRAL;
@@ -371,6 +418,10 @@ __global__ void __launch_bounds__(kMaxThreads)
         prefetch_map(&p.tm_x);
         if (has_u) prefetch_map(&p.tm_u);
         if (has_c) prefetch_map(&p.tm_c);
+        if (DEFER && p.mask_spans != nullptr) {
+            if (has_u) prefetch_map(&p.tm_uc);
+            if (has_c) prefetch_map(&p.tm_cc);
+        }
         if (INP) {
             prefetch_map(&p.tm_o);
             prefetch_map(&p.tm_m);
@@ -381,12 +432,15 @@ __global__ void __launch_bounds__(kMaxThreads)
             for (int r = 0; r < p.n_regions; ++r) prefetch_map(&p.tm_r[r]);
         }
         if constexpr (kSplit) {
-            mbar_init(bar, 1u);
+            // group A: thread 0 feeds it, or the parameter thread (DEFER); with only
+            // the uncond skip at scale 1 deferred, both do
+            mbar_init(bar, DEFER && !summary && nthreads > 32 ? 2u : 1u);
             mbar_init(barB, nthreads > 32 ? 2u : 1u);
         } else {
             mbar_init(bar, nthreads > 32 ? 2u : 1u);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tp.abandon = 0;
     }
     __syncthreads();
     // Everything above touches only kernel parameters; with programmatic
@@ -396,19 +450,24 @@ __global__ void __launch_bounds__(kMaxThreads)
     grid_dependents_launch();
 
     // The prediction boxes (uncond, cond, regions) go on `bar` (group A when split).
-    // With a row summary of the inpaint mask they wait for the parameter thread,
-    // which skips them for a band whose mask rows are all zero in a blended sample.
-    // (SKIP: instances launched only when the row summary is given)
-    constexpr bool defer = SKIP;
-    auto issue_prediction = [&]() {
-        if (has_u) {
+    // In DEFER instances the parameter thread issues them (see DEFER above).
+    constexpr bool defer = DEFER;
+    // One prediction plane (uncond or cond) of the tile: one [CG][RB][W] box, or, when
+    // narrowed to frame columns [xs, xs + n * kChunk), n [CG][RB][kChunk] boxes laid
+    // out one after the other (columns past W arrive as zeros).
+    auto issue_plane = [&](unsigned off, const CUtensorMap* map, const CUtensorMap* chunk_map,
+                           bool narrow, int xs, int n) {
+        if (!narrow) {
             mbar_add_tx(bar, p.plane_bytes);
-            tma_load_3d(s0 + p.off_u, &p.tm_u, 0, y_band, z, bar);
+            tma_load_3d(s0 + off, map, 0, y_band, z, bar);
+            return;
         }
-        if (has_c) {
-            mbar_add_tx(bar, p.plane_bytes);
-            tma_load_3d(s0 + p.off_c, &p.tm_c, 0, y_band, z, bar);
-        }
+        mbar_add_tx(bar, static_cast<unsigned>(n) * p.chunk_bytes);
+        for (int j = 0; j < n; ++j)
+            tma_load_3d(s0 + off + static_cast<unsigned>(j) * p.chunk_bytes, chunk_map,
+                        xs + j * kChunk, y_band, z, bar);
+    };
+    auto issue_regions = [&]() {
         if constexpr (REG) {
             // only the four fields the issue needs, read straight from the parameters
             for (int r = 0; r < p.n_regions; ++r) {
@@ -418,6 +477,11 @@ __global__ void __launch_bounds__(kMaxThreads)
                 tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], 0, y_band - ry0, z, bar);
             }
         }
+    };
+    auto issue_prediction = [&]() {
+        if (has_u) issue_plane(p.off_u, &p.tm_u, &p.tm_uc, false, 0, 1);
+        if (has_c) issue_plane(p.off_c, &p.tm_c, &p.tm_cc, false, 0, 1);
+        issue_regions();
     };
 
     // Thread 0: the boxes that need nothing but the tile coordinates.  Each box's
@@ -432,12 +496,20 @@ __global__ void __launch_bounds__(kMaxThreads)
                 tma_load_3d(s0 + p.off_n, &p.tm_n, 0, y_band, z, bar);
             }
         }
-        if constexpr (!defer) issue_prediction();
+        if constexpr (!defer) {
+            issue_prediction();
+        } else if (!summary) {
+            if (has_c) issue_plane(p.off_c, &p.tm_c, &p.tm_cc, false, 0, 1);
+            issue_regions();
+        }
         if constexpr (kSplit) {
             if constexpr (!defer) {
                 // group A is complete: thread 0 is its only feeder
                 if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
                 mbar_arrive(bar);
+            } else {
+                // with only the uncond skip deferred, thread 0's part of group A is in
+                if (!summary && ptid_of(nthreads) != 0) mbar_arrive(bar);
             }
             mbar_add_tx(barB, p.plane_bytes);
             tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, barB);
@@ -448,18 +520,44 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
     }
 
-    // The parameter thread: the step index, the inpaint flag and (with a row
+    // The parameter thread: the step index, the inpaint flag and (with a mask
     // summary) the band's mask rows are independent loads issued together; the
     // deferred prediction boxes and the original and mask boxes go out as soon as
-    // those are known, then the scale and sigmas (which depend on the index) are
-    // read.  With a single warp, thread 0 plays both parts (its boxes first) and
-    // arrives once on each barrier.
-    const int ptid = nthreads > 32 ? 32 : 0;
+    // those are known (the uncond box after the scale when samples of scale 1 skip
+    // it), then the scale and sigmas (which depend on the index) are read.  With a
+    // single warp, thread 0 plays both parts (its boxes first) and arrives once on
+    // each barrier.
+    const int ptid = ptid_of(nthreads);
     if (tid == ptid) {
         const int idx = p.step_idx != nullptr ? __ldg(p.step_idx + b) : p.step;
         const bool present = INP && (p.present == nullptr || __ldg(p.present + b) != 0);
         bool need_pred = true;
-        if (defer && present) {
+        bool narrow = false;
+        int xs = 0, xv = p.W, nch = 1;
+        if (defer && present && p.mask_spans != nullptr) {
+            // the union of the band's rows' nonzero column spans [lo, hi)
+            const unsigned* spans =
+                p.mask_spans + (p.mask_shared ? 0ll : static_cast<long long>(b) * p.H);
+            const int y_end = y_band + p.RB < p.H ? y_band + p.RB : p.H;
+            int lo = p.W, hi = 0;
+            for (int yy = y_band; yy < y_end; ++yy) {
+                const unsigned w = __ldg(spans + yy);
+                const int h = static_cast<int>(w >> 16);
+                if (h > 0) {
+                    lo = min(lo, static_cast<int>(w & 0xffffu));
+                    hi = max(hi, h);
+                }
+            }
+            need_pred = hi > 0;
+            if (need_pred) {
+                xs = lo - lo % VEC;                          // 16-byte aligned box start
+                xv = (hi + VEC - 1) / VEC * VEC;             // end of the vectors read
+                nch = (xv - xs + kChunk - 1) / kChunk;
+                narrow = nch * kChunk < p.W;                 // else one full-width box
+                // (with a full-width box the vectors outside [xs, xv) are still
+                // taken as 0: what is read does not depend on the box layout)
+            }
+        } else if (defer && present && p.mask_rows != nullptr) {
             // rows y_band .. y_end-1 of this sample's mask: any nonzero?
             const unsigned* words = p.mask_rows + (p.mask_shared ? 0 : b) * p.mask_words;
             const int y_end = y_band + p.RB < p.H ? y_band + p.RB : p.H;
@@ -472,12 +570,15 @@ __global__ void __launch_bounds__(kMaxThreads)
             }
             need_pred = any != 0u;
         }
+        bool use_u = has_u && need_pred;
         if constexpr (defer) {
-            if (need_pred) issue_prediction();
-            if constexpr (kSplit) {
-                // group A is complete: with deferral this thread is its only feeder
-                if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
-                mbar_arrive(bar);
+            if (need_pred) {
+                if (use_u && !p.unit_skip)
+                    issue_plane(p.off_u, &p.tm_u, &p.tm_uc, narrow, xs, nch);
+                if (summary) {
+                    if (has_c) issue_plane(p.off_c, &p.tm_c, &p.tm_cc, narrow, xs, nch);
+                    issue_regions();
+                }
             }
         }
         if (INP && present) {
@@ -485,6 +586,25 @@ __global__ void __launch_bounds__(kMaxThreads)
             tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, barB);
             tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, barB);
             if (want_mi) tma_load_3d(s0 + p.off_on, &p.tm_on, 0, y_band, z, barB);
+        }
+        if constexpr (defer) {
+            if (use_u && p.unit_skip) {
+                // "cfg = 1": a sample of scale exactly 1 needs no uncond (pred = pos)
+                const bool ok_idx =
+                    idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
+                const float s1 = p.lut != nullptr ? __ldg(p.lut + (ok_idx ? idx : 0)) : p.cfg;
+                use_u = !(s1 == 1.0f);
+                if (use_u) issue_plane(p.off_u, &p.tm_u, &p.tm_uc, narrow, xs, nch);
+            }
+            tp.use_u = use_u ? 1 : 0;
+            tp.narrow = narrow ? 1 : 0;
+            tp.xs = xs;
+            tp.xv = xv;
+            if constexpr (kSplit) {
+                // group A is complete: with deferral this thread is its only feeder
+                if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
+                mbar_arrive(bar);
+            }
         }
         tp.inpaint = present ? 1 : 0;
         if constexpr (defer) tp.need_pred = need_pred ? 1 : 0;
@@ -584,11 +704,20 @@ __global__ void __launch_bounds__(kMaxThreads)
         if constexpr (REG) __syncthreads();       // region tables and step parameters
         // ---- every thread waits for the boxes ----
         if (!mbar_wait(bar, 0)) {
-            flag(p.status, GS_DEV_TIMEOUT);
-            // let group B land before the CTA can exit (bounded)
-            if constexpr (kSplit) (void)mbar_wait_for(barB, 0, kDrainLimitNs);
+            // thread 0 keeps the CTA (and its shared memory) alive until the boxes
+            // of both groups have landed (bounded); the other threads leave.  The
+            // drain may complete the phase while threads are still waiting: the
+            // abandon flag, written first, tells them not to write the tile.
+            if (tid == 0) {
+                flag(p.status, GS_DEV_TIMEOUT);
+                tp.abandon = 1;
+                __threadfence_block();
+                mbar_drain(bar, p.test_wait_timeout != 0);
+                if constexpr (kSplit) mbar_drain(barB, false);
+            }
             return;
         }
+        if (tp.abandon != 0) return;       // (thread 0 is never here with it set)
         if (tp.ok != 1) {
             // A skipped sample: group B (x, original, mask, noise) may still be landing
             // in this CTA's shared memory, which must not be handed to another CTA
@@ -607,6 +736,7 @@ __global__ void __launch_bounds__(kMaxThreads)
             if (!mbar_wait(bar, 0)) {
                 flag(p.status, GS_DEV_TIMEOUT);
                 tp.arrived = 0;
+                mbar_drain(bar, p.test_wait_timeout != 0);
             }
         }
         __syncthreads();
@@ -617,12 +747,15 @@ __global__ void __launch_bounds__(kMaxThreads)
     const bool active = y < p.H;
     if (!active) return;
     const bool inpaint = INP && tp.inpaint != 0;
-    if (SKIP && tp.need_pred == 0) {
+    if (DEFER && INP && tp.need_pred == 0) {
         // A blended band whose mask is 0 on every row: den = original (up to the sign
         // of zero), so the prediction was not loaded.  Only x and the original remain.
         if constexpr (kSplit) {
             if (!mbar_wait(barB, 0)) {
-                flag(p.status, GS_DEV_TIMEOUT);
+                if (tid == 0) {
+                    flag(p.status, GS_DEV_TIMEOUT);
+                    mbar_drain(barB, false);
+                }
                 return;
             }
         }
@@ -659,6 +792,32 @@ __global__ void __launch_bounds__(kMaxThreads)
 
     const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
     const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
+    // The prediction planes (uncond, cond): where this thread's vector sits in the
+    // tile's box or column chunks, and whether it was read at all.  Narrowed tiles
+    // read only the vectors over the band's nonzero mask columns; elsewhere m = 0 on
+    // every row of the band, den = original whatever the prediction, and the
+    // prediction is taken as 0.
+    bool pred_in = true;
+    unsigned pred_base = pix, pred_kstride = kstride;
+    if constexpr (DEFER) {
+        const int dx = x0 - tp.xs;                        // a multiple of VEC
+        pred_in = dx >= 0 && x0 < tp.xv;
+        if (tp.narrow) {
+            const int dc = pred_in ? dx : 0;
+            pred_base = static_cast<unsigned>(dc / kChunk) * p.chunk_bytes +
+                        static_cast<unsigned>(row * kChunk + dc % kChunk) * ES;
+            pred_kstride = static_cast<unsigned>(p.RB) * kChunk * ES;
+        }
+    }
+    auto ld_pred = [&](unsigned plane_off, int k) {
+        Raw<T, VEC> v;
+        if (pred_in) return ld_smem<T, VEC>(st + plane_off, pred_base + k * pred_kstride);
+#pragma unroll
+        for (int i = 0; i < Raw<T, VEC>::kWords; ++i) v.w[i] = 0u;
+        return v;
+    };
+    // deferred instances: a sample of scale 1 may have skipped its uncond box
+    const bool use_u = DEFER ? tp.use_u != 0 : has_u;
 
     // positive branch
     f2 pos[CG][NP];
@@ -689,7 +848,7 @@ __global__ void __launch_bounds__(kMaxThreads)
 #pragma unroll
             for (int k = 0; k < CG; ++k) {
                 if (has_c) {
-                    const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_c, k * kstride + pix);
+                    const Raw<T, VEC> v = ld_pred(p.off_c, k);
 #pragma unroll
                     for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(v, q);
                 } else {
@@ -768,7 +927,7 @@ __global__ void __launch_bounds__(kMaxThreads)
     } else {
 #pragma unroll
         for (int k = 0; k < CG; ++k) {
-            const Raw<T, VEC> v = ld_smem<T, VEC>(st + p.off_c, k * kstride + pix);
+            const Raw<T, VEC> v = ld_pred(p.off_c, k);
 #pragma unroll
             for (int q = 0; q < NP; ++q) pos[k][q] = widen2<T, VEC>(v, q);
         }
@@ -776,17 +935,20 @@ __global__ void __launch_bounds__(kMaxThreads)
 
     if constexpr (kSplit) {
         // combine while group B lands, then wait for it (NEG: combined above)
-        if (!NEG && has_u) {
+        if (!NEG && use_u) {
 #pragma unroll
             for (int k = 0; k < CG; ++k) {
-                const Raw<T, VEC> uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+                const Raw<T, VEC> uv = ld_pred(p.off_u, k);
 #pragma unroll
                 for (int q = 0; q < NP; ++q)
                     pos[k][q] = fma2(s2, pos[k][q], mul2(oms2, widen2<T, VEC>(uv, q)));
             }
         }
         if (!mbar_wait(barB, 0)) {
-            flag(p.status, GS_DEV_TIMEOUT);
+            if (tid == 0) {
+                flag(p.status, GS_DEV_TIMEOUT);
+                mbar_drain(barB, false);
+            }
             return;
         }
     }
@@ -813,14 +975,14 @@ __global__ void __launch_bounds__(kMaxThreads)
     for (int k = 0; k < CG; ++k) {
         const Raw<T, VEC> xv = ld_smem<T, VEC>(st + p.off_x, k * kstride + pix);
         Raw<T, VEC> uv, ov, nv, onv, xo, dn, mi;
-        if (!NEG && !kSplit && has_u) uv = ld_smem<T, VEC>(st + p.off_u, k * kstride + pix);
+        if (!NEG && !kSplit && use_u) uv = ld_pred(p.off_u, k);
         if (INP && inpaint) ov = ld_smem<T, VEC>(st + p.off_o, k * kstride + pix);
         if (NZ && anc) nv = ld_smem<T, VEC>(st + p.off_n, k * kstride + pix);
         if (NZ && INP && want_mi && inpaint) onv = ld_smem<T, VEC>(st + p.off_on, k * kstride + pix);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             f2 pred = pos[k][q];
-            if (!NEG && !kSplit && has_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(uv, q)));
+            if (!NEG && !kSplit && use_u) pred = fma2(s2, pred, mul2(oms2, widen2<T, VEC>(uv, q)));
             f2 den = pred;
             if (INP && inpaint) den = fma2(m2[q], pred, mul2(omm2[q], widen2<T, VEC>(ov, q)));
             f2 xn = fma2(r2, sub2(widen2<T, VEC>(xv, q), den), den);
@@ -842,9 +1004,9 @@ __global__ void __launch_bounds__(kMaxThreads)
     }
 }
 
-template <typename T, int CG, bool REG, bool INP, bool SKIP, bool NZ, bool NEG = false>
+template <typename T, int CG, bool REG, bool INP, bool DEFER, bool NZ, bool NEG = false>
 gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stream, unsigned flags) {
-    auto kern = guided_step_tma_kernel<T, CG, REG, INP, SKIP, NZ, NEG>;
+    auto kern = guided_step_tma_kernel<T, CG, REG, INP, DEFER, NZ, NEG>;
     static std::mutex mu;
     static unsigned smem_set[64] = {0};
     int dev = 0;
@@ -882,12 +1044,12 @@ gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stre
     return GS_OK;
 }
 
-template <typename T, bool REG, bool INP, bool SKIP, bool NZ, bool NEG = false>
+template <typename T, bool REG, bool INP, bool DEFER, bool NZ, bool NEG = false>
 gs_status launch_cg(TmaParams& p, int cg, int threads, unsigned smem, gs_stream stream,
                     unsigned flags) {
-    if (cg == 4) return launch_kernel<T, 4, REG, INP, SKIP, NZ, NEG>(p, threads, smem, stream, flags);
-    if (cg == 2) return launch_kernel<T, 2, REG, INP, SKIP, NZ, NEG>(p, threads, smem, stream, flags);
-    return launch_kernel<T, 1, REG, INP, SKIP, NZ, NEG>(p, threads, smem, stream, flags);
+    if (cg == 4) return launch_kernel<T, 4, REG, INP, DEFER, NZ, NEG>(p, threads, smem, stream, flags);
+    if (cg == 2) return launch_kernel<T, 2, REG, INP, DEFER, NZ, NEG>(p, threads, smem, stream, flags);
+    return launch_kernel<T, 1, REG, INP, DEFER, NZ, NEG>(p, threads, smem, stream, flags);
 }
 
 // Negative regions (the regional uncond branch): region instances without read
@@ -900,17 +1062,24 @@ gs_status launch_features_neg(TmaParams& p, int cg, int threads, unsigned smem, 
     return launch_cg<T, true, false, false, NZ, true>(p, cg, threads, smem, stream, flags);
 }
 
-// NZ = false: the deterministic Euler step; NZ = true: the sampler options.  Read
-// skipping (a row summary of the inpaint mask) has instances of its own in both.
+// NZ = false: the deterministic Euler step; NZ = true: the sampler options.  The
+// deferred-prediction instances (a row or span summary of the inpaint mask, or the
+// uncond skip at scale 1) are instances of their own in both, so that the common
+// path pays nothing for them.
 template <typename T, bool NZ>
 gs_status launch_features(TmaParams& p, int cg, int threads, unsigned smem, bool reg, bool inp,
                           gs_stream stream, unsigned flags) {
-    const bool skip = inp && p.mask_rows != nullptr;
-    if (reg && skip) return launch_cg<T, true, true, true, NZ>(p, cg, threads, smem, stream, flags);
-    if (reg && inp) return launch_cg<T, true, true, false, NZ>(p, cg, threads, smem, stream, flags);
-    if (reg) return launch_cg<T, true, false, false, NZ>(p, cg, threads, smem, stream, flags);
-    if (skip) return launch_cg<T, false, true, true, NZ>(p, cg, threads, smem, stream, flags);
+    const bool defer =
+        (inp && (p.mask_rows != nullptr || p.mask_spans != nullptr)) || p.unit_skip != 0;
+    if (reg) {
+        if (inp && defer) return launch_cg<T, true, true, true, NZ>(p, cg, threads, smem, stream, flags);
+        if (inp) return launch_cg<T, true, true, false, NZ>(p, cg, threads, smem, stream, flags);
+        if (defer) return launch_cg<T, true, false, true, NZ>(p, cg, threads, smem, stream, flags);
+        return launch_cg<T, true, false, false, NZ>(p, cg, threads, smem, stream, flags);
+    }
+    if (inp && defer) return launch_cg<T, false, true, true, NZ>(p, cg, threads, smem, stream, flags);
     if (inp) return launch_cg<T, false, true, false, NZ>(p, cg, threads, smem, stream, flags);
+    if (defer) return launch_cg<T, false, false, true, NZ>(p, cg, threads, smem, stream, flags);
     return launch_cg<T, false, false, false, NZ>(p, cg, threads, smem, stream, flags);
 }
 

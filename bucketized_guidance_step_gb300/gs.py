@@ -36,9 +36,10 @@ GS_MAX_REGIONS = 16
 GS_LAUNCH_PDL = 1
 GS_LAUNCH_NO_TMA = 2
 GS_LAUNCH_TEST_WAIT_TIMEOUT = 4
-GS_ABI_VERSION = 5
+GS_ABI_VERSION = 6
 
-EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_guided_step",
+EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_mask_spans",
+           "gs_guided_step",
            "gs_areas_to_latent", "gs_pack_conds",
            "gs_step_kernel_kind", "gs_status_from_word", "gs_status_string", "gs_abi_version")
 GS_KERNEL_SCALAR, GS_KERNEL_VECTOR, GS_KERNEL_TMA = 0, 1, 2
@@ -118,7 +119,8 @@ class StepArgs(ctypes.Structure):
                 ("dev_status", ctypes.c_void_p), ("launch_flags", ctypes.c_uint32),
                 ("mask_rows", ctypes.c_void_p),
                 ("sampler", ctypes.c_int32), ("noise", ctypes.c_void_p),
-                ("model_in_out", ctypes.c_void_p), ("orig_noise", ctypes.c_void_p)]
+                ("model_in_out", ctypes.c_void_p), ("orig_noise", ctypes.c_void_p),
+                ("mask_spans", ctypes.c_void_p), ("unit_scale_skip", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -145,6 +147,7 @@ def load() -> ctypes.CDLL:
         lib.gs_bucket_plan.argtypes = [i32, i32, ctypes.POINTER(CurveDesc), p, p, p]
         lib.gs_mask_prepare.argtypes = [p, i32, i32, i32, p, i32, i32, p]
         lib.gs_mask_rows.argtypes = [p, i32, i32, i32, p, p]
+        lib.gs_mask_spans.argtypes = [p, i32, i32, i32, p, p]
         lib.gs_guided_step.argtypes = [ctypes.POINTER(StepArgs), p]
         lib.gs_step_kernel_kind.argtypes = [ctypes.POINTER(StepArgs), p]
         lib.gs_status_from_word.argtypes = [ctypes.c_uint32]
@@ -155,7 +158,8 @@ def load() -> ctypes.CDLL:
                                            ctypes.POINTER(Rect)]
         lib.gs_pack_conds.argtypes = [ctypes.POINTER(CondEntry), i32, ctypes.c_int64,
                                       ctypes.POINTER(CondChunk), i32, p, p]
-        for f in ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_guided_step",
+        for f in ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_mask_spans",
+                  "gs_guided_step",
                   "gs_step_kernel_kind", "gs_status_from_word", "gs_abi_version",
                   "gs_areas_to_latent", "gs_pack_conds"):
             getattr(lib, f).restype = i32
@@ -325,6 +329,24 @@ def mask_rows(lat_mask, out=None, stream=None):
     return out
 
 
+def mask_spans(lat_mask, out=None, stream=None):
+    """gs_mask_spans: [Bm,1,H,W] fp32 latent mask -> [Bm, H] int32 words, word y of mask
+    b = lo | hi << 16 with [lo, hi) its row's nonzero column span (0: no nonzero value;
+    the bits of a uint32, stored as int32)."""
+    torch = _torch()
+    Bm, one, H, W = lat_mask.shape
+    if one != 1:
+        raise ValueError("latent mask must have one channel")
+    if out is None:
+        out = torch.empty((Bm, H), dtype=torch.int32, device=lat_mask.device)
+    elif tuple(out.shape) != (Bm, H):
+        raise ValueError(f"out must be [{Bm}, {H}]")
+    _check("gs_mask_spans", load().gs_mask_spans(
+        _dptr(lat_mask, "lat_mask", torch.float32), Bm, H, W, _dptr(out, "out", torch.int32),
+        _stream_ptr(stream)))
+    return out
+
+
 @dataclass
 class Region:
     """One regional conditioning output for ``guided_step`` (see gs_region)."""
@@ -358,7 +380,8 @@ def _dtype_code(t) -> int:
 def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=None,
                    step: int = 0, scale_lut=None, cfg: float = 1.0,
                    regions: Sequence[Region] = (), inpaint_mask=None, mask_present=None,
-                   original=None, mask_rows=None, x_out=None, denoised_out=None, status=None,
+                   original=None, mask_rows=None, mask_spans=None, unit_scale_skip=False,
+                   x_out=None, denoised_out=None, status=None,
                    sampler: str = "euler", noise=None, model_in_out=None, orig_noise=None,
                    pdl: bool = False, tma: bool = True, test_wait_timeout: bool = False):
     """Build a gs_step_args (and the region array it points to) from tensors."""
@@ -434,6 +457,13 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
         if tuple(mask_rows.shape) != (inpaint_mask.shape[0], (H + 31) // 32):
             raise ValueError("mask_rows must be [masks, ceil(H/32)] (from mask_rows())")
     a.mask_rows = _dptr(mask_rows, "mask_rows", torch.int32)
+    if mask_spans is not None:
+        if inpaint_mask is None:
+            raise ValueError("mask_spans needs inpaint_mask")
+        if tuple(mask_spans.shape) != (inpaint_mask.shape[0], H):
+            raise ValueError("mask_spans must be [masks, H] (from mask_spans())")
+    a.mask_spans = _dptr(mask_spans, "mask_spans", torch.int32)
+    a.unit_scale_skip = 1 if unit_scale_skip else 0
     if sampler not in SAMPLERS:
         raise ValueError(f"sampler must be one of {tuple(SAMPLERS)}")
     if sampler == "euler_ancestral" and noise is None:
@@ -469,7 +499,9 @@ def guided_step(x, *, sigmas, stream=None, **kw):
     ([B or 1, 1, H, W] fp32), mask_present (uint8 [B]), original, x_out,
     denoised_out, status (int32 [1], device flags OR-ed in), mask_rows (the row
     summary of inpaint_mask from ``mask_rows()``: bands whose mask is 0 on every row
-    then skip reading the prediction), sampler ("euler" or "euler_ancestral"), noise
+    then skip reading the prediction), mask_spans (the span summary from
+    ``mask_spans()``: also narrows the prediction reads to the nonzero columns),
+    unit_scale_skip (samples of scale exactly 1 read no uncond), sampler ("euler" or "euler_ancestral"), noise
     (the ancestral step's fresh noise), model_in_out and orig_noise (the next model
     input under the inpaint wrapper), pdl, tma (False forces the register-streaming
     kernel).

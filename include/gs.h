@@ -200,6 +200,27 @@ gs_status gs_mask_prepare(const float* pix_mask, int32_t B, int32_t Hp, int32_t 
 gs_status gs_mask_rows(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
                        uint32_t* rows_out, gs_stream stream);
 
+/*
+ * gs_mask_spans -- the nonzero column span of every row of a latent mask.
+ *
+ * Where a sample's mask is 0, the inpaint blend keeps the original (den = 0 * pred
+ * + 1 * original, [SAMPLING] "inpaint 与 mask"), so the guided prediction there is
+ * not needed.  This summary, computed once per run, lets gs_guided_step skip the
+ * prediction reads of whole bands of rows (like gs_mask_rows) and, in the bands it
+ * reads, narrow them to the columns between the band's first and last nonzero
+ * mask value (gs_step_args.mask_spans).
+ *
+ * lat_mask:  device float[Bm][1][H][W] (row pitch W), W <= 65535.
+ * spans_out: device uint32[Bm][H]: word y of mask b is lo | (hi << 16), lo the first
+ *            and hi - 1 the last column x with lat_mask[b][0][y][x] != 0 (NaN counts
+ *            as nonzero, -0 as zero); 0 for a row with no nonzero value.
+ *            Caller-owned.
+ * Errors: GS_ERR_INVALID_ARG (NULL pointers, sizes < 1), GS_ERR_UNSUPPORTED
+ *         (Bm or W above 65535), GS_ERR_CUDA.
+ */
+gs_status gs_mask_spans(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
+                        uint32_t* spans_out, gs_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* The guided step (device, one kernel launch per call).                     */
 /* ------------------------------------------------------------------------ */
@@ -332,6 +353,26 @@ typedef struct gs_step_args {
        not overlap x_out or denoised_out (the same start address is GS_ERR_INVALID_ARG). */
     void*       model_in_out;   /* device [B][C][H][W] or NULL                           */
     const void* orig_noise;     /* device [B][C][H][W]: the run's fixed noise            */
+
+    /* Optional span summary of inpaint_mask from gs_mask_spans: device uint32[.][H],
+       sample b's rows at b * H words (0 when mask_bstride is 0); NULL = not given.  It
+       takes the place of mask_rows (which is then ignored): the TMA-fed kernels skip
+       the prediction reads of a blended band whose mask is 0 on every row, as with
+       mask_rows, and in the other bands of a blended sample read uncond and cond
+       only from the band's first to its last nonzero mask column (rounded out to
+       16-byte vectors; loaded as 64-byte column chunks): outside that span the
+       prediction is taken as 0 (den is the original exactly there, up to the sign of
+       zero), so a non-finite prediction there does not propagate.  Region outputs
+       are read whole in the bands they touch.
+       The caller keeps it in step with inpaint_mask.  Negative regions: ignored. */
+    const uint32_t* mask_spans;
+    /* 0 or 1.  With 1, a sample whose scale is exactly 1 does not read its uncond
+       output in the TMA-fed kernels: pred = pos exactly, the per-sample form of
+       [SAMPLING] "cfg = 1 的优化" (the uncond branch is still given for the other
+       samples).  The uncond box of every sample then waits for the sample's scale
+       (two dependent loads), so set it only when the scale table holds a 1 (or cfg
+       is 1).  Negative regions: ignored.  Other values: GS_ERR_INVALID_ARG. */
+    int32_t     unit_scale_skip;
 } gs_step_args;
 
 /*
@@ -385,8 +426,9 @@ typedef struct gs_step_args {
  * step_idx NULL, neither cond nor a positive region, a negative flag other than
  * 0 / 1, inpaint without original, unknown dtype or sampler, the ancestral
  * sampler without noise, the model input without inpaint_mask or orig_noise or
- * on x_out / denoised_out), GS_ERR_CUDA (launch failure).  Device-found errors:
- * see dev_status.
+ * on x_out / denoised_out, mask_rows or mask_spans without inpaint_mask or not
+ * 4-byte aligned, mask_spans with W above 65535, unit_scale_skip not 0 or 1),
+ * GS_ERR_CUDA (launch failure).  Device-found errors: see dev_status.
  */
 gs_status gs_guided_step(const gs_step_args* args, gs_stream stream);
 
@@ -471,7 +513,7 @@ gs_status gs_status_from_word(uint32_t word);
 const char* gs_status_string(gs_status status);
 
 /* ABI version of this header (bumped on any layout change). */
-#define GS_ABI_VERSION 5
+#define GS_ABI_VERSION 6
 int32_t gs_abi_version(void);
 
 #ifdef __cplusplus

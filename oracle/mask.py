@@ -68,3 +68,28 @@ def row_bits(lat_mask) -> np.ndarray:
             if np.any(m[b, 0, y, :] != 0):
                 out[b, y // 32] |= np.uint32(1) << np.uint32(y % 32)
     return out
+
+
+def row_spans(lat_mask) -> np.ndarray:
+    """The nonzero column span of every latent row of each mask.
+
+    [Bm, 1, H, W] (any float) -> uint32 [Bm, H]: word y of mask b is lo | hi << 16,
+    where lo is the first and hi - 1 the last column x with m[b, 0, y, x] != 0 (a NaN
+    counts as nonzero); 0 for a row with no nonzero value.
+
+    Same reasoning as ``row_bits`` at column resolution: where the mask is 0 the
+    inpaint blend of [SAMPLING] "inpaint 与 mask" keeps the original, so only the
+    columns between a row's first and last nonzero mask value can need the guided
+    prediction.  Written as the definition: Python loops over rows and columns.
+    """
+    m = np.asarray(lat_mask)
+    Bm, one, H, W = m.shape
+    if one != 1:
+        raise ValueError("mask must have one channel")
+    out = np.zeros((Bm, H), dtype=np.uint32)
+    for b in range(Bm):
+        for y in range(H):
+            nz = [x for x in range(W) if m[b, 0, y, x] != 0]
+            if nz:
+                out[b, y] = np.uint32(nz[0]) | (np.uint32(nz[-1] + 1) << np.uint32(16))
+    return out

@@ -27,3 +27,36 @@ def test_skipped_prediction_bytes_hand_count():
     # without a full-frame cond only the uncond row counts
     assert skipped_prediction_bytes([[True]], 3, 8, "fp32", cond=False) == 3 * 8 * 4
     assert skipped_prediction_bytes([], 3, 8, "fp32") == 0
+
+
+def test_required_bytes_hand_counts():
+    import numpy as np
+
+    from bucketized_guidance_step_gb300.accounting import required_bytes
+    # without a mask or a scale-1 sample it is the algorithmic count
+    assert required_bytes(3, 2, 4, 6, "fp32", cond=False, regions=[(0, 0, 3, 5, 8)]) == \
+        step_bytes(3, 2, 4, 6, "fp32", cond=False, regions=[(3, 5)])
+    # two of three samples skip their uncond: two planes fewer
+    assert required_bytes(3, 2, 4, 6, "fp32", unit_scale=[True, False, True]) == \
+        step_bytes(3, 2, 4, 6, "fp32") - 2 * 2 * 24 * 4
+    # bf16, rows of 32 elements = 64 bytes = two sectors; one nonzero mask pixel at
+    # (y 1, x 20): per channel only row 1's second sector (16 elements) is required
+    m = np.zeros((1, 2, 32), bool)
+    m[0, 1, 20] = True
+    full = step_bytes(1, 2, 2, 32, "bf16", inpaint_samples=1)
+    plane = 2 * 2 * 32 * 2
+    assert required_bytes(1, 2, 2, 32, "bf16", mask_nz=m) == full - 2 * (plane - 2 * 32)
+    # the same sample not blended: everything is required
+    assert required_bytes(1, 2, 2, 32, "bf16", mask_nz=m, present=[False]) == \
+        step_bytes(1, 2, 2, 32, "bf16")
+    # a region slab of pitch 8 (16-byte rows, two rows a sector): its element (0, 0) is
+    # needed, so slab rows 0 and 1 of channel 0 (one sector) are required; channel 1
+    # starts at byte 2 * 16 = 32, its rows 0 and 1 share a sector likewise
+    m = np.zeros((1, 4, 32), bool)
+    m[0, 2, 4] = True                              # frame (2, 4) = region (0, 0) at y0 2, x0 4
+    reg = [(2, 4, 2, 8, 8)]
+    got = required_bytes(1, 2, 4, 32, "bf16", cond=False, regions=reg, mask_nz=m)
+    full = step_bytes(1, 2, 4, 32, "bf16", cond=False, regions=[(2, 8)], inpaint_samples=1)
+    uncond_needed = 2 * 16 * 2                     # row 2's first sector, both channels
+    region_needed = 2 * 2 * 8 * 2                  # both rows of both channels
+    assert got == full - (2 * 4 * 32 * 2 - uncond_needed) - (2 * 2 * 8 * 2 - region_needed)

@@ -18,9 +18,29 @@ def _wl(*argv):
         sys.argv = old
 
 
-def test_default_is_the_bcg_workload():
+def test_default_is_the_largest_workload():
+    """The headline line times the throughput sweep (B=64, 16x128x128 bf16), the largest
+    configuration that fits one GPU; the other target workloads follow in per_config."""
     wl = _wl()
-    assert wl.name == "bcg_bf16_b16" and wl.sampler == "euler" and not wl.model_input
+    assert wl.name == "sweep_bf16_b64" and wl.sampler == "euler" and not wl.model_input
+    assert wl.elements == max(w.elements for w in WORKLOADS)
+    assert set(bench.TARGET_WORKLOADS) == {w.name for w in WORKLOADS[1:]}
+
+
+def test_cpu_procs_default_to_host_cores():
+    old = sys.argv
+    sys.argv = ["bench.py"]
+    try:
+        args = bench.parse_args()
+    finally:
+        sys.argv = old
+    assert args.cpu_procs == bench.host_cores() >= 1
+
+
+def test_traffic_entries_split_read_and_write():
+    for key, entry in bench.TRAFFIC.items():
+        read, write, rev = entry
+        assert read > 0 and write >= 0 and len(rev) == 16, key
 
 
 def test_variant_names_and_fields():

@@ -48,3 +48,23 @@ def test_mask_rows_match_oracle(Bm, H, W):
     torch.cuda.synchronize()
     want = OM.row_bits(lat)
     assert np.array_equal(got.cpu().numpy().view(np.uint32), want)
+
+
+@pytest.mark.parametrize("Bm,H,W", [(32, 128, 128), (3, 70, 9), (1, 1, 1), (2, 33, 300),
+                                    (4, 64, 40)])
+def test_mask_spans_match_oracle(Bm, H, W):
+    """gs_mask_spans against the oracle's span summary, bit for bit, on resized
+    rectangle masks and on sparse random masks with NaN and -0."""
+    if H == 128:
+        lat = OM.bilinear_resize(pixel_mask(Bm, 1024, 1024, (1, 3), seed=8).numpy(), H, W)
+        lat = np.ascontiguousarray(lat, dtype=np.float32)
+    else:
+        rng = np.random.default_rng(H * W + Bm + 1)
+        lat = np.where(rng.random((Bm, 1, H, W)) < 0.02, rng.random((Bm, 1, H, W)), 0.0)
+        lat = np.ascontiguousarray(lat, dtype=np.float32)
+        lat[0, 0, H // 2, W // 2] = np.nan
+        lat[-1, 0, H - 1, :] = -0.0
+    got = gs.mask_spans(torch.from_numpy(lat).cuda())
+    torch.cuda.synchronize()
+    want = OM.row_spans(lat)
+    assert np.array_equal(got.cpu().numpy().view(np.uint32), want)

@@ -46,6 +46,8 @@ MUTATIONS = [
     ("buckets.py", "((1.0 - p) / (1.0 - apex))", "(p / (1.0 - apex))"),
     ("buckets.py", "f = p * num_buckets - b", "f = p * num_buckets - b - 0.5"),
     ("mask.py", "(j + 0.5) * scale - 0.5", "j * scale"),
+    ("mask.py", "(np.uint32(nz[-1] + 1) << np.uint32(16))", "(np.uint32(nz[-1]) << np.uint32(16))"),
+    ("mask.py", "np.uint32(nz[0]) | ", "np.uint32(nz[0] + 1) | "),
     ("conds.py", "top = max(math.floor(ly0), 0)", "top = max(math.ceil(ly0), 0)"),
     ("conds.py", "bottom = min(math.ceil(ly0 + lh), H)", "bottom = min(math.floor(ly0 + lh), H)"),
     ("conds.py", "lx0, lw = vals[1] * float(W), vals[3] * float(W)",

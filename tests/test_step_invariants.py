@@ -233,17 +233,33 @@ def test_host_rejects_before_launch_on_gpu():
         gs.guided_step(x, sigmas=sig(1.0, 0.0), uncond=x, regions=regs)
 
 
-def test_bounded_wait_expires_with_status(kernel_choice):
-    """The TMA kernel's tile wait is bounded: made to run out, it reports and returns."""
+@pytest.mark.parametrize("case", ["dense", "regions_one_group", "regions_two_groups",
+                                  "deferred_one_group", "deferred_two_groups"])
+def test_bounded_wait_expires_with_status(kernel_choice, case):
+    """The TMA kernel's tile waits are bounded: made to run out (the test flag adds 16
+    expected bytes that never arrive), the CTA reports, lets the boxes already issued
+    land, and returns without writing.  Covered: tiles without regions, region tiles
+    with one barrier (small steps) and with two barrier groups (large steps), and the
+    tiles whose prediction boxes the parameter thread issues (row summary given)."""
     if not kernel_choice:
         pytest.skip("the register kernel has no waits")
-    shape = (1, 4, 8, 16)                       # one tile
-    x, u, c = (rnd(shape, s, torch.bfloat16) for s in (40, 41, 42))
+    large = case.endswith("two_groups")
+    shape = (64, 16, 16, 128) if large else (1, 4, 8, 16)
+    B, C, H, W = shape
+    x, u, c, o = (rnd(shape, s, torch.bfloat16) for s in (40, 41, 42, 43))
+    kw = dict(uncond=u, cond=c)
+    if case != "dense":
+        out_r = rnd((B, C, 4, 16), 44, torch.bfloat16)
+        kw["regions"] = [gs.Region(2, 0, 4, 16, 0.75, 1, out_r)]
+    if case.startswith("deferred"):
+        m = torch.zeros((B, 1, H, W), device=DEV)
+        m[:, :, H // 2:] = 1.0
+        kw.update(inpaint_mask=m, original=o, mask_rows=gs.mask_rows(m))
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     sentinel = torch.full_like(x, 9.0)
     out = sentinel.clone()
-    a, keep = gs.make_step_args(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=out,
-                                status=st, test_wait_timeout=True)
+    a, keep = gs.make_step_args(x, sigmas=sig(3.0, 1.0), cfg=2.0, x_out=out, status=st,
+                                test_wait_timeout=True, **kw)
     assert gs.kernel_kind(a) == "tma"
     gs.launch_step(a)
     torch.cuda.synchronize()
@@ -252,7 +268,7 @@ def test_bounded_wait_expires_with_status(kernel_choice):
     assert torch.equal(out, sentinel)           # no output from a tile that never arrived
     # the context stays usable: the same call without the hook steps normally
     st.zero_()
-    gs.guided_step(x, sigmas=sig(3.0, 1.0), uncond=u, cond=c, cfg=2.0, x_out=out, status=st)
+    gs.guided_step(x, sigmas=sig(3.0, 1.0), cfg=2.0, x_out=out, status=st, **kw)
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and not torch.equal(out, sentinel)
 

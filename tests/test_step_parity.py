@@ -35,7 +35,8 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
              uncond_none: bool = False, want_den: bool = False, pitch_align: int = 8,
              tma: bool = True, expect_kernel: str = None, mask_rows: bool = False,
              poison: bool = False, region_ranges=None, sampler: str = "euler",
-             model_in: bool = False, sigmas=None, negative=()):
+             model_in: bool = False, sigmas=None, negative=(), mask_spans: bool = False,
+             unit_skip: bool = False, lut=None):
     """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok).
 
     mask_rows: pass the row summary of the latent mask (gs_mask_rows), so that bands
@@ -48,7 +49,14 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     same on both sides).  model_in: also produce the next model input under the
     inpaint wrapper (needs an inpaint workload) and gate it against the oracle's.
     sigmas: a schedule (float32) in place of the workload's.  negative: indices of
-    regions that belong to the uncond branch (on both sides).
+    regions that belong to the uncond branch (on both sides).  mask_spans: pass the
+    span summary of the latent mask (gs_mask_spans) instead of the row summary; with
+    poison, also fill uncond and cond with NaN in every 16-byte vector of a blended
+    sample's row that lies outside the first-to-last nonzero mask columns of every
+    row that can share a band with it (a band has at most 256 threads' rows), so
+    that no vector the kernel reads is poisoned, whatever tile shape it picks.  unit_skip: samples whose scale is
+    exactly 1 skip their uncond read; with poison their whole uncond is NaN on the GPU
+    side.  lut: a per-step scale table (float32) in place of the workload's.
     """
     if sampler != wl.sampler or model_in != wl.model_input:
         wl = dataclasses.replace(wl, sampler=sampler, model_input=model_in)
@@ -57,7 +65,10 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     dt = DTYPES[wl.dtype]
     Bn, Cn, Hn, Wn = inp.noise.shape
     sig = oracle_sigmas(wl) if sigmas is None else np.asarray(sigmas, dtype=np.float32)
-    lut = oracle_lut(wl, len(sig) - 1)
+    if lut is None:
+        lut = oracle_lut(wl, len(sig) - 1)
+    else:
+        lut = np.asarray(lut, dtype=np.float32)
     if inp.step_idx is not None:
         idx = inp.step_idx.numpy().astype(np.int64)
     else:
@@ -85,15 +96,42 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     u_gpu, c_gpu = u, inp.cond
     reg_outs = [r.out for r in inp.regions]
     if poison:
-        assert lat is not None and mask_rows
+        assert (lat is not None and (mask_rows or mask_spans)) or unit_skip
         present_np = (np.ones(Bn, bool) if inp.mask_present is None
                       else inp.mask_present.numpy().astype(bool))
-        m_np = lat.numpy()
+        m_np = None if lat is None else lat.numpy()
         u_gpu = None if u is None else u.clone()
         c_gpu = None if inp.cond is None else inp.cond.clone()
         reg_outs = [o.clone() for o in reg_outs]
         nan = float("nan")
-        for bi in range(Bn):
+        if unit_skip and u_gpu is not None:
+            s_b = lut[idx] if lut is not None else np.full(Bn, np.float32(cfg))
+            for bi in range(Bn):
+                if s_b[bi] == 1.0:
+                    u_gpu[bi] = nan
+        vec = 4 if wl.dtype == "fp32" else 8
+        for bi in range(Bn if (mask_spans and m_np is not None) else 0):
+            if not present_np[bi]:
+                continue
+            nzc = m_np[bi if m_np.shape[0] > 1 else 0, 0] != 0           # [H, W]
+            cols = np.arange(Wn)
+            lo_r = np.where(nzc.any(1), np.where(nzc, cols, Wn).min(1), Wn)   # per row
+            hi_r = np.where(nzc.any(1), np.where(nzc, cols + 1, 0).max(1), 0)
+            # a tile's band has at most 256 threads / (W / vec) rows: rows farther apart
+            # never share a band, so the columns a band containing row y can read lie
+            # between the first and last nonzero column of the rows around y
+            radius = 256 // max(1, Wn // vec) - 1
+            far = np.zeros((Hn, Wn), bool)
+            for yy in range(Hn):
+                lo = lo_r[max(0, yy - radius):yy + radius + 1].min()
+                hi = hi_r[max(0, yy - radius):yy + radius + 1].max()
+                lo_v, hi_v = lo - lo % vec, -(-hi // vec) * vec
+                far[yy] = (cols < lo_v) | (cols >= hi_v)
+            far_t = torch.from_numpy(far)
+            for t in (u_gpu, c_gpu):
+                if t is not None:
+                    t[bi][:, far_t] = nan
+        for bi in range(Bn if (mask_rows or mask_spans) and m_np is not None else 0):
             if not present_np[bi]:
                 continue
             mb = m_np[bi if m_np.shape[0] > 1 else 0, 0]
@@ -139,6 +177,10 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
                   mask_present=_cuda(inp.mask_present))
         if mask_rows:
             kw["mask_rows"] = gs.mask_rows(kw["inpaint_mask"])
+        if mask_spans:
+            kw["mask_spans"] = gs.mask_spans(kw["inpaint_mask"])
+    if unit_skip:
+        kw["unit_scale_skip"] = True
     args, _keep = gs.make_step_args(xd, **kw)
     kind = gs.kernel_kind(args)
     if expect_kernel is not None:
@@ -499,3 +541,75 @@ def test_mask_rows_skip_reads_with_sampler_options(wl, poison):
     _, plain, _, _ = run_case(wl, sampler="euler_ancestral", model_in=True, expect_kernel="tma")
     assert np.array_equal(got.view(np.uint64), plain.view(np.uint64))
     assert np.array_equal(mi.view(np.uint64), run_case.last_model_in.view(np.uint64))
+
+
+@pytest.mark.parametrize("poison", [False, True], ids=["clean", "poisoned"])
+@pytest.mark.parametrize("wl", [WORKLOADS[3], WORKLOADS[4]], ids=["inpaint", "sweep"])
+def test_mask_spans_narrow_reads(wl, poison):
+    """Column-narrowed reads with the mask's span summary: the full-size inpaint and
+    sweep steps match the oracle; with the prediction poisoned (NaN) wherever no band
+    reads it (vectors outside the nonzero column span of the rows a band can hold, and
+    whole 32-row blocks of zero mask for the regions) they still do; and the output
+    equals the step without any summary bit for bit."""
+    rep, got, ref, ok = run_case(wl, mask_spans=True, poison=poison, expect_kernel="tma")
+    assert rep.n == wl.elements and np.isfinite(got).all()
+    _, plain, _, _ = run_case(wl, expect_kernel="tma")
+    assert np.array_equal(got.view(np.uint64), plain.view(np.uint64))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+@pytest.mark.parametrize("shape", [(24, 8, 70, 64), (64, 16, 37, 128), (3, 3, 13, 16)])
+def test_mask_spans_other_shapes(dtype, shape):
+    """Narrowed reads in one- and multi-channel tiles, with regions, region masks, a
+    denoised output, the sampler options, ragged last bands and a partial batch,
+    poisoned."""
+    B, C, H, W = shape
+    base = WORKLOADS[4]
+    wl = Workload("spans", B, C, H, W, dtype, base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=2, region_side=(4, min(H, W) - 1),
+                  inpaint=True, inpaint_samples=max(1, 2 * B // 3),
+                  pixel_mask_hw=(8 * H, 8 * W), seed=24)
+    for sampler, model_in in (("euler", False), ("euler_ancestral", True)):
+        rep, got, _, _ = run_case(wl, region_masks=True, want_den=True, mask_spans=True,
+                                  poison=True, sampler=sampler, model_in=model_in,
+                                  expect_kernel="tma")
+        assert rep.n == wl.elements and np.isfinite(got).all()
+
+
+def _unit_lut(steps):
+    """A per-step scale table whose flat tail is exactly 1 (no guidance after 20 %)."""
+    return np.where(np.arange(steps) / steps < 0.2, 3.0, 1.0).astype(np.float32)
+
+
+@pytest.mark.parametrize("poison", [False, True], ids=["clean", "poisoned"])
+@pytest.mark.parametrize("name", ["bcg_bf16_b16", "inpaint_bcg_bf16_b32", "sweep_bf16_b64"])
+def test_unit_scale_skips_uncond(name, poison):
+    """Samples whose scale is exactly 1 read no uncond: with their uncond poisoned (NaN)
+    the full-size step still matches the oracle, which uses the clean uncond (s = 1 gives
+    pred = pos exactly), and equals the step without the skip bit for bit."""
+    from bucketized_guidance_step_gb300.workloads import workload
+    wl = workload(name)
+    lut = _unit_lut(wl.schedule.steps)
+    rep, got, _, _ = run_case(wl, lut=lut, unit_skip=True, poison=poison, expect_kernel="tma")
+    assert rep.n == wl.elements and np.isfinite(got).all()
+    _, plain, _, _ = run_case(wl, lut=lut, expect_kernel="tma")
+    assert np.array_equal(got.view(np.uint64), plain.view(np.uint64))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+def test_unit_scale_with_spans_and_samplers(dtype):
+    """The uncond skip at scale 1 together with narrowed reads, regions, the ancestral
+    step and the model input, poisoned, on a ragged multi-channel shape; and a scalar
+    cfg of 1 with an uncond given (every sample skips it)."""
+    base = WORKLOADS[4]
+    wl = Workload("unit", 40, 8, 45, 64, dtype, base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=2, region_side=(6, 40), inpaint=True,
+                  inpaint_samples=25, pixel_mask_hw=(360, 512), seed=25)
+    rep, got, _, _ = run_case(wl, lut=_unit_lut(wl.schedule.steps), unit_skip=True,
+                              mask_spans=True, poison=True, region_masks=True, want_den=True,
+                              sampler="euler_ancestral", model_in=True, expect_kernel="tma")
+    assert np.isfinite(got).all()
+    wl1 = Workload("unit_cfg1", 6, 4, 16, 32, dtype, base.schedule,
+                   base.guidance.__class__(cfg=1.0), seed=26)
+    rep, got, _, _ = run_case(wl1, unit_skip=True, poison=True, expect_kernel="tma")
+    assert np.isfinite(got).all()
