@@ -537,7 +537,15 @@ class Timed:
             return algorithmic_bytes(wl, proto.regions)
         return sum(self.required_bytes(st, proto) for st in self.sets) // len(self.sets)
 
-    def required_bytes(self, st, proto):
+    def required_line_bytes(self):
+        """The same at 128-byte L2-line granularity (None without a summary or skip)."""
+        from bucketized_guidance_step_gb300.workloads import step_inputs
+        if not (self.use_rows or self.use_spans or self.unit_skip):
+            return None
+        proto = step_inputs(self.wl, 0, B=1)
+        return sum(self.required_bytes(st, proto, 128) for st in self.sets) // len(self.sets)
+
+    def required_bytes(self, st, proto, granule=32):
         import numpy as np
 
         from bucketized_guidance_step_gb300.accounting import required_bytes
@@ -557,7 +565,7 @@ class Timed:
                               regions=[(r.y0, r.x0, r.h, r.w, r.pitch) for r in proto.regions],
                               mask_nz=mask_nz, present=present, unit_scale=unit,
                               noise=wl.sampler == "euler_ancestral",
-                              model_input=wl.model_input)
+                              model_input=wl.model_input, granule=granule)
 
 
 def run_api(timed, stream, dev, n: int):
@@ -571,33 +579,40 @@ def run_api(timed, stream, dev, n: int):
     (the larger of the kernel time and the host cost); ctypes_call_us and
     checks_and_encode_us: a trivial call into the library and gs_step_kernel_kind
     (the same checks and encoding, no launch), the parts of the host cost before the
-    launch itself."""
+    launch itself; prepared: the same two numbers for gs_step_launch on plans made
+    once by gs_step_prepare (no checks or encoding per call)."""
     import torch
 
     from bucketized_guidance_step_gb300 import gs
     lib = gs.load()
     R = timed.R
     args = [a for a, _ in timed.prepared]
+    plans = [gs.prepare_step(a) for a in args]
     burst = 100
-    with torch.cuda.stream(stream):
-        for k in range(min(n, 50)):
-            gs.launch_step(args[k % R], stream)
-        torch.cuda.synchronize(dev)
-        best = float("inf")
-        for _ in range(10):
-            t0 = time.perf_counter()
-            for k in range(burst):
-                gs.launch_step(args[k % R], stream)
-            best = min(best, time.perf_counter() - t0)
+
+    def measure(call):
+        with torch.cuda.stream(stream):
+            for k in range(min(n, 50)):
+                call(k)
             torch.cuda.synchronize(dev)
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for k in range(n):
-            gs.launch_step(args[k % R], stream)
-        end.record(stream)
-        torch.cuda.synchronize(dev)
-    dev_ms = start.elapsed_time(end)
+            best = float("inf")
+            for _ in range(10):
+                t0 = time.perf_counter()
+                for k in range(burst):
+                    call(k)
+                best = min(best, time.perf_counter() - t0)
+                torch.cuda.synchronize(dev)
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for k in range(n):
+                call(k)
+            end.record(stream)
+            torch.cuda.synchronize(dev)
+        return best / burst * 1e6, start.elapsed_time(end) * 1e3 / n
+
+    host_us, dev_us = measure(lambda k: gs.launch_step(args[k % R], stream))
+    phost_us, pdev_us = measure(lambda k: gs.launch_prepared(plans[k % R], 0, stream))
     t2 = time.perf_counter()
     for _ in range(n):
         lib.gs_abi_version()
@@ -606,8 +621,10 @@ def run_api(timed, stream, dev, n: int):
         gs.kernel_kind(args[k % R])
     t4 = time.perf_counter()
     return {"steps": n,
-            "host_us_per_call": round(best / burst * 1e6, 3),
-            "device_us_per_step": round(dev_ms * 1e3 / n, 3),
+            "host_us_per_call": round(host_us, 3),
+            "device_us_per_step": round(dev_us, 3),
+            "prepared": {"host_us_per_call": round(phost_us, 3),
+                         "device_us_per_step": round(pdev_us, 3)},
             "ctypes_call_us": round((t3 - t2) / n * 1e6, 3),
             "checks_and_encode_us": round((t4 - t3) / n * 1e6, 3),
             "mode": "one gs_guided_step call per step from Python (ctypes), no CUDA graph, "
@@ -678,6 +695,10 @@ def run_ours(args, world, rank, local):
     sec_step = ms_max / 1e3 / K
     value = world * wl.elements / sec_step / 1e9
     rl = roofline(abytes, ms, K, peak, peak_src, timed.key)
+    line_bytes = timed.required_line_bytes()
+    if line_bytes is not None:
+        rl["required_line_bytes"] = line_bytes
+        rl["frac_line"] = round(line_bytes / (ms / 1e3 / K) / 1e9 / peak, 4)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
@@ -741,7 +762,7 @@ def run_ours(args, world, rank, local):
                          "input_sets": t2.R}
             if api2 is not None:
                 per[name]["api"] = {k: api2[k] for k in ("host_us_per_call",
-                                                         "device_us_per_step")}
+                                                         "device_us_per_step", "prepared")}
             launches += Kc
             del t2
             torch.cuda.empty_cache()

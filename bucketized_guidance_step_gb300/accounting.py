@@ -70,13 +70,14 @@ def skipped_prediction_bytes(zero_rows, C: int, W: int, dtype: str, *, cond: boo
 SECTOR = 32          # bytes: the unit in which DRAM and L2 move data
 
 
-def _needed_bytes(nz, addr, e: int) -> int:
-    """Bytes of the given elements that share a 32-byte sector with a needed element.
+def _needed_bytes(nz, addr, e: int, granule: int = SECTOR) -> int:
+    """Bytes of the given elements that share a granule (32-byte sector) with a needed
+    element.
 
     nz: bool [n] (element needed); addr: int [n], each element's byte address from a
-    32-byte-aligned base; e: element size (a divisor of 32, so no element straddles
-    two sectors)."""
-    sec = np.asarray(addr, dtype=np.int64) // SECTOR
+    granule-aligned base; e: element size (a divisor of the granule, so no element
+    straddles two granules)."""
+    sec = np.asarray(addr, dtype=np.int64) // granule
     lo = int(sec.min())
     hit = np.zeros(int(sec.max()) - lo + 1, dtype=bool)
     hit[sec[np.asarray(nz, dtype=bool)] - lo] = True
@@ -86,7 +87,8 @@ def _needed_bytes(nz, addr, e: int) -> int:
 def required_bytes(B: int, C: int, H: int, W: int, dtype: str, *, uncond: bool = True,
                    cond: bool = True, regions: Iterable[Tuple[int, int, int, int, int]] = (),
                    mask_nz=None, present=None, unit_scale=None, denoised_out: bool = False,
-                   noise: bool = False, model_input: bool = False) -> int:
+                   noise: bool = False, model_input: bool = False,
+                   granule: int = SECTOR) -> int:
     """The bytes a step must move given its data, counted per 32-byte sector.
 
     Start from ``step_bytes``.  A blended sample needs its prediction (uncond, cond and
@@ -95,11 +97,13 @@ def required_bytes(B: int, C: int, H: int, W: int, dtype: str, *, uncond: bool =
     32-byte sectors, so a prediction element is required when its sector holds an
     element at a nonzero mask pixel.  A sample whose scale is exactly 1 needs no uncond
     at all when the step is asked to skip it ("cfg = 1 的优化", per sample).
+    granule: the unit of transfer counted (32: a sector; 128: an L2 line, the unit in
+    which DRAM serves L2 on the GPU this is measured on).
 
     regions: (y0, x0, h, w, pitch) per regional output.  mask_nz: bool [B, H, W]
     (mask != 0) or None; present: bool [B], the samples that blend (None: all, with a
     mask); unit_scale: bool [B], the samples that skip their uncond, or None.  Every
-    tensor is taken to start on a 32-byte boundary; row y of plane (b, c) starts
+    tensor is taken to start on a granule boundary; row y of plane (b, c) starts
     ((b C + c) H + y) W |T| bytes in, row t of a regional slab ((b C + c) h + t) pitch
     |T| bytes in.
     """
@@ -127,10 +131,10 @@ def required_bytes(B: int, C: int, H: int, W: int, dtype: str, *, uncond: bool =
             c, y, x = np.meshgrid(np.arange(C), np.arange(H), np.arange(W), indexing="ij")
             addr = (((b * C + c) * H + y) * W + x) * e
             nz = np.broadcast_to(m[b][None], (C, H, W))
-            total -= planes * (plane - _needed_bytes(nz.ravel(), addr.ravel(), e))
+            total -= planes * (plane - _needed_bytes(nz.ravel(), addr.ravel(), e, granule))
         for (y0, x0, h, w, pitch) in regions:
             c, t, x = np.meshgrid(np.arange(C), np.arange(h), np.arange(w), indexing="ij")
             addr = (((b * C + c) * h + t) * pitch + x) * e
             nz = np.broadcast_to(m[b, y0:y0 + h, x0:x0 + w][None], (C, h, w))
-            total -= C * h * w * e - _needed_bytes(nz.ravel(), addr.ravel(), e)
+            total -= C * h * w * e - _needed_bytes(nz.ravel(), addr.ravel(), e, granule)
     return total

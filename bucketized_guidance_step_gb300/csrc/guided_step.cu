@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "gs.h"
 #include "guided_step.cuh"
@@ -33,9 +34,9 @@ bool aligned16(const void* q) { return (reinterpret_cast<unsigned long long>(q) 
 
 namespace {
 
-// Validate, build the launch parameters and launch (or, with kind != nullptr, only
-// report which kernel would run).
-gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kind) {
+// Validate the arguments and build the launch parameters; *vec says whether every
+// latent-shaped base allows 16-byte vectors.
+gs_status build_params(const gs_step_args* a, StepParams* out, bool* vec_out) {
     if (a == nullptr) return GS_ERR_INVALID_ARG;
     if (a->B < 1 || a->C < 1 || a->H < 1 || a->W < 1) return GS_ERR_INVALID_ARG;
     if (a->dtype != GS_DTYPE_F32 && a->dtype != GS_DTYPE_BF16 && a->dtype != GS_DTYPE_F16)
@@ -74,7 +75,8 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
         (a->model_in_out == a->x_out || a->model_in_out == a->denoised_out))
         return GS_ERR_INVALID_ARG;
 
-    StepParams p = {};
+    StepParams& p = *out;
+    p = StepParams{};
     p.B = a->B;
     p.C = a->C;
     p.H = a->H;
@@ -155,7 +157,27 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
         vec = vec && aligned16(a->original) && aligned16(a->inpaint_mask) && a->mask_bstride % 4 == 0;
     if (p.noise != nullptr) vec = vec && aligned16(p.noise);
     if (p.model_in != nullptr) vec = vec && aligned16(p.model_in) && aligned16(p.orig_noise);
+    *vec_out = vec;
+    return GS_OK;
+}
 
+// The register-streaming kernel for validated parameters.
+gs_status launch_registers(StepParams& p, int dtype, bool vec, gs_stream stream, unsigned flags) {
+    if (p.has_neg) return reg_launch_neg(p, dtype, vec, stream, flags);
+    switch (dtype) {
+        case GS_DTYPE_F32: return launch_dtype<F32, false>(p, vec, stream, flags);
+        case GS_DTYPE_BF16: return launch_dtype<BF16, false>(p, vec, stream, flags);
+        default: return launch_dtype<F16, false>(p, vec, stream, flags);
+    }
+}
+
+// Validate, build the launch parameters and launch (or, with kind != nullptr, only
+// report which kernel would run).
+gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kind) {
+    StepParams p;
+    bool vec = false;
+    const gs_status bst = build_params(a, &p, &vec);
+    if (bst != GS_OK) return bst;
     bool used_tma = false;
     const gs_status st =
         launch_step_tma(p, a->dtype, a->launch_flags, stream, &used_tma, kind != nullptr);
@@ -167,15 +189,67 @@ gs_status guided_step_impl(const gs_step_args* a, gs_stream stream, int32_t* kin
         return GS_OK;
     }
     if (used_tma) return GS_OK;
-    if (p.has_neg) return reg_launch_neg(p, a->dtype, vec, stream, a->launch_flags);
-    switch (a->dtype) {
-        case GS_DTYPE_F32: return launch_dtype<F32, false>(p, vec, stream, a->launch_flags);
-        case GS_DTYPE_BF16: return launch_dtype<BF16, false>(p, vec, stream, a->launch_flags);
-        default: return launch_dtype<F16, false>(p, vec, stream, a->launch_flags);
-    }
+    return launch_registers(p, a->dtype, vec, stream, a->launch_flags);
 }
 
+// A prepared launch inside the caller's gs_step_plan: a header, then (at byte 64)
+// either the TMA-fed kernel's launch or the register kernel's parameters.
+struct PlanHeader {
+    uint32_t magic;
+    uint32_t kind;                 // GS_KERNEL_TMA or GS_KERNEL_VECTOR / SCALAR
+    int32_t n_sig, has_idx, dtype;
+    uint32_t flags;
+    int32_t vec;
+};
+constexpr uint32_t kPlanMagic = 0x31506773u ^ static_cast<uint32_t>(GS_ABI_VERSION);
+constexpr size_t kPlanPayload = 64;
+static_assert(sizeof(PlanHeader) <= kPlanPayload, "plan header");
+static_assert(kPlanPayload + sizeof(StepParams) <= GS_STEP_PLAN_BYTES, "plan payload");
+
 }  // namespace
+
+extern "C" gs_status gs_step_prepare(const gs_step_args* args, gs_step_plan* plan) {
+    if (plan == nullptr || args == nullptr) return GS_ERR_INVALID_ARG;
+    gs_step_args checked = *args;
+    checked.step = 0;             // (gs_step_launch passes the step and checks it)
+    const gs_step_args* a = &checked;
+    StepParams p;
+    bool vec = false;
+    const gs_status st = build_params(a, &p, &vec);
+    if (st != GS_OK) return st;
+    if (kPlanPayload + tma_plan_bytes() > GS_STEP_PLAN_BYTES) return GS_ERR_UNSUPPORTED;
+    unsigned char* raw = reinterpret_cast<unsigned char*>(plan);
+    PlanHeader h = {};
+    h.magic = kPlanMagic;
+    h.n_sig = a->n_sigmas;
+    h.has_idx = a->step_idx != nullptr ? 1 : 0;
+    h.dtype = a->dtype;
+    h.flags = a->launch_flags;
+    h.vec = vec ? 1 : 0;
+    if (tma_plan_build(p, a->dtype, a->launch_flags, raw + kPlanPayload)) {
+        h.kind = GS_KERNEL_TMA;
+    } else {
+        const int vec16 = a->dtype == GS_DTYPE_F32 ? 4 : 8;
+        h.kind = vec && a->W % vec16 == 0 ? GS_KERNEL_VECTOR : GS_KERNEL_SCALAR;
+        std::memcpy(raw + kPlanPayload, &p, sizeof(p));
+    }
+    std::memcpy(raw, &h, sizeof(h));
+    return GS_OK;
+}
+
+extern "C" gs_status gs_step_launch(const gs_step_plan* plan, int32_t step, gs_stream stream) {
+    if (plan == nullptr) return GS_ERR_INVALID_ARG;
+    const unsigned char* raw = reinterpret_cast<const unsigned char*>(plan);
+    PlanHeader h;
+    std::memcpy(&h, raw, sizeof(h));
+    if (h.magic != kPlanMagic) return GS_ERR_INVALID_ARG;
+    if (!h.has_idx && (step < 0 || step > h.n_sig - 2)) return GS_ERR_INVALID_ARG;
+    if (h.kind == GS_KERNEL_TMA) return tma_plan_launch(raw + kPlanPayload, step, stream);
+    StepParams p;                 // (an aligned copy: the plan may sit anywhere)
+    std::memcpy(&p, raw + kPlanPayload, sizeof(p));
+    p.step = step;
+    return launch_registers(p, h.dtype, h.vec != 0, stream, h.flags);
+}
 
 extern "C" gs_status gs_guided_step(const gs_step_args* a, gs_stream stream) {
     return guided_step_impl(a, stream, nullptr);

@@ -367,4 +367,11 @@ __device__ __forceinline__ void store_raw(void* base, long long off, const Raw<T
 gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_stream stream,
                           bool* used, bool dry_run);
 
+// step_tma.cu: a prepared launch of the TMA-fed kernel (gs_step_prepare): its size,
+// building it into dst (false: the request does not fit the TMA-fed kernel) and
+// launching it with the shared step index `step`.
+size_t tma_plan_bytes();
+bool tma_plan_build(const StepParams& sp, int dtype, unsigned flags, void* dst);
+gs_status tma_plan_launch(const void* src, int step, gs_stream stream);
+
 }  // namespace gs_detail

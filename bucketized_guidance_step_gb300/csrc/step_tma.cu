@@ -30,10 +30,10 @@ EncodeTiled encoder() {
     return fn;
 }
 
-// A 3-D tiled map of a dense [d2][d1][d0] tensor with a [b2][b1][b0] box.  Boxes
-// whose rows are whole 256-byte lines or more let L2 fetch whole 256-byte lines;
-// narrower boxes (the column chunks of the narrowed prediction reads) fetch only the
-// sectors they touch, or the narrowing would bring in the columns it skips.
+// A 3-D tiled map of a dense [d2][d1][d0] tensor with a [b2][b1][b0] box.  Boxes of
+// whole rows let L2 fetch 256 bytes at a time; the 128-byte column chunks of the
+// narrowed prediction reads fetch 128 bytes, or the narrowing would bring in the
+// columns it skips.
 bool encode3d(CUtensorMap* m, CUtensorMapDataType dt, unsigned esize, const void* base,
               unsigned long long d0, unsigned long long d1, unsigned long long d2,
               unsigned long long pitch_elems, unsigned b0, unsigned b1, unsigned b2,
@@ -60,38 +60,44 @@ int gcd_int(int a, int b) {
     return a;
 }
 
-}  // namespace
+// Everything a launch of the TMA-fed step needs: the kernel parameters (with the
+// tensor maps encoded) and the instance and launch shape to use.
+struct TmaLaunch {
+    TmaParams p;
+    int dtype, cg, threads;
+    unsigned smem, flags;
+    bool reg, inp, nz, neg;
+};
 
-// Launch the TMA-pipelined step if the request fits it; *used says whether it did.
-gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_stream stream,
-                          bool* used, bool dry_run) {
-    *used = false;
-    if (flags & GS_LAUNCH_NO_TMA) return GS_OK;
-    if (encoder() == nullptr) return GS_OK;
+// Check that the request fits the TMA-fed kernel and build its launch; false if it
+// does not fit (or a tensor map cannot be encoded): the register kernel serves it.
+bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
+    if (flags & GS_LAUNCH_NO_TMA) return false;
+    if (encoder() == nullptr) return false;
     const unsigned es = dtype == GS_DTYPE_F32 ? 4u : 2u;
     const int vec = static_cast<int>(16u / es);
     const int B = sp.B, C = sp.C, H = sp.H, W = sp.W;
-    if ((static_cast<unsigned>(W) * es) % 16u != 0 || W > 256) return GS_OK;
-    if (!aligned16(sp.x) || !aligned16(sp.x_out)) return GS_OK;
-    if (sp.den_out != nullptr && !aligned16(sp.den_out)) return GS_OK;
-    if (sp.u != nullptr && !aligned16(sp.u)) return GS_OK;
-    if (sp.c != nullptr && !aligned16(sp.c)) return GS_OK;
+    if ((static_cast<unsigned>(W) * es) % 16u != 0 || W > 256) return false;
+    if (!aligned16(sp.x) || !aligned16(sp.x_out)) return false;
+    if (sp.den_out != nullptr && !aligned16(sp.den_out)) return false;
+    if (sp.u != nullptr && !aligned16(sp.u)) return false;
+    if (sp.c != nullptr && !aligned16(sp.c)) return false;
     const bool inp = sp.imask != nullptr;
     const bool anc = sp.sampler == GS_SAMPLER_EULER_ANCESTRAL;
     const bool mi = sp.model_in != nullptr;
     const bool nz = anc || mi;
     const bool neg = sp.has_neg != 0;
-    if (anc && !aligned16(sp.noise)) return GS_OK;
-    if (mi && (!aligned16(sp.model_in) || !aligned16(sp.orig_noise))) return GS_OK;
+    if (anc && !aligned16(sp.noise)) return false;
+    if (mi && (!aligned16(sp.model_in) || !aligned16(sp.orig_noise))) return false;
     if (inp && (!aligned16(sp.orig) || !aligned16(sp.imask) ||
                 (sp.imask_bstride != 0 && sp.imask_bstride != static_cast<long long>(H) * W)))
-        return GS_OK;
-    if (static_cast<long long>(B) * C > (1ll << 31) - 1 || B > 65535) return GS_OK;
+        return false;
+    if (static_cast<long long>(B) * C > (1ll << 31) - 1 || B > 65535) return false;
     for (int r = 0; r < sp.n_regions; ++r) {
         const DevRegion& R = sp.reg[r];
-        if (!R.vec_ok) return GS_OK;
+        if (!R.vec_ok) return false;
         const int wbox = (R.w + vec - 1) / vec * vec;
-        if (wbox > 256 || wbox > R.pitch) return GS_OK;
+        if (wbox > 256 || wbox > R.pitch) return false;
     }
 
     // Tile shape.  Measured on GB300 (rotating L2-cold inputs, back-to-back steps):
@@ -110,7 +116,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     // not depend on them).
     const int gpr = W / vec;
     const int rb0 = 32 / gcd_int(gpr, 32);             // smallest band with whole warps
-    if (rb0 * gpr > kMaxThreads) return GS_OK;
+    if (rb0 * gpr > kMaxThreads) return false;
     const long long units = static_cast<long long>(B) * H * gpr * C;
     const bool large = units >= (1ll << 18);
     int cg = 1, target_threads = 128;
@@ -136,8 +142,8 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
         rb = rows_override;
     const int threads = rb * gpr;
 
-    TmaParams p;
-    std::memset(&p, 0, sizeof(p));
+    std::memset(L, 0, sizeof(*L));
+    TmaParams& p = L->p;
     p.B = B;
     p.C = C;
     p.H = H;
@@ -224,7 +230,7 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     p.rowtab_off = off;
     off += round128(static_cast<unsigned>(sp.n_regions) * rb * 4u);
     p.tile_bytes = off;
-    if (p.tile_bytes > kMaxTileBytes) return GS_OK;
+    if (p.tile_bytes > kMaxTileBytes) return false;
     const unsigned smem = 128u + 128u + p.tile_bytes;   // alignment slack + mbarrier line
 
     // tensor maps
@@ -236,9 +242,9 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
     if (p.has_u) ok = ok && encode3d(&p.tm_u, dt, es, sp.u, W, H, bc, W, W, rb, cg);
     if (p.has_c) ok = ok && encode3d(&p.tm_c, dt, es, sp.c, W, H, bc, W, W, rb, cg);
     if (p.mask_spans != nullptr) {
-        // column chunks of 64 bytes for the prediction boxes narrowed to the mask
+        // column chunks of 128 bytes for the prediction boxes narrowed to the mask
         const unsigned chunk = static_cast<unsigned>(kChunkBytes) / es;
-        const CUtensorMapL2promotion np = CU_TENSOR_MAP_L2_PROMOTION_NONE;
+        const CUtensorMapL2promotion np = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
         if (p.has_u) ok = ok && encode3d(&p.tm_uc, dt, es, sp.u, W, H, bc, W, chunk, rb, cg, np);
         if (p.has_c) ok = ok && encode3d(&p.tm_cc, dt, es, sp.c, W, H, bc, W, chunk, rb, cg, np);
     }
@@ -257,33 +263,65 @@ gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_st
                       static_cast<unsigned long long>(R.pitch),
                       static_cast<unsigned>(p.reg[r].wbox), rb, cg);
     }
-    if (!ok) return GS_OK;
+    if (!ok) return false;
+    L->dtype = dtype;
+    L->cg = cg;
+    L->threads = threads;
+    L->smem = smem;
+    L->flags = flags;
+    L->reg = sp.n_regions > 0;
+    L->inp = inp;
+    L->nz = nz;
+    L->neg = neg;
+    return true;
+}
+
+gs_status launch_tma(TmaLaunch& L, gs_stream stream) {
+    TmaParams& p = L.p;
+    if (L.neg) return tma_launch_neg(p, L.dtype, L.nz, L.cg, L.threads, L.smem, L.inp, stream, L.flags);
+    if (L.nz)
+        return tma_launch_sampler(p, L.dtype, L.cg, L.threads, L.smem, L.reg, L.inp, stream, L.flags);
+    switch (L.dtype) {
+        case GS_DTYPE_F32:
+            return launch_features<F32, false>(p, L.cg, L.threads, L.smem, L.reg, L.inp, stream, L.flags);
+        case GS_DTYPE_BF16:
+            return launch_features<BF16, false>(p, L.cg, L.threads, L.smem, L.reg, L.inp, stream, L.flags);
+        default:
+            return launch_features<F16, false>(p, L.cg, L.threads, L.smem, L.reg, L.inp, stream, L.flags);
+    }
+}
+
+}  // namespace
+
+// Launch the TMA-pipelined step if the request fits it; *used says whether it did.
+gs_status launch_step_tma(const StepParams& sp, int dtype, unsigned flags, gs_stream stream,
+                          bool* used, bool dry_run) {
+    *used = false;
+    TmaLaunch L;
+    if (!build_tma(sp, dtype, flags, &L)) return GS_OK;
     if (dry_run) {
         *used = true;
         return GS_OK;
     }
-
-    gs_status st;
-    const bool reg = sp.n_regions > 0;
-    if (neg) {
-        st = tma_launch_neg(p, dtype, nz, cg, threads, smem, inp, stream, flags);
-    } else if (nz) {
-        st = tma_launch_sampler(p, dtype, cg, threads, smem, reg, inp, stream, flags);
-    } else {
-        switch (dtype) {
-            case GS_DTYPE_F32:
-                st = launch_features<F32, false>(p, cg, threads, smem, reg, inp, stream, flags);
-                break;
-            case GS_DTYPE_BF16:
-                st = launch_features<BF16, false>(p, cg, threads, smem, reg, inp, stream, flags);
-                break;
-            default:
-                st = launch_features<F16, false>(p, cg, threads, smem, reg, inp, stream, flags);
-                break;
-        }
-    }
+    const gs_status st = launch_tma(L, stream);
     if (st == GS_OK) *used = true;
     return st;
+}
+
+size_t tma_plan_bytes() { return sizeof(TmaLaunch); }
+
+bool tma_plan_build(const StepParams& sp, int dtype, unsigned flags, void* dst) {
+    TmaLaunch L;
+    if (!build_tma(sp, dtype, flags, &L)) return false;
+    std::memcpy(dst, &L, sizeof(L));
+    return true;
+}
+
+gs_status tma_plan_launch(const void* src, int step, gs_stream stream) {
+    TmaLaunch L;                  // (an aligned copy: the plan may sit anywhere)
+    std::memcpy(&L, src, sizeof(L));
+    L.p.step = step;
+    return launch_tma(L, stream);
 }
 
 }  // namespace gs_detail

@@ -105,9 +105,12 @@ struct TmaParams {
     unsigned chunk_bytes;        // CG * RB * kChunkCols * element size (column-chunk boxes)
 };
 
-// Column chunks of the narrowed prediction boxes: 64 bytes of a row (two DRAM
-// sectors), i.e. 32 16-bit or 16 fp32 elements.
-constexpr int kChunkBytes = 64;
+// Column chunks of the narrowed prediction boxes: 128 bytes of a row (64 16-bit or
+// 32 fp32 elements), aligned to 128 bytes of the row.  DRAM serves L2 in whole
+// 128-byte lines (measured: narrowing to 64-byte chunks still brought in the lines
+// they touch), so this is the finest narrowing that saves DRAM traffic, and it keeps
+// the number of boxes per plane small (one at W = 128 in 16-bit types).
+constexpr int kChunkBytes = 128;
 
 // Launch the instances with the sampler options (ancestral noise and/or the next
 // model input); defined in step_tma_sampler.cu.
@@ -327,6 +330,7 @@ struct TileParams {
     int xs, xv;         // frame columns [xs, xv) of the prediction are read (whole
                         //     vectors over the band's nonzero mask columns); the rest
                         //     is taken as 0
+    int xa;             // narrow: frame column of the first chunk's first element
 };
 
 // One region as this tile's threads use it, built once per CTA by the region's
@@ -351,8 +355,9 @@ __global__ void __launch_bounds__(kMaxThreads)
     // DEFER: the parameter thread issues the prediction boxes (uncond, cond, regions)
     // once it knows what the tile needs: nothing for a blended band whose mask is 0
     // on every row, uncond and cond narrowed to the band's nonzero mask columns (as
-    // column chunks) with the mask's span summary, and no uncond for a sample whose
-    // scale is exactly 1 when the caller asks for that.
+    // column chunks) with the mask's span summary, no uncond for a sample whose
+    // scale is exactly 1 when the caller asks for that, and no output of a region
+    // whose timestep range excludes the sample's step.
     // NEG: some regions belong to the uncond branch, which is then their weighted sum
     // with the full-frame uncond output (weight 1, if given), like the positive branch
     static_assert(!NEG || (REG && !DEFER), "negative regions: region instances only");
@@ -402,6 +407,10 @@ __global__ void __launch_bounds__(kMaxThreads)
     // at scale 1, thread 0 still issues cond and the regions, and the parameter thread
     // the uncond box alone
     const bool summary = DEFER && INP && (p.mask_rows != nullptr || p.mask_spans != nullptr);
+    // DEFER instances with regions that have timestep ranges: the parameter thread issues
+    // the region boxes once it knows the step index, and only those of the regions in
+    // range for the sample
+    const bool late_regions = DEFER && REG && (summary || p.ranged != 0);
     // sampler options (NZ instances only): ancestral noise (a box in x's group) and
     // the next model input (the fixed noise a box in the original's group)
     const bool anc = NZ && p.sampler == GS_SAMPLER_EULER_ANCESTRAL;
@@ -453,8 +462,9 @@ __global__ void __launch_bounds__(kMaxThreads)
     // In DEFER instances the parameter thread issues them (see DEFER above).
     constexpr bool defer = DEFER;
     // One prediction plane (uncond or cond) of the tile: one [CG][RB][W] box, or, when
-    // narrowed to frame columns [xs, xs + n * kChunk), n [CG][RB][kChunk] boxes laid
-    // out one after the other (columns past W arrive as zeros).
+    // narrowed to frame columns [xa, xa + n * kChunk) (xa a multiple of kChunk), n
+    // [CG][RB][kChunk] boxes laid out one after the other (columns past W arrive as
+    // zeros).
     auto issue_plane = [&](unsigned off, const CUtensorMap* map, const CUtensorMap* chunk_map,
                            bool narrow, int xs, int n) {
         if (!narrow) {
@@ -467,12 +477,14 @@ __global__ void __launch_bounds__(kMaxThreads)
             tma_load_3d(s0 + off + static_cast<unsigned>(j) * p.chunk_bytes, chunk_map,
                         xs + j * kChunk, y_band, z, bar);
     };
-    auto issue_regions = [&]() {
+    // (sidx >= 0: the sample's step index; regions out of their range are skipped)
+    auto issue_regions = [&](int sidx) {
         if constexpr (REG) {
-            // only the four fields the issue needs, read straight from the parameters
+            // only the fields the issue needs, read straight from the parameters
             for (int r = 0; r < p.n_regions; ++r) {
                 const int ry0 = p.reg[r].y0, rh = p.reg[r].h;
                 if (y_band >= ry0 + rh || y_band + p.RB <= ry0) continue;
+                if (sidx >= 0 && (sidx < p.reg[r].step_lo || sidx >= p.reg[r].step_hi)) continue;
                 mbar_add_tx(bar, p.reg[r].tile_bytes);
                 tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], 0, y_band - ry0, z, bar);
             }
@@ -481,7 +493,7 @@ __global__ void __launch_bounds__(kMaxThreads)
     auto issue_prediction = [&]() {
         if (has_u) issue_plane(p.off_u, &p.tm_u, &p.tm_uc, false, 0, 1);
         if (has_c) issue_plane(p.off_c, &p.tm_c, &p.tm_cc, false, 0, 1);
-        issue_regions();
+        issue_regions(-1);
     };
 
     // Thread 0: the boxes that need nothing but the tile coordinates.  Each box's
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(kMaxThreads)
             issue_prediction();
         } else if (!summary) {
             if (has_c) issue_plane(p.off_c, &p.tm_c, &p.tm_cc, false, 0, 1);
-            issue_regions();
+            if (!late_regions) issue_regions(-1);
         }
         if constexpr (kSplit) {
             if constexpr (!defer) {
@@ -533,7 +545,7 @@ __global__ void __launch_bounds__(kMaxThreads)
         const bool present = INP && (p.present == nullptr || __ldg(p.present + b) != 0);
         bool need_pred = true;
         bool narrow = false;
-        int xs = 0, xv = p.W, nch = 1;
+        int xs = 0, xv = p.W, xa = 0, nch = 1;
         if (defer && present && p.mask_spans != nullptr) {
             // the union of the band's rows' nonzero column spans [lo, hi)
             const unsigned* spans =
@@ -550,9 +562,10 @@ __global__ void __launch_bounds__(kMaxThreads)
             }
             need_pred = hi > 0;
             if (need_pred) {
-                xs = lo - lo % VEC;                          // 16-byte aligned box start
+                xs = lo - lo % VEC;                          // first vector read
                 xv = (hi + VEC - 1) / VEC * VEC;             // end of the vectors read
-                nch = (xv - xs + kChunk - 1) / kChunk;
+                xa = xs - xs % kChunk;                       // first chunk (128-byte aligned)
+                nch = (xv - xa + kChunk - 1) / kChunk;
                 narrow = nch * kChunk < p.W;                 // else one full-width box
                 // (with a full-width box the vectors outside [xs, xv) are still
                 // taken as 0: what is read does not depend on the box layout)
@@ -574,10 +587,13 @@ __global__ void __launch_bounds__(kMaxThreads)
         if constexpr (defer) {
             if (need_pred) {
                 if (use_u && !p.unit_skip)
-                    issue_plane(p.off_u, &p.tm_u, &p.tm_uc, narrow, xs, nch);
-                if (summary) {
-                    if (has_c) issue_plane(p.off_c, &p.tm_c, &p.tm_cc, narrow, xs, nch);
-                    issue_regions();
+                    issue_plane(p.off_u, &p.tm_u, &p.tm_uc, narrow, xa, nch);
+                if (summary && has_c) issue_plane(p.off_c, &p.tm_c, &p.tm_cc, narrow, xa, nch);
+                if (late_regions) {
+                    // the index decides which regions' timestep ranges hold (an index
+                    // out of range skips the sample: its boxes are not needed)
+                    const bool idx_ok = idx >= 0 && idx + 1 < p.n_sig;
+                    if (idx_ok || !p.ranged) issue_regions(p.ranged ? idx : -1);
                 }
             }
         }
@@ -594,12 +610,13 @@ __global__ void __launch_bounds__(kMaxThreads)
                     idx >= 0 && idx + 1 < p.n_sig && (p.lut == nullptr || idx < p.n_lut);
                 const float s1 = p.lut != nullptr ? __ldg(p.lut + (ok_idx ? idx : 0)) : p.cfg;
                 use_u = !(s1 == 1.0f);
-                if (use_u) issue_plane(p.off_u, &p.tm_u, &p.tm_uc, narrow, xs, nch);
+                if (use_u) issue_plane(p.off_u, &p.tm_u, &p.tm_uc, narrow, xa, nch);
             }
             tp.use_u = use_u ? 1 : 0;
             tp.narrow = narrow ? 1 : 0;
             tp.xs = xs;
             tp.xv = xv;
+            tp.xa = xa;
             if constexpr (kSplit) {
                 // group A is complete: with deferral this thread is its only feeder
                 if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
@@ -800,10 +817,9 @@ __global__ void __launch_bounds__(kMaxThreads)
     bool pred_in = true;
     unsigned pred_base = pix, pred_kstride = kstride;
     if constexpr (DEFER) {
-        const int dx = x0 - tp.xs;                        // a multiple of VEC
-        pred_in = dx >= 0 && x0 < tp.xv;
+        pred_in = x0 >= tp.xs && x0 < tp.xv;
         if (tp.narrow) {
-            const int dc = pred_in ? dx : 0;
+            const int dc = pred_in ? x0 - tp.xa : 0;      // a multiple of VEC
             pred_base = static_cast<unsigned>(dc / kChunk) * p.chunk_bytes +
                         static_cast<unsigned>(row * kChunk + dc % kChunk) * ES;
             pred_kstride = static_cast<unsigned>(p.RB) * kChunk * ES;
@@ -1063,14 +1079,14 @@ gs_status launch_features_neg(TmaParams& p, int cg, int threads, unsigned smem, 
 }
 
 // NZ = false: the deterministic Euler step; NZ = true: the sampler options.  The
-// deferred-prediction instances (a row or span summary of the inpaint mask, or the
-// uncond skip at scale 1) are instances of their own in both, so that the common
-// path pays nothing for them.
+// deferred-prediction instances (a row or span summary of the inpaint mask, the
+// uncond skip at scale 1, or regions with timestep ranges) are instances of their own
+// in both, so that the common path pays nothing for them.
 template <typename T, bool NZ>
 gs_status launch_features(TmaParams& p, int cg, int threads, unsigned smem, bool reg, bool inp,
                           gs_stream stream, unsigned flags) {
-    const bool defer =
-        (inp && (p.mask_rows != nullptr || p.mask_spans != nullptr)) || p.unit_skip != 0;
+    const bool defer = (inp && (p.mask_rows != nullptr || p.mask_spans != nullptr)) ||
+                       p.unit_skip != 0 || (reg && p.ranged != 0);
     if (reg) {
         if (inp && defer) return launch_cg<T, true, true, true, NZ>(p, cg, threads, smem, stream, flags);
         if (inp) return launch_cg<T, true, true, false, NZ>(p, cg, threads, smem, stream, flags);

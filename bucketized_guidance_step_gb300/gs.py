@@ -37,9 +37,10 @@ GS_LAUNCH_PDL = 1
 GS_LAUNCH_NO_TMA = 2
 GS_LAUNCH_TEST_WAIT_TIMEOUT = 4
 GS_ABI_VERSION = 6
+GS_STEP_PLAN_BYTES = 8192
 
 EXPORTS = ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_mask_spans",
-           "gs_guided_step",
+           "gs_guided_step", "gs_step_prepare", "gs_step_launch",
            "gs_areas_to_latent", "gs_pack_conds",
            "gs_step_kernel_kind", "gs_status_from_word", "gs_status_string", "gs_abi_version")
 GS_KERNEL_SCALAR, GS_KERNEL_VECTOR, GS_KERNEL_TMA = 0, 1, 2
@@ -123,6 +124,11 @@ class StepArgs(ctypes.Structure):
                 ("mask_spans", ctypes.c_void_p), ("unit_scale_skip", ctypes.c_int32)]
 
 
+class StepPlan(ctypes.Structure):
+    """gs_step_plan: a prepared launch (opaque, caller-owned host memory)."""
+    _fields_ = [("opaque", ctypes.c_uint64 * (GS_STEP_PLAN_BYTES // 8))]
+
+
 def library_path() -> str:
     return _LIB_PATH
 
@@ -150,6 +156,8 @@ def load() -> ctypes.CDLL:
         lib.gs_mask_spans.argtypes = [p, i32, i32, i32, p, p]
         lib.gs_guided_step.argtypes = [ctypes.POINTER(StepArgs), p]
         lib.gs_step_kernel_kind.argtypes = [ctypes.POINTER(StepArgs), p]
+        lib.gs_step_prepare.argtypes = [ctypes.POINTER(StepArgs), ctypes.POINTER(StepPlan)]
+        lib.gs_step_launch.argtypes = [ctypes.POINTER(StepPlan), i32, p]
         lib.gs_status_from_word.argtypes = [ctypes.c_uint32]
         lib.gs_status_string.argtypes = [i32]
         lib.gs_status_string.restype = ctypes.c_char_p
@@ -159,7 +167,7 @@ def load() -> ctypes.CDLL:
         lib.gs_pack_conds.argtypes = [ctypes.POINTER(CondEntry), i32, ctypes.c_int64,
                                       ctypes.POINTER(CondChunk), i32, p, p]
         for f in ("gs_sigmas", "gs_bucket_plan", "gs_mask_prepare", "gs_mask_rows", "gs_mask_spans",
-                  "gs_guided_step",
+                  "gs_guided_step", "gs_step_prepare", "gs_step_launch",
                   "gs_step_kernel_kind", "gs_status_from_word", "gs_abi_version",
                   "gs_areas_to_latent", "gs_pack_conds"):
             getattr(lib, f).restype = i32
@@ -482,6 +490,21 @@ def make_step_args(x, *, sigmas, uncond=None, cond=None, stacked=None, step_idx=
 def launch_step(args: StepArgs, stream=None) -> None:
     """gs_guided_step on prepared arguments (the lowest-overhead call)."""
     _check("gs_guided_step", load().gs_guided_step(ctypes.byref(args), _stream_ptr(stream)))
+
+
+def prepare_step(args: StepArgs) -> StepPlan:
+    """gs_step_prepare: check prepared arguments once and build the launch (the
+    tensors behind the arguments must stay alive while the plan is used)."""
+    plan = StepPlan()
+    _check("gs_step_prepare", load().gs_step_prepare(ctypes.byref(args), ctypes.byref(plan)))
+    return plan
+
+
+def launch_prepared(plan: StepPlan, step: int = 0, stream=None) -> None:
+    """gs_step_launch: one step from a plan (step: the shared step index when the plan
+    was prepared without step_idx)."""
+    _check("gs_step_launch", load().gs_step_launch(ctypes.byref(plan), int(step),
+                                                   _stream_ptr(stream)))
 
 
 def kernel_kind(args: StepArgs) -> str:

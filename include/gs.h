@@ -242,7 +242,9 @@ gs_status gs_mask_spans(const float* lat_mask, int32_t Bm, int32_t H, int32_t W,
  *            the region takes part for sample b only when t_start <= i/S < t_end,
  *            i = the sample's step index, S = n_sigmas - 1, evaluated in binary64
  *            (the progress the guidance buckets use).  t_end <= t_start (a zeroed
- *            struct) means no range: every step.
+ *            struct) means no range: every step.  The TMA-fed kernels do not read
+ *            a region's output for the samples whose step is out of its range
+ *            (except with negative regions).
  *   negative: 0 = the region is part of the positive (cond) branch; 1 = of the
  *            uncond branch (regional uncond: negative conditioning carries the same
  *            area, mask and strength metadata, [SAMPLING] "negative 不是简单“反向
@@ -360,7 +362,8 @@ typedef struct gs_step_args {
        the prediction reads of a blended band whose mask is 0 on every row, as with
        mask_rows, and in the other bands of a blended sample read uncond and cond
        only from the band's first to its last nonzero mask column (rounded out to
-       16-byte vectors; loaded as 64-byte column chunks): outside that span the
+       16-byte vectors; loaded as 128-byte column chunks aligned to 128 bytes of the
+       row, DRAM's unit of transfer to L2, or as whole rows): outside that span the
        prediction is taken as 0 (den is the original exactly there, up to the sign of
        zero), so a non-finite prediction there does not propagate.  Region outputs
        are read whole in the bands they touch.
@@ -431,6 +434,40 @@ typedef struct gs_step_args {
  * GS_ERR_CUDA (launch failure).  Device-found errors: see dev_status.
  */
 gs_status gs_guided_step(const gs_step_args* args, gs_stream stream);
+
+/* ---- Prepared launches ------------------------------------------------------------
+ * A sampler that steps the same buffers many times can check the arguments and build
+ * the launch once (gs_step_prepare) and then launch one step per call
+ * (gs_step_launch), which skips the argument checks and the tensor-map encoding
+ * gs_guided_step repeats on every call.  The plan is caller-owned host memory; the
+ * library allocates nothing.  The plan holds the device pointers of the arguments it
+ * was prepared from: the caller keeps those buffers alive and unmoved while it uses
+ * the plan, and prepares a new plan for other buffers (e.g. one plan per buffer of a
+ * ping-pong pair).  The step's results are those of gs_guided_step with the same
+ * arguments ([SAMPLING] "comfy.sample.sample()": the sampler calls the same step
+ * function every step; only the step index moves).
+ */
+#define GS_STEP_PLAN_BYTES 8192
+typedef struct gs_step_plan {
+    uint64_t opaque[GS_STEP_PLAN_BYTES / 8];   /* any 8-byte-aligned host memory */
+} gs_step_plan;
+
+/*
+ * gs_step_prepare -- check the arguments as gs_guided_step does and write a plan.
+ * args: as for gs_guided_step (args->step is ignored: gs_step_launch passes it);
+ * plan: host, caller-owned, written in full.
+ * Errors: those of gs_guided_step's checks; GS_ERR_INVALID_ARG for a NULL plan.
+ */
+gs_status gs_step_prepare(const gs_step_args* args, gs_step_plan* plan);
+
+/*
+ * gs_step_launch -- one step from a plan, enqueued on `stream` (one kernel launch).
+ * step: the step index of every sample (0 <= step <= n_sigmas - 2) when the plan was
+ *       prepared without step_idx; ignored otherwise.
+ * Errors: GS_ERR_INVALID_ARG (NULL or unprepared plan, step out of range),
+ *         GS_ERR_CUDA (launch failure).  Device-found errors: see dev_status.
+ */
+gs_status gs_step_launch(const gs_step_plan* plan, int32_t step, gs_stream stream);
 
 /* Kernels gs_guided_step chooses between (same results, different data movement). */
 enum { GS_KERNEL_SCALAR = 0, GS_KERNEL_VECTOR = 1, GS_KERNEL_TMA = 2 };

@@ -155,6 +155,7 @@ int main(void) {
     printf("gs_rect sizeof %zu\n", sizeof(gs_rect));
     printf("gs_cond_entry sizeof %zu\n", sizeof(gs_cond_entry));
     printf("gs_cond_chunk sizeof %zu\n", sizeof(gs_cond_chunk));
+    printf("gs_step_plan sizeof %zu\n", sizeof(gs_step_plan));
     %FIELDS%
     return 0;
 }
@@ -171,7 +172,7 @@ def test_ctypes_structs_match_the_header_layout(repo_tmp):
     pairs = {"gs_step_args": gs.StepArgs, "gs_region": gs.RegionDesc,
              "gs_curve_desc": gs.CurveDesc, "gs_schedule_desc": gs.ScheduleDesc,
              "gs_area": gs.Area, "gs_rect": gs.Rect, "gs_cond_entry": gs.CondEntry,
-             "gs_cond_chunk": gs.CondChunk}
+             "gs_cond_chunk": gs.CondChunk, "gs_step_plan": gs.StepPlan}
     fields = "\n    ".join(f"F({c}, {f})" for c, py in pairs.items() for f, _ in py._fields_)
     src = repo_tmp / "layout.c"
     src.write_text(_LAYOUT_PROBE.replace("%FIELDS%", fields))
@@ -203,3 +204,21 @@ def test_step_rejects_bad_negative_regions(lib):
     a.n_regions = 1
     a.regions = ctypes.cast(arr, ctypes.POINTER(gs.RegionDesc))
     assert lib.gs_guided_step(ctypes.byref(a), None) == gs.GS_ERR_INVALID_ARG
+
+
+def test_step_plan_checks_before_any_launch(lib):
+    """gs_step_prepare answers like gs_guided_step's checks; gs_step_launch refuses an
+    unprepared plan and a step index out of range before launching anything."""
+    plan = gs.StepPlan()
+    assert lib.gs_step_prepare(ctypes.byref(_valid_args()), None) == gs.GS_ERR_INVALID_ARG
+    for field, value in (("B", 0), ("x", 0), ("n_sigmas", 1), ("n_regions", 17)):
+        a = _valid_args()
+        setattr(a, field, value)
+        assert lib.gs_step_prepare(ctypes.byref(a), ctypes.byref(plan)) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_step_launch(ctypes.byref(gs.StepPlan()), 0, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_step_launch(None, 0, None) == gs.GS_ERR_INVALID_ARG
+    a = _valid_args()                                     # n_sigmas 5: steps 0 .. 3
+    a.step = 99                                           # (ignored by the plan)
+    assert lib.gs_step_prepare(ctypes.byref(a), ctypes.byref(plan)) == gs.GS_OK
+    for step in (-1, 4, 1 << 30):
+        assert lib.gs_step_launch(ctypes.byref(plan), step, None) == gs.GS_ERR_INVALID_ARG

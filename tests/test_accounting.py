@@ -60,3 +60,20 @@ def test_required_bytes_hand_counts():
     uncond_needed = 2 * 16 * 2                     # row 2's first sector, both channels
     region_needed = 2 * 2 * 8 * 2                  # both rows of both channels
     assert got == full - (2 * 4 * 32 * 2 - uncond_needed) - (2 * 2 * 8 * 2 - region_needed)
+
+
+def test_required_bytes_at_line_granularity():
+    """At 128-byte granularity a line holds two 64-byte rows: the one nonzero pixel of
+    the hand example makes both rows of each channel's line required."""
+    import numpy as np
+
+    from bucketized_guidance_step_gb300.accounting import required_bytes
+    m = np.zeros((1, 2, 32), bool)
+    m[0, 1, 20] = True
+    full = step_bytes(1, 2, 2, 32, "bf16", inpaint_samples=1)
+    assert required_bytes(1, 2, 2, 32, "bf16", mask_nz=m, granule=128) == full
+    m = np.zeros((1, 4, 32), bool)                 # rows 2..3 of each channel: second line
+    m[0, 0, 0] = True
+    plane = 2 * 4 * 32 * 2
+    assert required_bytes(1, 2, 4, 32, "bf16", mask_nz=m, granule=128) == \
+        step_bytes(1, 2, 4, 32, "bf16", inpaint_samples=1) - 2 * (plane - 2 * 128)

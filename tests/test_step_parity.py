@@ -36,7 +36,7 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
              tma: bool = True, expect_kernel: str = None, mask_rows: bool = False,
              poison: bool = False, region_ranges=None, sampler: str = "euler",
              model_in: bool = False, sigmas=None, negative=(), mask_spans: bool = False,
-             unit_skip: bool = False, lut=None):
+             unit_skip: bool = False, lut=None, poison_ranges: bool = False):
     """Run one step on the GPU and in the oracle; return (report, gpu, ref, ok).
 
     mask_rows: pass the row summary of the latent mask (gs_mask_rows), so that bands
@@ -57,6 +57,8 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     that no vector the kernel reads is poisoned, whatever tile shape it picks.  unit_skip: samples whose scale is
     exactly 1 skip their uncond read; with poison their whole uncond is NaN on the GPU
     side.  lut: a per-step scale table (float32) in place of the workload's.
+    poison_ranges: on the GPU side only, fill each region's slab with NaN for the samples
+    whose step is outside the region's timestep range (the TMA kernel must not read it).
     """
     if sampler != wl.sampler or model_in != wl.model_input:
         wl = dataclasses.replace(wl, sampler=sampler, model_input=model_in)
@@ -146,10 +148,19 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
                     lo, hi = max(y0, r.y0), min(y0 + 32, r.y0 + r.h)
                     if lo < hi:
                         o[bi, :, lo - r.y0:hi - r.y0] = nan
+    ranges = region_ranges or [(0.0, 0.0)] * len(inp.regions)
+    if poison_ranges:
+        S = len(sig) - 1
+        reg_outs = [o.clone() for o in reg_outs]
+        for (t0, t1), o in zip(ranges, reg_outs):
+            if t1 <= t0:
+                continue
+            for bi in range(Bn):
+                if not (t0 <= idx[bi] / S < t1):
+                    o[bi] = float("nan")
     xd = dev_latent(x)
     outd = dev_latent(torch.full_like(x, float("nan")))
     dend = dev_latent(torch.full_like(x, float("nan"))) if want_den else None
-    ranges = region_ranges or [(0.0, 0.0)] * len(inp.regions)
     regs = [gs.Region(r.y0, r.x0, r.h, r.w, r.strength, r.feather, _cuda(o), _cuda(r.mask),
                       t_start=t0, t_end=t1, negative=i in negative)
             for i, (r, o, (t0, t1)) in enumerate(zip(inp.regions, reg_outs, ranges))]
@@ -379,6 +390,11 @@ def test_region_timestep_ranges(wl, tma):
     rep, *_ = run_case(wl, tma=tma, region_ranges=ranges, step=7,
                        expect_kernel="tma" if tma else "vector")
     assert rep.n == wl.elements
+    if tma:
+        # the TMA kernel does not read a region's output for samples out of its range
+        rep, got, *_ = run_case(wl, region_ranges=ranges, step=7, poison_ranges=True,
+                                expect_kernel="tma")
+        assert np.isfinite(got).all()
 
 
 @pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
