@@ -77,7 +77,32 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
     const unsigned es = dtype == GS_DTYPE_F32 ? 4u : 2u;
     const int vec = static_cast<int>(16u / es);
     const int B = sp.B, C = sp.C, H = sp.H, W = sp.W;
-    if ((static_cast<unsigned>(W) * es) % 16u != 0 || W > 256) return false;
+    if ((static_cast<unsigned>(W) * es) % 16u != 0) return false;
+    // Tile width: whole rows of W columns, or column blocks of Wt columns each (a
+    // multiple of the vector, at most 256 - vec, so that a region's box over a block --
+    // its columns under the block, from a 16-byte boundary -- stays within TMA's
+    // 256-column box).  The ncb blocks of a row cover ncb * Wt >= W columns; columns
+    // past W are loaded as zeros and not written.  A width qualifies when a band of
+    // whole warps of its pixel groups fits 256 threads; among those, the least
+    // ncb * (Wt + 32) wins (the columns a row's tiles load, plus a per-tile cost of
+    // about 32 columns), fewer blocks on a tie.  W <= 256 with such a band: one block.
+    int Wt = 0, ncb = 0;
+    {
+        long long best = -1;
+        for (int wt = vec; wt <= 256; wt += vec) {
+            const int nb = (W + wt - 1) / wt;
+            if (nb > 1 && wt + vec > 256) continue;
+            const int g = wt / vec;
+            if (32 / gcd_int(g, 32) * g > kMaxThreads) continue;
+            const long long cost = static_cast<long long>(nb) * (wt + 32);
+            if (best < 0 || cost < best || (cost == best && nb < ncb)) {
+                best = cost;
+                Wt = wt;
+                ncb = nb;
+            }
+        }
+        if (best < 0) return false;
+    }
     if (!aligned16(sp.x) || !aligned16(sp.x_out)) return false;
     if (sp.den_out != nullptr && !aligned16(sp.den_out)) return false;
     if (sp.u != nullptr && !aligned16(sp.u)) return false;
@@ -93,10 +118,15 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
                 (sp.imask_bstride != 0 && sp.imask_bstride != static_cast<long long>(H) * W)))
         return false;
     if (static_cast<long long>(B) * C > (1ll << 31) - 1 || B > 65535) return false;
+    // a region's box: its whole width, or over a column block at most Wt + vec columns
+    auto region_box = [&](const DevRegion& R) {
+        const int wbox = (R.w + vec - 1) / vec * vec;
+        return ncb > 1 ? std::min(wbox, Wt + vec) : wbox;
+    };
     for (int r = 0; r < sp.n_regions; ++r) {
         const DevRegion& R = sp.reg[r];
         if (!R.vec_ok) return false;
-        const int wbox = (R.w + vec - 1) / vec * vec;
+        const int wbox = region_box(R);
         if (wbox > 256 || wbox > R.pitch) return false;
     }
 
@@ -114,10 +144,10 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
     //     per SM): 2 channels measured 30 % slower on the sweep shape.
     // GS_TMA_CHANNELS=1|2|4 and GS_TMA_ROWS override (tuning knobs; results do
     // not depend on them).
-    const int gpr = W / vec;
+    const int gpr = Wt / vec;                            // threads per tile row
     const int rb0 = 32 / gcd_int(gpr, 32);             // smallest band with whole warps
     if (rb0 * gpr > kMaxThreads) return false;
-    const long long units = static_cast<long long>(B) * H * gpr * C;
+    const long long units = static_cast<long long>(B) * H * (W / vec) * C;
     const bool large = units >= (1ll << 18);
     int cg = 1, target_threads = 128;
     if (large && sp.n_regions > 0) {
@@ -149,9 +179,11 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
     p.H = H;
     p.W = W;
     p.RB = rb;
+    p.Wt = Wt;
+    p.ncb = ncb;
     p.nbands = (H + rb - 1) / rb;
     p.ncg = C / cg;
-    p.n_tiles = static_cast<long long>(B) * p.ncg * p.nbands;
+    p.n_tiles = static_cast<long long>(B) * p.ncg * p.nbands * ncb;
     p.x_out = sp.x_out;
     p.den_out = sp.den_out;
     p.sig = sp.sig;
@@ -181,8 +213,8 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
     p.n_regions = sp.n_regions;
 
     // stage layout
-    const unsigned plane = static_cast<unsigned>(cg) * rb * W * es;
-    const unsigned maskb = static_cast<unsigned>(rb) * W * 4u;
+    const unsigned plane = static_cast<unsigned>(cg) * rb * Wt * es;
+    const unsigned maskb = static_cast<unsigned>(rb) * Wt * 4u;
     unsigned off = 0;
     p.plane_bytes = plane;
     p.mask_bytes = maskb;
@@ -209,7 +241,7 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
         d.inv_feather = R.inv_feather;
         d.edges = R.edges | (R.negative ? kRegionNegative : 0);
         d.feather = R.feather;
-        d.wbox = (R.w + vec - 1) / vec * vec;
+        d.wbox = region_box(R);
         d.mask = R.mask;
         d.mask_bstride = R.mask_bstride;
         d.step_lo = R.step_lo;
@@ -224,7 +256,8 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
         d.col0 = d.x0 - d.x0 % vec;
         d.ncol = (d.x0 + d.w - d.col0 + vec - 1) / vec * vec;
         d.tab_off = off;
-        off += round128(static_cast<unsigned>(d.ncol) * 4u);
+        // (a tile fills only its own columns' entries: at most Wt of them)
+        off += round128(static_cast<unsigned>(std::min(d.ncol, Wt)) * 4u);
     }
     // Row-factor tables (fp32): region r's band rows at rowtab_off + 4 * (r * rb + i).
     p.rowtab_off = off;
@@ -238,9 +271,9 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
                                    : dtype == GS_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const unsigned long long bc = static_cast<unsigned long long>(B) * C;
-    bool ok = encode3d(&p.tm_x, dt, es, sp.x, W, H, bc, W, W, rb, cg);
-    if (p.has_u) ok = ok && encode3d(&p.tm_u, dt, es, sp.u, W, H, bc, W, W, rb, cg);
-    if (p.has_c) ok = ok && encode3d(&p.tm_c, dt, es, sp.c, W, H, bc, W, W, rb, cg);
+    bool ok = encode3d(&p.tm_x, dt, es, sp.x, W, H, bc, W, Wt, rb, cg);
+    if (p.has_u) ok = ok && encode3d(&p.tm_u, dt, es, sp.u, W, H, bc, W, Wt, rb, cg);
+    if (p.has_c) ok = ok && encode3d(&p.tm_c, dt, es, sp.c, W, H, bc, W, Wt, rb, cg);
     if (p.mask_spans != nullptr) {
         // column chunks of 128 bytes for the prediction boxes narrowed to the mask
         const unsigned chunk = static_cast<unsigned>(kChunkBytes) / es;
@@ -249,12 +282,12 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
         if (p.has_c) ok = ok && encode3d(&p.tm_cc, dt, es, sp.c, W, H, bc, W, chunk, rb, cg, np);
     }
     if (inp) {
-        ok = ok && encode3d(&p.tm_o, dt, es, sp.orig, W, H, bc, W, W, rb, cg);
+        ok = ok && encode3d(&p.tm_o, dt, es, sp.orig, W, H, bc, W, Wt, rb, cg);
         ok = ok && encode3d(&p.tm_m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sp.imask, W, H,
-                            p.mask_shared ? 1 : B, W, W, rb, 1);
-        if (mi) ok = ok && encode3d(&p.tm_on, dt, es, sp.orig_noise, W, H, bc, W, W, rb, cg);
+                            p.mask_shared ? 1 : B, W, Wt, rb, 1);
+        if (mi) ok = ok && encode3d(&p.tm_on, dt, es, sp.orig_noise, W, H, bc, W, Wt, rb, cg);
     }
-    if (anc) ok = ok && encode3d(&p.tm_n, dt, es, sp.noise, W, H, bc, W, W, rb, cg);
+    if (anc) ok = ok && encode3d(&p.tm_n, dt, es, sp.noise, W, H, bc, W, Wt, rb, cg);
     for (int r = 0; r < sp.n_regions && ok; ++r) {
         const DevRegion& R = sp.reg[r];
         // Inner extent w (not pitch): TMA zero-fills box columns w .. wbox-1.

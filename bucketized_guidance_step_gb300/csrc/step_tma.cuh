@@ -87,6 +87,8 @@ struct TmaParams {
     long long n_tiles;
     int B, C, H, W;
     int RB, nbands, ncg;
+    int Wt, ncb;                 // tile width in columns (W, or a column block of a wider
+                                 // latent) and column blocks per row band
     int n_regions, n_sig, step, n_lut;
     float cfg;
     int has_u, has_c, mask_shared;
@@ -218,6 +220,14 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 
 __device__ __forceinline__ void flag(unsigned int* status, unsigned bits) {
     if (status != nullptr) atomicOr(status, bits);
+}
+
+// The first slab column of a region's box in the tile whose first frame column is xb0:
+// the region's column under xb0 (0 if the region starts inside the tile), rounded
+// down to whole 16-byte vectors (TMA boxes start on 16-byte boundaries).
+__device__ __forceinline__ int region_box_x(int rx0, int xb0, int vec) {
+    const int sx = xb0 > rx0 ? xb0 - rx0 : 0;
+    return sx - sx % vec;
 }
 
 // The parameter thread: the first lane of warp 1, or thread 0 in one-warp tiles.
@@ -391,13 +401,15 @@ __global__ void __launch_bounds__(kMaxThreads)
     unsigned long long* full = reinterpret_cast<unsigned long long*>(smem);
     unsigned char* st = smem + 128;
 
-    const int band = blockIdx.x;
+    const int band = blockIdx.x / p.ncb;
+    const int xb0 = (blockIdx.x - band * p.ncb) * p.Wt;   // the tile's first frame column
     const int cgi = blockIdx.y;
     const int b = blockIdx.z;
     const int nthreads = blockDim.x * blockDim.y;
     const int tid = threadIdx.y * blockDim.x + threadIdx.x;
     const int row = threadIdx.y;
-    const int x0 = threadIdx.x * VEC;
+    const int lx = threadIdx.x * VEC;                     // column within the tile
+    const int x0 = xb0 + lx;                              // frame column
     const int y_band = band * p.RB;
     const int y = y_band + row;
     const int z = b * p.C + cgi * CG;
@@ -469,7 +481,7 @@ __global__ void __launch_bounds__(kMaxThreads)
                            bool narrow, int xs, int n) {
         if (!narrow) {
             mbar_add_tx(bar, p.plane_bytes);
-            tma_load_3d(s0 + off, map, 0, y_band, z, bar);
+            tma_load_3d(s0 + off, map, xb0, y_band, z, bar);
             return;
         }
         mbar_add_tx(bar, static_cast<unsigned>(n) * p.chunk_bytes);
@@ -485,8 +497,11 @@ __global__ void __launch_bounds__(kMaxThreads)
                 const int ry0 = p.reg[r].y0, rh = p.reg[r].h;
                 if (y_band >= ry0 + rh || y_band + p.RB <= ry0) continue;
                 if (sidx >= 0 && (sidx < p.reg[r].step_lo || sidx >= p.reg[r].step_hi)) continue;
+                const int rx0 = p.reg[r].x0;
+                if (rx0 >= xb0 + p.Wt || rx0 + p.reg[r].w <= xb0) continue;   // column block
                 mbar_add_tx(bar, p.reg[r].tile_bytes);
-                tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], 0, y_band - ry0, z, bar);
+                tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], region_box_x(rx0, xb0, VEC),
+                            y_band - ry0, z, bar);
             }
         }
     };
@@ -502,10 +517,10 @@ __global__ void __launch_bounds__(kMaxThreads)
     if (tid == 0) {
         if constexpr (!kSplit) {
             mbar_add_tx(bar, p.plane_bytes);
-            tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, bar);
+            tma_load_3d(s0 + p.off_x, &p.tm_x, xb0, y_band, z, bar);
             if (anc) {
                 mbar_add_tx(bar, p.plane_bytes);
-                tma_load_3d(s0 + p.off_n, &p.tm_n, 0, y_band, z, bar);
+                tma_load_3d(s0 + p.off_n, &p.tm_n, xb0, y_band, z, bar);
             }
         }
         if constexpr (!defer) {
@@ -524,10 +539,10 @@ __global__ void __launch_bounds__(kMaxThreads)
                 if (!summary && ptid_of(nthreads) != 0) mbar_arrive(bar);
             }
             mbar_add_tx(barB, p.plane_bytes);
-            tma_load_3d(s0 + p.off_x, &p.tm_x, 0, y_band, z, barB);
+            tma_load_3d(s0 + p.off_x, &p.tm_x, xb0, y_band, z, barB);
             if (anc) {
                 mbar_add_tx(barB, p.plane_bytes);
-                tma_load_3d(s0 + p.off_n, &p.tm_n, 0, y_band, z, barB);
+                tma_load_3d(s0 + p.off_n, &p.tm_n, xb0, y_band, z, barB);
             }
         }
     }
@@ -545,28 +560,30 @@ __global__ void __launch_bounds__(kMaxThreads)
         const bool present = INP && (p.present == nullptr || __ldg(p.present + b) != 0);
         bool need_pred = true;
         bool narrow = false;
-        int xs = 0, xv = p.W, xa = 0, nch = 1;
+        int xs = xb0, xv = min(xb0 + p.Wt, p.W), xa = 0, nch = 1;
         if (defer && present && p.mask_spans != nullptr) {
             // the union of the band's rows' nonzero column spans [lo, hi)
             const unsigned* spans =
                 p.mask_spans + (p.mask_shared ? 0ll : static_cast<long long>(b) * p.H);
             const int y_end = y_band + p.RB < p.H ? y_band + p.RB : p.H;
-            int lo = p.W, hi = 0;
+            const int xe0 = min(xb0 + p.Wt, p.W);                // the tile's columns
+            int lo = xe0, hi = xb0;
             for (int yy = y_band; yy < y_end; ++yy) {
                 const unsigned w = __ldg(spans + yy);
-                const int h = static_cast<int>(w >> 16);
-                if (h > 0) {
-                    lo = min(lo, static_cast<int>(w & 0xffffu));
+                const int h = min(static_cast<int>(w >> 16), xe0);
+                const int l = max(static_cast<int>(w & 0xffffu), xb0);
+                if (h > l) {
+                    lo = min(lo, l);
                     hi = max(hi, h);
                 }
             }
-            need_pred = hi > 0;
+            need_pred = hi > lo;
             if (need_pred) {
                 xs = lo - lo % VEC;                          // first vector read
                 xv = (hi + VEC - 1) / VEC * VEC;             // end of the vectors read
                 xa = xs - xs % kChunk;                       // first chunk (128-byte aligned)
                 nch = (xv - xa + kChunk - 1) / kChunk;
-                narrow = nch * kChunk < p.W;                 // else one full-width box
+                narrow = nch * kChunk < p.Wt;                // else one full-width box
                 // (with a full-width box the vectors outside [xs, xv) are still
                 // taken as 0: what is read does not depend on the box layout)
             }
@@ -599,9 +616,9 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
         if (INP && present) {
             mbar_add_tx(barB, p.plane_bytes + p.mask_bytes + (want_mi ? p.plane_bytes : 0u));
-            tma_load_3d(s0 + p.off_o, &p.tm_o, 0, y_band, z, barB);
-            tma_load_3d(s0 + p.off_m, &p.tm_m, 0, y_band, p.mask_shared ? 0 : b, barB);
-            if (want_mi) tma_load_3d(s0 + p.off_on, &p.tm_on, 0, y_band, z, barB);
+            tma_load_3d(s0 + p.off_o, &p.tm_o, xb0, y_band, z, barB);
+            tma_load_3d(s0 + p.off_m, &p.tm_m, xb0, y_band, p.mask_shared ? 0 : b, barB);
+            if (want_mi) tma_load_3d(s0 + p.off_on, &p.tm_on, xb0, y_band, z, barB);
         }
         if constexpr (defer) {
             if (use_u && p.unit_skip) {
@@ -672,8 +689,12 @@ __global__ void __launch_bounds__(kMaxThreads)
                              : 0;
         for (int r = warp - w0; r >= 0 && r < p.n_regions; r += nwarps - w0) {
             const TmaRegion R = p.reg[r];
-            const bool hits =
-                band_hits(R, y_band, p.RB) && sidx >= R.step_lo && sidx < R.step_hi;
+            const bool hits = band_hits(R, y_band, p.RB) && sidx >= R.step_lo &&
+                              sidx < R.step_hi && R.x0 < xb0 + p.Wt && R.x0 + R.w > xb0;
+            // column-table entries for the tile's part of the region: frame columns
+            // [c0b, c1b), entry i at frame column c0b + i
+            const int c0b = max(R.col0, xb0);
+            const int c1b = min(R.col0 + R.ncol, xb0 + p.Wt);
             if (lane == 0) {
                 regs[r] = R;
                 TileRegion t;
@@ -682,13 +703,13 @@ __global__ void __launch_bounds__(kMaxThreads)
                 t.x_lo = R.x0;
                 t.x_hi = R.x0 + R.w;
                 t.sh = (VEC - R.x0 % VEC) % VEC;
-                t.qoff = -R.x0 - t.sh;
+                t.qoff = -R.x0 - t.sh - region_box_x(R.x0, xb0, VEC);
                 t.nq = R.wbox / VEC;
                 t.flags = (R.mask != nullptr ? 1 : 0) | ((R.edges & kRegionNegative) ? 2 : 0);
                 t.rbase0 = R.smem_off;
                 t.rrow = static_cast<unsigned>(R.wbox) * sizeof(S);
                 t.rk = static_cast<unsigned>(p.RB) * R.wbox * sizeof(S);
-                t.tabx = static_cast<int>(R.tab_off) - 4 * R.col0;
+                t.tabx = static_cast<int>(R.tab_off) - 4 * c0b;
                 tregs[r] = t;
             }
             if (!hits) continue;
@@ -702,8 +723,8 @@ __global__ void __launch_bounds__(kMaxThreads)
                 rowtab[i] = wrow;
             }
             float* tab = reinterpret_cast<float*>(st + R.tab_off);
-            for (int i = lane; i < R.ncol; i += 32) {
-                const int tx = R.col0 + i - R.x0;
+            for (int i = lane; i < c1b - c0b; i += 32) {
+                const int tx = c0b + i - R.x0;
                 tab[i] = (tx >= 0 && tx < R.w)
                              ? column_factor(R.edges, R.feather, R.inv_feather, tx, R.w)
                              : 0.0f;
@@ -761,7 +782,7 @@ __global__ void __launch_bounds__(kMaxThreads)
     }
     // rows past H (a ragged last band): no arithmetic (the CTA stays resident while
     // its other threads wait for group B)
-    const bool active = y < p.H;
+    const bool active = y < p.H && x0 < p.W;
     if (!active) return;
     const bool inpaint = INP && tp.inpaint != 0;
     if (DEFER && INP && tp.need_pred == 0) {
@@ -776,8 +797,8 @@ __global__ void __launch_bounds__(kMaxThreads)
                 return;
             }
         }
-        const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
-        const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
+        const unsigned pix = (static_cast<unsigned>(row) * p.Wt + lx) * ES;
+        const unsigned kstride = static_cast<unsigned>(p.RB) * p.Wt * ES;
         const long long plane = static_cast<long long>(p.H) * p.W;
         const long long gbase =
             static_cast<long long>(z) * plane + static_cast<long long>(y) * p.W + x0;
@@ -807,8 +828,8 @@ __global__ void __launch_bounds__(kMaxThreads)
         return;
     }
 
-    const unsigned pix = (static_cast<unsigned>(row) * p.W + x0) * ES;
-    const unsigned kstride = static_cast<unsigned>(p.RB) * p.W * ES;
+    const unsigned pix = (static_cast<unsigned>(row) * p.Wt + lx) * ES;
+    const unsigned kstride = static_cast<unsigned>(p.RB) * p.Wt * ES;
     // The prediction planes (uncond, cond): where this thread's vector sits in the
     // tile's box or column chunks, and whether it was read at all.  Narrowed tiles
     // read only the vectors over the band's nonzero mask columns; elsewhere m = 0 on
@@ -976,7 +997,7 @@ __global__ void __launch_bounds__(kMaxThreads)
 #pragma unroll
         for (int q = 0; q < VEC / 4; ++q) {
             const float4 v = *reinterpret_cast<const float4*>(
-                st + p.off_m + (static_cast<unsigned>(row) * p.W + x0 + 4 * q) * 4u);
+                st + p.off_m + (static_cast<unsigned>(row) * p.Wt + lx + 4 * q) * 4u);
             m2[2 * q] = mk2(v.x, v.y);
             m2[2 * q + 1] = mk2(v.z, v.w);
         }
@@ -1041,7 +1062,9 @@ gs_status launch_kernel(TmaParams& p, int threads, unsigned smem, gs_stream stre
     if (p.B > 65535 || p.ncg > 65535) return GS_ERR_UNSUPPORTED;
     const int gpr = threads / p.RB;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.nbands), static_cast<unsigned>(p.ncg),
+    const long long gx = static_cast<long long>(p.nbands) * p.ncb;
+    if (gx > 0x7fffffffll) return GS_ERR_UNSUPPORTED;
+    cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p.ncg),
                        static_cast<unsigned>(p.B));
     cfg.blockDim = dim3(static_cast<unsigned>(gpr), static_cast<unsigned>(p.RB));
     cfg.dynamicSmemBytes = smem;

@@ -409,13 +409,15 @@ typedef struct gs_step_args {
  *
  * Kernels (all give the same results):
  *   - TMA-pipelined: used when every latent-shaped pointer is 16-byte aligned,
- *     W * element size is a multiple of 16 bytes, W <= 256, every region output
- *     is 16-byte aligned with a 16-byte-multiple row pitch and rounds up to at
- *     most 256 columns, and the inpaint mask is per-sample dense or shared.
- *     Tensor maps are encoded per call (host cost of a few microseconds).
- *     One CTA per tile of (sample, up to 4 channels, a band of rows); the band
- *     height is chosen for about 128 threads per tile, or set with the
- *     environment variable GS_TMA_ROWS (a tuning knob; results do not change).
+ *     W * element size is a multiple of 16 bytes, every region output is 16-byte
+ *     aligned with a 16-byte-multiple row pitch, and the inpaint mask is
+ *     per-sample dense or shared.  Tensor maps are encoded per call (about a
+ *     microsecond of host time; gs_step_prepare does it once).  One CTA per
+ *     tile of (sample, up to 4 channels, a band of rows, whole rows or a block
+ *     of columns: rows wider than 256 columns, or whose 16-byte groups make no
+ *     whole warps, are cut into blocks); the band height is chosen for about
+ *     128 threads per tile, or set with the environment variable GS_TMA_ROWS
+ *     (a tuning knob; results do not change).
  *   - register-streaming with 16-byte vectors: pointers 16-byte aligned and W a
  *     multiple of 16 bytes / element size; one item of 8 (16-bit) or 4 (fp32)
  *     pixels x 2 channels per thread, or as many channels (1, 2 or 4) as the

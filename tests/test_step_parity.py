@@ -53,8 +53,9 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
     span summary of the latent mask (gs_mask_spans) instead of the row summary; with
     poison, also fill uncond and cond with NaN in every 16-byte vector of a blended
     sample's row that lies outside the first-to-last nonzero mask columns of every
-    row that can share a band with it (a band has at most 256 threads' rows), so
-    that no vector the kernel reads is poisoned, whatever tile shape it picks.  unit_skip: samples whose scale is
+    row that can share a band with it (a band of whole rows has at most 256 threads'
+    rows; with column blocks, every row of the frame), so that no vector the kernel
+    reads is poisoned, whatever tile shape it picks.  unit_skip: samples whose scale is
     exactly 1 skip their uncond read; with poison their whole uncond is NaN on the GPU
     side.  lut: a per-step scale table (float32) in place of the workload's.
     poison_ranges: on the GPU side only, fill each region's slab with NaN for the samples
@@ -119,10 +120,12 @@ def run_case(wl: Workload, step_seed: int = 0, *, B=None, C=None, H=None, W=None
             cols = np.arange(Wn)
             lo_r = np.where(nzc.any(1), np.where(nzc, cols, Wn).min(1), Wn)   # per row
             hi_r = np.where(nzc.any(1), np.where(nzc, cols + 1, 0).max(1), 0)
-            # a tile's band has at most 256 threads / (W / vec) rows: rows farther apart
-            # never share a band, so the columns a band containing row y can read lie
-            # between the first and last nonzero column of the rows around y
-            radius = 256 // max(1, Wn // vec) - 1
+            # a tile of whole rows (W <= 256: the library cuts no narrower tiles) has at
+            # most 256 threads / (W / vec) rows: rows farther apart never share a band, so
+            # the columns a band containing row y can read lie between the first and last
+            # nonzero column of the rows around y; wider latents are cut into column
+            # blocks whose bands may be taller, so there the whole frame counts
+            radius = 256 // max(1, Wn // vec) - 1 if Wn <= 256 else Hn
             far = np.zeros((Hn, Wn), bool)
             for yy in range(Hn):
                 lo = lo_r[max(0, yy - radius):yy + radius + 1].min()
@@ -497,7 +500,7 @@ def test_negative_regions_with_sampler_options(model_in, tma):
     assert rep.n == wl.elements
 
 
-def _combo(seed):
+def _combo(seed, widths=None):
     """A random feature combination on a small shape (deterministic in seed)."""
     import random
     rng = random.Random(1000 + seed)
@@ -505,6 +508,8 @@ def _combo(seed):
     B, C = rng.randint(1, 6), rng.randint(1, 6)
     H = rng.randint(1, 40)
     W = rng.choice([8, 16, 24, 40, 64, 128, rng.randint(1, 70)])
+    if widths is not None:
+        W = rng.choice(widths)
     n_regions = rng.randint(0, 4)
     full_cond = n_regions == 0 or rng.random() < 0.5
     negative = tuple(i for i in range(n_regions) if rng.random() < 0.4)
@@ -629,3 +634,34 @@ def test_unit_scale_with_spans_and_samplers(dtype):
                    base.guidance.__class__(cfg=1.0), seed=26)
     rep, got, _, _ = run_case(wl1, unit_skip=True, poison=True, expect_kernel="tma")
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("shape,dtype", [((4, 4, 24, 384), "bf16"), ((2, 4, 16, 1024), "bf16"),
+                                         ((3, 2, 20, 392), "fp16"), ((2, 4, 12, 512), "fp32"),
+                                         ((3, 4, 9, 200), "fp16"), ((64, 16, 8, 384), "bf16")])
+def test_wide_latents_on_the_tma_kernel(shape, dtype):
+    """Latents wider than 256 columns (and rows whose pixel groups make no whole warps)
+    run on the TMA kernel in column blocks: regions wider than 256 columns, region
+    masks, a partial inpaint batch, a denoised output and a ragged last block match the
+    oracle; so do the span summary (poisoned) and the sampler options."""
+    B, C, H, W = shape
+    base = WORKLOADS[4]
+    wl = Workload("wide", B, C, H, W, dtype, base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=3, region_side=(min(H, W) // 2, W - 3),
+                  feather=4, inpaint=True, inpaint_samples=max(1, 2 * B // 3),
+                  pixel_mask_hw=(8 * H, 8 * W), seed=27)
+    rep, *_ = run_case(wl, region_masks=True, want_den=True, expect_kernel="tma")
+    assert rep.n == wl.elements
+    rep, got, *_ = run_case(wl, mask_spans=True, poison=True, expect_kernel="tma")
+    assert np.isfinite(got).all()
+    rep, *_ = run_case(wl, sampler="euler_ancestral", model_in=True, expect_kernel="tma")
+    assert rep.n == wl.elements
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_wide_feature_combinations(seed):
+    """Random option combinations on widths that take column blocks or a padded tile
+    (264, 328, 392, 520 and 72, 200 columns), on the TMA kernel (or the scalar one
+    with an unaligned base)."""
+    wl, kw = _combo(200 + seed, widths=[72, 200, 264, 328, 392, 520])
+    run_case(wl, **kw)
