@@ -401,8 +401,10 @@ __global__ void __launch_bounds__(kMaxThreads)
     unsigned long long* full = reinterpret_cast<unsigned long long*>(smem);
     unsigned char* st = smem + 128;
 
-    const int band = blockIdx.x / p.ncb;
-    const int xb0 = (blockIdx.x - band * p.ncb) * p.Wt;   // the tile's first frame column
+    // (one column block: whole rows, the common case, without the division)
+    const bool blocked = p.ncb > 1;
+    const int band = blocked ? static_cast<int>(blockIdx.x) / p.ncb : static_cast<int>(blockIdx.x);
+    const int xb0 = blocked ? (static_cast<int>(blockIdx.x) - band * p.ncb) * p.Wt : 0;   // first frame column
     const int cgi = blockIdx.y;
     const int b = blockIdx.z;
     const int nthreads = blockDim.x * blockDim.y;
@@ -493,15 +495,28 @@ __global__ void __launch_bounds__(kMaxThreads)
     auto issue_regions = [&](int sidx) {
         if constexpr (REG) {
             // only the fields the issue needs, read straight from the parameters
+            if (!blocked && sidx < 0) {
+                // whole rows, every region in range: the common case
+                for (int r = 0; r < p.n_regions; ++r) {
+                    const int ry0 = p.reg[r].y0, rh = p.reg[r].h;
+                    if (y_band >= ry0 + rh || y_band + p.RB <= ry0) continue;
+                    mbar_add_tx(bar, p.reg[r].tile_bytes);
+                    tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], 0, y_band - ry0, z, bar);
+                }
+                return;
+            }
             for (int r = 0; r < p.n_regions; ++r) {
                 const int ry0 = p.reg[r].y0, rh = p.reg[r].h;
                 if (y_band >= ry0 + rh || y_band + p.RB <= ry0) continue;
                 if (sidx >= 0 && (sidx < p.reg[r].step_lo || sidx >= p.reg[r].step_hi)) continue;
-                const int rx0 = p.reg[r].x0;
-                if (rx0 >= xb0 + p.Wt || rx0 + p.reg[r].w <= xb0) continue;   // column block
+                int bx = 0;
+                if (blocked) {
+                    const int rx0 = p.reg[r].x0;
+                    if (rx0 >= xb0 + p.Wt || rx0 + p.reg[r].w <= xb0) continue;   // column block
+                    bx = region_box_x(rx0, xb0, VEC);
+                }
                 mbar_add_tx(bar, p.reg[r].tile_bytes);
-                tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], region_box_x(rx0, xb0, VEC),
-                            y_band - ry0, z, bar);
+                tma_load_3d(s0 + p.reg[r].smem_off, &p.tm_r[r], bx, y_band - ry0, z, bar);
             }
         }
     };
