@@ -81,6 +81,15 @@ NOMINAL_HBM_GBS = 7900.0
 # line reports traffic null.  Keys: workload name, then "+mask_rows" or "+mask_spans"
 # with a mask summary.
 TRAFFIC = {
+    # profiles/guided_step_tma__dram_traffic.md
+    "bcg_bf16_b16": (6304512, 0, "746fb3398e5a694f"),
+    "area_fp16_b8": (2961664, 0, "746fb3398e5a694f"),
+    "inpaint_bcg_bf16_b32": (69226240, 624128, "746fb3398e5a694f"),
+    "sweep_bf16_b64": (100668160, 5376000, "746fb3398e5a694f"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51130624, 30720, "746fb3398e5a694f"),
+    "sweep_bf16_b64+mask_rows": (88808704, 3495680, "746fb3398e5a694f"),
+    "inpaint_bcg_bf16_b32+mask_spans": (48050176, 5376, "746fb3398e5a694f"),
+    "sweep_bf16_b64+mask_spans": (87188480, 3300096, "746fb3398e5a694f"),
 }
 
 
@@ -480,17 +489,21 @@ class Timed:
         return self.graphs[n]
 
     def time(self, K, W, stream, dev, pg, soak_s=0.0, clocks=None):
-        """Milliseconds for exactly K steps (graph replays of R launches, then a graph of
-        the remainder), after W untimed warm-up launches and an optional soak."""
+        """Milliseconds for exactly K steps, after W untimed warm-up launches and an
+        optional soak.  The steps are replays of a graph of L launches (the rotating sets
+        in order, L a multiple of R and at least 128, so that the boundaries between
+        graph launches, where consecutive steps cannot overlap, are rare), then a graph
+        of the remainder; with K < L one graph of K launches."""
         import torch
 
         from bucketized_guidance_step_gb300 import gs
+        L = self.R * max(1, math.ceil(128 / self.R))
         with torch.cuda.stream(stream):
             for k in range(W):
                 gs.launch_step(self.prepared[k % self.R][0])
             torch.cuda.synchronize(dev)
-            g_full = self.graph(self.R, stream)
-            rem = K % self.R
+            g_full = self.graph(L, stream)
+            rem = K % L
             g_rem = self.graph(rem, stream) if rem else None
             g_full.replay()
             if g_rem is not None:
@@ -509,7 +522,7 @@ class Timed:
             torch.cuda.synchronize(dev)
             block_stream(stream)
             start.record(stream)
-            for _ in range(K // self.R):
+            for _ in range(K // L):
                 g_full.replay()
             if g_rem is not None:
                 g_rem.replay()
