@@ -82,14 +82,14 @@ NOMINAL_HBM_GBS = 7900.0
 # with a mask summary.
 TRAFFIC = {
     # profiles/guided_step_tma__dram_traffic.md
-    "bcg_bf16_b16": (6304512, 0, "746fb3398e5a694f"),
-    "area_fp16_b8": (2961664, 0, "746fb3398e5a694f"),
-    "inpaint_bcg_bf16_b32": (69226240, 624128, "746fb3398e5a694f"),
-    "sweep_bf16_b64": (100668160, 5376000, "746fb3398e5a694f"),
-    "inpaint_bcg_bf16_b32+mask_rows": (51130624, 30720, "746fb3398e5a694f"),
-    "sweep_bf16_b64+mask_rows": (88808704, 3495680, "746fb3398e5a694f"),
-    "inpaint_bcg_bf16_b32+mask_spans": (48050176, 5376, "746fb3398e5a694f"),
-    "sweep_bf16_b64+mask_spans": (87188480, 3300096, "746fb3398e5a694f"),
+    "bcg_bf16_b16": (6304512, 0, "192b8e7c41f5d7c6"),
+    "area_fp16_b8": (2961664, 0, "192b8e7c41f5d7c6"),
+    "inpaint_bcg_bf16_b32": (69226240, 624128, "192b8e7c41f5d7c6"),
+    "sweep_bf16_b64": (100668160, 5376000, "192b8e7c41f5d7c6"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51130624, 30720, "192b8e7c41f5d7c6"),
+    "sweep_bf16_b64+mask_rows": (88808704, 3495680, "192b8e7c41f5d7c6"),
+    "inpaint_bcg_bf16_b32+mask_spans": (48050176, 5376, "192b8e7c41f5d7c6"),
+    "sweep_bf16_b64+mask_spans": (87188480, 3300096, "192b8e7c41f5d7c6"),
 }
 
 
@@ -203,13 +203,39 @@ def workload_for(args):
     return dataclasses.replace(wl, name=name)
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and with whitespace runs collapsed, so that a
+    change to comments alone leaves the hash (and the counters taken on it) valid."""
+    import re
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":                       # string or char literal
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_source_hash() -> str:
-    """SHA-256 prefix over the kernel sources and the C ABI header."""
+    """SHA-256 prefix over the kernel sources and the C ABI header, comments left out."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bucketized_guidance_step_gb300", "csrc")
     for name in sorted(os.listdir(csrc)) + ["../../include/gs.h"]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

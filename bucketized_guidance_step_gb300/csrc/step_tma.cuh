@@ -650,7 +650,8 @@ __global__ void __launch_bounds__(kMaxThreads)
             tp.xv = xv;
             tp.xa = xa;
             if constexpr (kSplit) {
-                // group A is complete: with deferral this thread is its only feeder
+                // this thread's part of group A is in (with a mask summary it is A's only
+                // feeder; otherwise thread 0 arrives for its cond and region boxes)
                 if (p.test_wait_timeout) mbar_add_tx(bar, 16u);   // bytes nothing will deliver
                 mbar_arrive(bar);
             }

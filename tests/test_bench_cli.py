@@ -99,3 +99,12 @@ def test_binding_rejects_mismatched_sampler_tensors():
         gs.make_step_args(x, sigmas=sig, cond=x, model_in_out=torch.zeros(1, 3, 4, 8))
     with pytest.raises(ValueError, match="orig_noise must have the shape"):
         gs.make_step_args(x, sigmas=sig, cond=x, orig_noise=torch.zeros(2, 3, 5, 8))
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The traffic counters stay valid across comment edits, not across code edits."""
+    a = bench._code_only('int f(int x) {  // doubles\n  /* the\n  value */ return 2 * x; }\n')
+    b = bench._code_only('int f(int x) { return 2 * x; }  // twice x')
+    c = bench._code_only('int f(int x) { return 3 * x; }')
+    assert a == b != c
+    assert bench._code_only('const char* s = "// kept"; // dropped') == 'const char* s = "// kept";'

@@ -532,6 +532,13 @@ def _combo(seed, widths=None):
               mask_rows=inpaint and rng.random() < 0.5,
               uncond_none=bool(negative) and rng.random() < 0.3,
               offset=1 if rng.random() < 0.15 else 0, step=rng.randint(0, 49))
+    # (drawn after the options above, so that those keep their earlier values)
+    if inpaint and not kw["mask_rows"] and rng.random() < 0.4:
+        kw["mask_spans"] = True
+    if not kw["uncond_none"] and rng.random() < 0.3:
+        kw.update(unit_skip=True, lut=_unit_lut(wl.schedule.steps))
+    kw["poison"] = (kw.get("mask_rows") or kw.get("mask_spans") or kw.get("unit_skip")) \
+        and not negative and kw["offset"] == 0 and rng.random() < 0.5
     return wl, kw
 
 
@@ -546,6 +553,9 @@ def test_feature_combinations(seed, tma):
     feathers, timestep ranges and negative regions, inpaint with partial presence and the
     row summary, both samplers, the model input, unaligned bases) against the oracle."""
     wl, kw = _combo(seed)
+    es = 4 if wl.dtype == "fp32" else 2
+    if not tma or (wl.W * es) % 16 != 0:
+        kw["poison"] = False            # only the TMA-fed kernel skips the reads
     run_case(wl, tma=tma, **kw)
 
 
