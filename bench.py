@@ -619,7 +619,8 @@ def run_api(timed, stream, dev, n: int):
     checks_and_encode_us: a trivial call into the library and gs_step_kernel_kind
     (the same checks and encoding, no launch), the parts of the host cost before the
     launch itself; prepared: the same two numbers for gs_step_launch on plans made
-    once by gs_step_prepare (no checks or encoding per call)."""
+    once by gs_step_prepare (no checks or encoding per call); prepared_bound: the same
+    through gs.StepLauncher (plan, stream and function bound once)."""
     import torch
 
     from bucketized_guidance_step_gb300 import gs
@@ -652,6 +653,8 @@ def run_api(timed, stream, dev, n: int):
 
     host_us, dev_us = measure(lambda k: gs.launch_step(args[k % R], stream))
     phost_us, pdev_us = measure(lambda k: gs.launch_prepared(plans[k % R], 0, stream))
+    bound = [gs.StepLauncher(pl, stream) for pl in plans]
+    bhost_us, bdev_us = measure(lambda k: bound[k % R](0))
     t2 = time.perf_counter()
     for _ in range(n):
         lib.gs_abi_version()
@@ -664,6 +667,8 @@ def run_api(timed, stream, dev, n: int):
             "device_us_per_step": round(dev_us, 3),
             "prepared": {"host_us_per_call": round(phost_us, 3),
                          "device_us_per_step": round(pdev_us, 3)},
+            "prepared_bound": {"host_us_per_call": round(bhost_us, 3),
+                               "device_us_per_step": round(bdev_us, 3)},
             "ctypes_call_us": round((t3 - t2) / n * 1e6, 3),
             "checks_and_encode_us": round((t4 - t3) / n * 1e6, 3),
             "mode": "one gs_guided_step call per step from Python (ctypes), no CUDA graph, "
@@ -801,7 +806,8 @@ def run_ours(args, world, rank, local):
                          "input_sets": t2.R}
             if api2 is not None:
                 per[name]["api"] = {k: api2[k] for k in ("host_us_per_call",
-                                                         "device_us_per_step", "prepared")}
+                                                         "device_us_per_step", "prepared",
+                                                         "prepared_bound")}
             launches += Kc
             del t2
             torch.cuda.empty_cache()

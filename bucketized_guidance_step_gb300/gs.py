@@ -507,6 +507,23 @@ def launch_prepared(plan: StepPlan, step: int = 0, stream=None) -> None:
                                                    _stream_ptr(stream)))
 
 
+class StepLauncher:
+    """A prepared step bound to one stream: ``launcher(step)`` launches one step
+    (gs_step_launch) with the least Python work per call -- the plan, the stream handle
+    and the library function are looked up once, here."""
+
+    def __init__(self, plan: StepPlan, stream=None):
+        self._fn = load().gs_step_launch
+        self._plan = plan                       # keeps the plan alive
+        self._ref = ctypes.byref(plan)
+        self._stream = ctypes.c_void_p(_stream_ptr(stream))
+
+    def __call__(self, step: int = 0) -> None:
+        status = self._fn(self._ref, step, self._stream)
+        if status != GS_OK:
+            raise GSError("gs_step_launch", status)
+
+
 def kernel_kind(args: StepArgs) -> str:
     """gs_step_kernel_kind: "tma", "vector" or "scalar" for prepared arguments."""
     k = ctypes.c_int32(-1)

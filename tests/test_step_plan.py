@@ -82,6 +82,10 @@ def test_plan_matches_guided_step(case):
     torch.cuda.synchronize()
     assert torch.isfinite(out_a.float()).all()
     assert _same_bits(out_a, out_b)
+    out_b.fill_(float("nan"))                   # the same plan through a bound launcher
+    gs.StepLauncher(plan)(step)
+    torch.cuda.synchronize()
+    assert _same_bits(out_a, out_b)
 
 
 @pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
