@@ -213,6 +213,18 @@ __device__ __forceinline__ void tma_load_3d(unsigned dst, const CUtensorMap* map
         : "memory");
 }
 
+// Ask L2 to fetch a box's lines from DRAM (no shared memory, no barrier, no value
+// returned to the thread): a cache hint only.  L2 is the point of coherence for every
+// SM and bulk copies do not go through L1, so a line fetched early is updated in L2 by
+// any later write and the loads after the grid dependency wait still see the previous
+// kernel's results.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<unsigned long long>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<unsigned long long>(map))
                  : "memory");
@@ -454,6 +466,34 @@ __global__ void __launch_bounds__(kMaxThreads)
         if constexpr (REG) {
             for (int r = 0; r < p.n_regions; ++r) prefetch_map(&p.tm_r[r]);
         }
+        // x and the prediction boxes the tile reads whatever the inputs hold are
+        // requested into L2 before the grid dependency wait: while the previous kernel
+        // drains its last CTAs the step's first loads are already on their way from
+        // DRAM (back-to-back steps, us: sweep 23.91 -> 22.91, inpaint 14.25 -> 13.47,
+        // bcg 2.86 -> 2.43, area 3.68 -> 3.63).  Boxes chosen by a data value (the
+        // sample's inpaint flag, the mask summary, the scale, the step index against
+        // region ranges) are not.  Requesting the original and mask boxes as well (when
+        // every sample is blended) made the inpaint step slower (13.71 against 13.47 us),
+        // and so did x alone (sweep 23.60, bcg 2.65) or the prediction alone (bcg 2.51).
+        tma_prefetch_3d(&p.tm_x, xb0, y_band, z);
+        if (anc) tma_prefetch_3d(&p.tm_n, xb0, y_band, z);
+        if (!DEFER && has_u) tma_prefetch_3d(&p.tm_u, xb0, y_band, z);
+        if (!summary && has_c) tma_prefetch_3d(&p.tm_c, xb0, y_band, z);
+        if constexpr (REG) {
+            if (!late_regions) {
+                for (int r = 0; r < p.n_regions; ++r) {
+                    const int ry0 = p.reg[r].y0;
+                    if (y_band >= ry0 + p.reg[r].h || y_band + p.RB <= ry0) continue;
+                    int bx = 0;
+                    if (blocked) {
+                        const int rx0 = p.reg[r].x0;
+                        if (rx0 >= xb0 + p.Wt || rx0 + p.reg[r].w <= xb0) continue;
+                        bx = region_box_x(rx0, xb0, VEC);
+                    }
+                    tma_prefetch_3d(&p.tm_r[r], bx, y_band - ry0, z);
+                }
+            }
+        }
         if constexpr (kSplit) {
             // group A: thread 0 feeds it, or the parameter thread (DEFER); with only
             // the uncond skip at scale 1 deferred, both do
@@ -466,9 +506,10 @@ __global__ void __launch_bounds__(kMaxThreads)
         tp.abandon = 0;
     }
     __syncthreads();
-    // Everything above touches only kernel parameters; with programmatic
-    // dependent launch it overlaps the tail of the previous kernel.  Inputs
-    // (which a preceding kernel may produce) are read only after this wait.
+    // Everything above touches only kernel parameters (and asks L2 for lines, which
+    // reads no value); with programmatic dependent launch it overlaps the tail of the
+    // previous kernel.  Inputs (which a preceding kernel may produce) are read only
+    // after this wait.
     grid_dependency_wait();
     grid_dependents_launch();
 

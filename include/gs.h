@@ -272,7 +272,10 @@ enum { GS_SAMPLER_EULER = 0, GS_SAMPLER_EULER_ANCESTRAL = 1 };
 /* launch_flags */
 #define GS_LAUNCH_PDL    1u  /* launch with programmatic dependent launch: the kernel
                                 may be scheduled before the previous kernel in the
-                                stream ends; it waits for it before any memory access */
+                                stream ends; it waits for it before it reads or writes
+                                any argument's memory (the TMA kernel asks L2 for the
+                                lines of its input boxes before the wait, a cache hint
+                                that reads no value)                                  */
 #define GS_LAUNCH_NO_TMA 2u  /* use the register-streaming kernel even where the
                                 TMA-pipelined one applies (same results)            */
 #define GS_LAUNCH_TEST_WAIT_TIMEOUT 4u
