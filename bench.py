@@ -82,14 +82,14 @@ NOMINAL_HBM_GBS = 7900.0
 # with a mask summary.
 TRAFFIC = {
     # profiles/guided_step_tma__dram_traffic.md
-    "bcg_bf16_b16": (6304512, 0, "192b8e7c41f5d7c6"),
-    "area_fp16_b8": (2961664, 0, "192b8e7c41f5d7c6"),
-    "inpaint_bcg_bf16_b32": (69226240, 624128, "192b8e7c41f5d7c6"),
-    "sweep_bf16_b64": (100668160, 5376000, "192b8e7c41f5d7c6"),
-    "inpaint_bcg_bf16_b32+mask_rows": (51130624, 30720, "192b8e7c41f5d7c6"),
-    "sweep_bf16_b64+mask_rows": (88808704, 3495680, "192b8e7c41f5d7c6"),
-    "inpaint_bcg_bf16_b32+mask_spans": (48050176, 5376, "192b8e7c41f5d7c6"),
-    "sweep_bf16_b64+mask_spans": (87188480, 3300096, "192b8e7c41f5d7c6"),
+    "bcg_bf16_b16": (6305024, 0, "0fa28f5a76adebd9"),
+    "area_fp16_b8": (2962432, 0, "0fa28f5a76adebd9"),
+    "inpaint_bcg_bf16_b32": (69226496, 539392, "0fa28f5a76adebd9"),
+    "sweep_bf16_b64": (100668160, 5795840, "0fa28f5a76adebd9"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51130880, 25344, "0fa28f5a76adebd9"),
+    "sweep_bf16_b64+mask_rows": (88810752, 3629056, "0fa28f5a76adebd9"),
+    "inpaint_bcg_bf16_b32+mask_spans": (48050176, 13568, "0fa28f5a76adebd9"),
+    "sweep_bf16_b64+mask_spans": (87189248, 3288832, "0fa28f5a76adebd9"),
 }
 
 
