@@ -82,14 +82,14 @@ NOMINAL_HBM_GBS = 7900.0
 # with a mask summary.
 TRAFFIC = {
     # profiles/guided_step_tma__dram_traffic.md
-    "bcg_bf16_b16": (6305024, 0, "0fa28f5a76adebd9"),
-    "area_fp16_b8": (2962432, 0, "0fa28f5a76adebd9"),
-    "inpaint_bcg_bf16_b32": (69226496, 539392, "0fa28f5a76adebd9"),
-    "sweep_bf16_b64": (100668160, 5795840, "0fa28f5a76adebd9"),
-    "inpaint_bcg_bf16_b32+mask_rows": (51130880, 25344, "0fa28f5a76adebd9"),
-    "sweep_bf16_b64+mask_rows": (88810752, 3629056, "0fa28f5a76adebd9"),
-    "inpaint_bcg_bf16_b32+mask_spans": (48050176, 13568, "0fa28f5a76adebd9"),
-    "sweep_bf16_b64+mask_spans": (87189248, 3288832, "0fa28f5a76adebd9"),
+    "bcg_bf16_b16": (6307328, 0, "39636d136df89e4b"),
+    "area_fp16_b8": (2962944, 0, "39636d136df89e4b"),
+    "inpaint_bcg_bf16_b32": (69226496, 551936, "39636d136df89e4b"),
+    "sweep_bf16_b64": (100671744, 5245184, "39636d136df89e4b"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51130880, 19200, "39636d136df89e4b"),
+    "sweep_bf16_b64+mask_rows": (88809984, 3234304, "39636d136df89e4b"),
+    "inpaint_bcg_bf16_b32+mask_spans": (48050432, 7936, "39636d136df89e4b"),
+    "sweep_bf16_b64+mask_spans": (87188224, 3302144, "39636d136df89e4b"),
 }
 
 

@@ -130,18 +130,34 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
         if (wbox > 256 || wbox > R.pitch) return false;
     }
 
-    // Tile shape.  Measured on GB300 (rotating L2-cold inputs, back-to-back steps):
-    //   small steps (under ~2^18 pixel-group x channel units, a few MB) are
-    //     latency-bound: 1 channel x ~128 threads per tile, the most CTAs;
-    //   large steps without regions: 2 channels x ~64 threads per tile (short
-    //     CTA lifetimes keep the tail of the step short);
-    //   large steps with regions: 4 channels x ~128 threads per tile (the
-    //     per-tile region set-up is amortised over more work); with the next
-    //     model input (the fixed-noise box, and with the ancestral step its noise
-    //     box too) 2 channels, since the 4-channel tile's shared memory leaves
-    //     only 3 CTAs per SM.  Negative regions keep 4 channels although the
-    //     second accumulator takes that tile to 128 registers a thread (4 CTAs
-    //     per SM): 2 channels measured 30 % slower on the sweep shape.
+    // Tile shape.  Measured on GB300 (rotating L2-cold inputs, back-to-back steps with
+    // the early L2 requests), by size in pixel-group x channel units:
+    //   steps with regions, from 2^19 units: 4 channels x ~128 threads per tile (the
+    //     per-tile region set-up is amortised over more work); with the next model
+    //     input (the fixed-noise box, and with the ancestral step its noise box too) 2
+    //     channels, since the 4-channel tile's shared memory leaves only 3 CTAs per
+    //     SM.  Negative regions keep 4 channels although the second accumulator takes
+    //     that tile to 128 registers a thread (4 CTAs per SM): 2 channels measured 36 %
+    //     slower on the sweep shape.  Smaller steps (a wave or two of CTAs) take less
+    //     work a tile as they shrink: 2 channels x ~256 threads from 2^17 units (sweep
+    //     shape B = 8, us: 2x256 5.14, 4x128 5.39; area shape B = 16: 4.06 against
+    //     1x256 4.54), except with negative regions, the sampler options or a mask
+    //     summary, which keep the large steps' tile there (sweep shape B = 8: 4.95,
+    //     7.75 and 5.86 us against 6.95, 7.97 and 6.24 with 2x256), and below 2^17,
+    //     with few channels (area shape, 4 channels:
+    //     the per-thread region loop is the cost), 1 channel x ~256 threads from 2^15
+    //     (B = 8: 3.43 against 1x128 3.65, 2x128 3.59), with many (sweep shape, 16
+    //     channels) 2 channels x ~128 threads from 2^16 (B = 4: 3.48 against 1x128
+    //     4.50, 1x256 4.28); negative regions 2 x ~256 from 2^15 (area shape, two of
+    //     four negative: 3.62 against 1x128 4.00, 1x256 4.30); else 1 x ~128.
+    //   steps without regions take more channels per tile as they grow (bcg shape,
+    //     4 x 128 x 128 bf16, us: B = 8 1x128 1.85 / 2x128 1.81; B = 16 2.43 / 2.30;
+    //     B = 32 2x64 4.31 / 4x128 3.39; B = 128 4x128 10.95 / 4x64 10.58): 1 channel
+    //     x ~128 threads below 2^16 units, 2 x ~128 below 2^18, 4 x ~128 below 2^20,
+    //     4 x ~64 above; with inpaint or the ancestral noise (four or more boxes a
+    //     tile) 2 x ~128 below 2^18 and 2 x ~64 above (inpaint shape, 16 x 128 x 128
+    //     bf16, B = 8: 2x64 4.25 against 4x128 5.80, 1x128 5.16; ancestral bcg shape,
+    //     B = 64: 2x64 7.97 against 4x128 8.22).
     // GS_TMA_CHANNELS=1|2|4 and GS_TMA_ROWS override (tuning knobs; results do
     // not depend on them).
     const int gpr = Wt / vec;                            // threads per tile row
@@ -150,11 +166,22 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
     const long long units = static_cast<long long>(B) * H * (W / vec) * C;
     const bool large = units >= (1ll << 18);
     int cg = 1, target_threads = 128;
-    if (large && sp.n_regions > 0) {
-        cg = mi ? 2 : 4;
-    } else if (large) {
-        cg = 2;
-        target_threads = 64;
+    if (sp.n_regions > 0) {
+        const bool summary = inp && !neg && (sp.mask_rows != nullptr || sp.mask_spans != nullptr);
+        if (units >= (1ll << 17) && (units >= (1ll << 19) || neg || nz || summary)) {
+            cg = mi ? 2 : 4;
+        } else if (units >= (1ll << 17) || (neg && units >= (1ll << 15))) {
+            cg = 2;
+            target_threads = 256;
+        } else if (C < 8 && units >= (1ll << 15)) {
+            target_threads = 256;
+        } else if (C >= 8 && units >= (1ll << 16)) {
+            cg = 2;
+        }
+    } else if (units >= (1ll << 16)) {
+        const bool more_boxes = inp || anc;
+        cg = more_boxes || !large ? 2 : 4;
+        if (units >= (more_boxes ? (1ll << 18) : (1ll << 20))) target_threads = 64;
     }
     while (cg > 1 && C % cg != 0) cg /= 2;
     static const int cg_override = [] {
@@ -170,6 +197,27 @@ bool build_tma(const StepParams& sp, int dtype, unsigned flags, TmaLaunch* L) {
     }();
     if (rows_override > 0 && rows_override % rb0 == 0 && rows_override * gpr <= kMaxThreads)
         rb = rows_override;
+    // The stage (the layout below) must fit the shared memory a CTA may use: a tile with
+    // many wide regions gives up rows, then channels, before the step leaves TMA.
+    auto stage_bytes = [&](int c, int r) {
+        const unsigned pl = round128(static_cast<unsigned>(c) * r * Wt * es);
+        unsigned n = pl * (1u + (anc ? 1u : 0u) + (sp.u != nullptr ? 1u : 0u) +
+                           (sp.c != nullptr ? 1u : 0u) + (inp ? 1u : 0u) + (inp && mi ? 1u : 0u));
+        if (inp) n += round128(static_cast<unsigned>(r) * Wt * 4u);
+        for (int i = 0; i < sp.n_regions; ++i) {
+            const DevRegion& R = sp.reg[i];
+            const int col0 = R.x0 - R.x0 % vec;
+            const int ncol = (R.x0 + R.w - col0 + vec - 1) / vec * vec;
+            n += round128(static_cast<unsigned>(c) * r * region_box(R) * es) +
+                 round128(static_cast<unsigned>(std::min(ncol, Wt)) * 4u);
+        }
+        return n + round128(static_cast<unsigned>(sp.n_regions) * r * 4u);
+    };
+    while (stage_bytes(cg, rb) > kMaxTileBytes) {
+        if (rb > rb0) rb = std::max(rb0, rb / 2 / rb0 * rb0);
+        else if (cg > 1) cg /= 2;
+        else break;
+    }
     const int threads = rb * gpr;
 
     std::memset(L, 0, sizeof(*L));

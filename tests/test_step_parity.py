@@ -319,6 +319,20 @@ def test_region_pitch_and_masks(pitch_align, tma):
     run_case(wl, region_masks=True, pitch_align=pitch_align, step=5, tma=tma, expect_kernel=want)
 
 
+@pytest.mark.parametrize("B", [4, 16], ids=["small_step", "large_step"])
+def test_many_wide_regions_stay_on_tma(B):
+    """Sixteen regions 64 to 256 columns wide on a 256-column latent: at the large step's
+    default tile (4 channels x 8 rows) their boxes and tables would take ~250 KB of
+    shared memory, more than a CTA may use; the host gives the tile fewer rows instead
+    of leaving the TMA kernel."""
+    base = WORKLOADS[4]
+    wl = Workload("wide_regions", B, 16, 64, 256, "bf16", base.schedule, base.guidance,
+                  full_frame_cond=True, n_regions=16, region_side=(64, 256), inpaint=True,
+                  inpaint_samples=B // 2, seed=16)
+    rep, *_ = run_case(wl, expect_kernel="tma")
+    assert rep.n == wl.elements
+
+
 @pytest.mark.parametrize("tma", [True, False], ids=["tma", "registers"])
 def test_every_scale_one_without_uncond(tma):
     base = WORKLOADS[1]
