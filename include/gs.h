@@ -418,9 +418,13 @@ typedef struct gs_step_args {
  *     microsecond of host time; gs_step_prepare does it once).  One CTA per
  *     tile of (sample, up to 4 channels, a band of rows, whole rows or a block
  *     of columns: rows wider than 256 columns, or whose 16-byte groups make no
- *     whole warps, are cut into blocks); the band height is chosen for about
- *     128 threads per tile, or set with the environment variable GS_TMA_ROWS
- *     (a tuning knob; results do not change).
+ *     whole warps, are cut into blocks); the channels and band height of a
+ *     tile follow the step's size and options (64 to 256 threads a tile; a tile
+ *     whose stage would not fit a CTA's shared memory takes fewer rows, then
+ *     fewer channels), or are set with the environment variables
+ *     GS_TMA_CHANNELS and GS_TMA_ROWS (tuning knobs; results do not change).
+ *     Each tile asks L2 for the lines of its x and prediction boxes before it
+ *     waits for the previous kernel (see GS_LAUNCH_PDL).
  *   - register-streaming with 16-byte vectors: pointers 16-byte aligned and W a
  *     multiple of 16 bytes / element size; one item of 8 (16-bit) or 4 (fp32)
  *     pixels x 2 channels per thread, or as many channels (1, 2 or 4) as the
