@@ -82,14 +82,14 @@ NOMINAL_HBM_GBS = 7900.0
 # with a mask summary.
 TRAFFIC = {
     # profiles/guided_step_tma__dram_traffic.md
-    "bcg_bf16_b16": (6307328, 0, "39636d136df89e4b"),
-    "area_fp16_b8": (2962944, 0, "39636d136df89e4b"),
-    "inpaint_bcg_bf16_b32": (69226496, 551936, "39636d136df89e4b"),
-    "sweep_bf16_b64": (100671744, 5245184, "39636d136df89e4b"),
-    "inpaint_bcg_bf16_b32+mask_rows": (51130880, 19200, "39636d136df89e4b"),
-    "sweep_bf16_b64+mask_rows": (88809984, 3234304, "39636d136df89e4b"),
-    "inpaint_bcg_bf16_b32+mask_spans": (48050432, 7936, "39636d136df89e4b"),
-    "sweep_bf16_b64+mask_spans": (87188224, 3302144, "39636d136df89e4b"),
+    "bcg_bf16_b16": (6307328, 0, "cb974a9ed10aedc5"),
+    "area_fp16_b8": (2963200, 0, "cb974a9ed10aedc5"),
+    "inpaint_bcg_bf16_b32": (69227264, 534528, "cb974a9ed10aedc5"),
+    "sweep_bf16_b64": (100667136, 5064192, "cb974a9ed10aedc5"),
+    "inpaint_bcg_bf16_b32+mask_rows": (51131136, 31488, "cb974a9ed10aedc5"),
+    "sweep_bf16_b64+mask_rows": (88816640, 3431424, "cb974a9ed10aedc5"),
+    "inpaint_bcg_bf16_b32+mask_spans": (48051456, 11520, "cb974a9ed10aedc5"),
+    "sweep_bf16_b64+mask_spans": (87192832, 3331072, "cb974a9ed10aedc5"),
 }
 
 

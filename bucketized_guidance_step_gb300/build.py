@@ -44,7 +44,7 @@ def _sources():
 
 def _inputs():
     files = _sources() + [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
-    files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh", ".inc"))]
     files.append(os.path.abspath(__file__))
     return files
 
