@@ -77,3 +77,69 @@ def test_required_bytes_at_line_granularity():
     plane = 2 * 4 * 32 * 2
     assert required_bytes(1, 2, 4, 32, "bf16", mask_nz=m, granule=128) == \
         step_bytes(1, 2, 4, 32, "bf16", inpaint_samples=1) - 2 * (plane - 2 * 128)
+
+
+def _small_case(seed: int):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    B, C, H, W = 3, 2, 8, 32
+    regions = [(1, 3, 5, 11, 16), (0, 0, 8, 32, 32)]        # (y0, x0, h, w, pitch)
+    return rng, B, C, H, W, regions
+
+
+def test_required_bytes_limits_all_ones_and_all_zeros():
+    """A mask that is nonzero everywhere leaves nothing to skip; one that is zero
+    everywhere on the blended samples leaves none of their prediction required."""
+    import numpy as np
+
+    from bucketized_guidance_step_gb300.accounting import required_bytes
+    _, B, C, H, W, regions = _small_case(0)
+    present = np.array([True, False, True])
+    full = step_bytes(B, C, H, W, "bf16", regions=[(h, w) for _, _, h, w, _ in regions],
+                      inpaint_samples=int(present.sum()))
+    for granule in (32, 128):
+        ones = np.ones((B, H, W), bool)
+        assert required_bytes(B, C, H, W, "bf16", regions=regions, mask_nz=ones,
+                              present=present, granule=granule) == full
+        zeros = np.zeros((B, H, W), bool)
+        pred = 2 * C * H * W * 2 + sum(C * h * w * 2 for _, _, h, w, _ in regions)
+        assert required_bytes(B, C, H, W, "bf16", regions=regions, mask_nz=zeros,
+                              present=present, granule=granule) == full - 2 * pred
+
+
+def test_required_bytes_bounds_and_monotonicity():
+    """Between the element-exact count and step_bytes; a coarser granule requires at
+    least as much; more nonzero pixels never require less."""
+    import numpy as np
+
+    from bucketized_guidance_step_gb300.accounting import required_bytes
+    rng, B, C, H, W, regions = _small_case(1)
+    present = np.ones(B, bool)
+    full = step_bytes(B, C, H, W, "bf16", regions=[(h, w) for _, _, h, w, _ in regions],
+                      inpaint_samples=B)
+    pred = 2 * C * H * W * 2 + sum(C * h * w * 2 for _, _, h, w, _ in regions)
+    for trial in range(20):
+        m = rng.random((B, H, W)) < rng.uniform(0.0, 0.3)
+        # element-exact: only the prediction elements at nonzero pixels
+        exact = full - B * pred + sum(
+            int(m[b].sum()) * C * 2 * 2 +
+            sum(int(m[b, y0:y0 + h, x0:x0 + w].sum()) * C * 2 for y0, x0, h, w, _ in regions)
+            for b in range(B))
+        sec = required_bytes(B, C, H, W, "bf16", regions=regions, mask_nz=m, present=present)
+        line = required_bytes(B, C, H, W, "bf16", regions=regions, mask_nz=m, present=present,
+                              granule=128)
+        assert exact <= sec <= line <= full
+        more = m | (rng.random((B, H, W)) < 0.05)
+        assert required_bytes(B, C, H, W, "bf16", regions=regions, mask_nz=more,
+                              present=present) >= sec
+
+
+def test_required_bytes_scale_one_drops_exactly_the_uncond():
+    import numpy as np
+
+    from bucketized_guidance_step_gb300.accounting import required_bytes
+    _, B, C, H, W, regions = _small_case(2)
+    unit = np.array([True, False, True])
+    full = step_bytes(B, C, H, W, "fp16", regions=[(h, w) for _, _, h, w, _ in regions])
+    got = required_bytes(B, C, H, W, "fp16", regions=regions, unit_scale=unit)
+    assert got == full - int(unit.sum()) * C * H * W * 2
