@@ -473,8 +473,9 @@ __global__ void __launch_bounds__(kMaxThreads)
         // bcg 2.86 -> 2.43, area 3.68 -> 3.63).  Boxes chosen by a data value (the
         // sample's inpaint flag, the mask summary, the scale, the step index against
         // region ranges) are not.  Requesting the original and mask boxes as well (when
-        // every sample is blended) made the inpaint step slower (13.71 against 13.47 us),
-        // and so did x alone (sweep 23.60, bcg 2.65) or the prediction alone (bcg 2.51).
+        // every sample is blended) made the inpaint step slower (13.71 against 13.47 us);
+        // x alone (sweep 23.60, bcg 2.65) or the prediction boxes alone (bcg 2.51) gained
+        // less than both together.
         tma_prefetch_3d(&p.tm_x, xb0, y_band, z);
         if (anc) tma_prefetch_3d(&p.tm_n, xb0, y_band, z);
         if (!DEFER && has_u) tma_prefetch_3d(&p.tm_u, xb0, y_band, z);
