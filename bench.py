@@ -465,7 +465,8 @@ def capture(launches, stream):
     return g
 
 
-# configs[1..4] of the measurement plan, timed in the same process as the headline
+# the target workloads (bcg B=16 4x128x128, area B=8 with 4 regions, inpaint B=32
+# 16x128x128, the throughput sweep B=64), timed in the same process as the headline
 TARGET_WORKLOADS = ("bcg_bf16_b16", "area_fp16_b8", "inpaint_bcg_bf16_b32", "sweep_bf16_b64")
 # floor on the steps of each per-workload timing: a short timed region would be
 # dominated by the graph launch around it
