@@ -42,7 +42,7 @@ typedef struct CUstream_st* gs_stream;
 typedef enum gs_status {
     GS_OK = 0,
     GS_ERR_INVALID_ARG = 1,   /* a pointer, size, rectangle or option is invalid      */
-    GS_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve                */
+    GS_ERR_UNSUPPORTED = 2,   /* a valid request the library cannot serve             */
     GS_ERR_CUDA = 3,          /* the CUDA runtime reported an error (launch, device)  */
     GS_ERR_STEP_RANGE = 4,    /* device: a step index did not address sigma[i], sigma[i+1]
                                  (or the scale table); that sample was skipped        */
